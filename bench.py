@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact tiled attention forward on one GB300 (or N replicas).
+
+One step = the attention of a 511-token causal prefill through 28 layers:
+28 calls of fa_fwd (bf16, B=1, Hq=16, Hkv=8, d=128, Tq=Tk=511), each layer
+with its own seeded synthetic Q/K/V (seeds 0..27), all resident in HBM.
+
+value     causal-adjusted TFLOP/s over the K timed steps: 4*d*(visible
+          query-key pairs) per call, summed over the 28 calls, divided by
+          the device time (CUDA events on the launching stream).  The 28
+          calls are replayed from a CUDA graph; L2 is flushed (a 256 MiB
+          write) before every timed step, outside the events.
+e2e       the same metric through the public call with host buffers: every
+          step copies the 28 layers' Q/K/V from pinned host memory, runs the
+          28 calls and copies O and lse back, all inside the events.
+roofline  the dominant kernel (the bf16 tcgen05 kernel) against the measured
+          dense bf16 tensor peak: algorithmic FLOPs per launch / average
+          launch duration (step time / 28 launches, so launch gaps count).
+cpu_baseline  the float64 oracle on the host cores on a bounded sample.
+
+--impl reference times the oracle itself (the only reference there is) on
+the host cores, each step one layer of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+import workloads  # noqa: E402
+
+WORKLOAD = "prefill511_gqa16x8_d128_x28"
+METRIC = "attention fwd TFLOP/s (causal-adj) and % of GB300 dense peak; ms per prefill"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+LONG_CONTEXT = ["longctx2044_gqa16x8_d128", "longctx8192_gqa16x8_d128", "longctx32768_gqa16x8_d128"]
+
+
+def _peaks():
+    try:
+        with open(os.path.join(_ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        under_load = [s for s in sm if smax and s >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(under_load) if under_load else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in self.rows)}
+
+
+# ------------------------------------------------------------------ oracle
+
+def time_oracle_layers(max_seconds: float, max_layers: int = 28):
+    """Oracle over whole layers of the workload until ``max_seconds`` pass.
+    Returns (flops, seconds, layers, threads)."""
+    import torch
+    import oracle
+    p = workloads.CONFIGS[WORKLOAD].problem
+    threads = os.cpu_count() or 1
+    orc = oracle.get()
+    flops, secs, layers = 0, 0.0, 0
+    while layers < max_layers and (layers == 0 or secs < max_seconds):
+        q, k, v = workloads.qkv(layers, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
+        qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+        t0 = time.perf_counter()
+        orc.attention(qn, kn, vn, p.sm_scale, causal=True, threads=threads)
+        secs += time.perf_counter() - t0
+        flops += p.flops()
+        layers += 1
+    return flops, secs, layers, threads
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one layer of the
+    workload (full rows) on all host cores."""
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    p = workloads.CONFIGS[WORKLOAD].problem
+    orc = oracle.get()
+    threads = os.cpu_count() or 1
+    inputs = []
+    for layer in range(min(28, args.warmup + args.steps)):
+        q, k, v = workloads.qkv(layer, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
+        inputs.append((q.float().numpy(), k.float().numpy(), v.float().numpy()))
+    times = []
+    for s in range(args.warmup + args.steps):
+        qn, kn, vn = inputs[s % len(inputs)]
+        t0 = time.perf_counter()
+        orc.attention(qn, kn, vn, p.sm_scale, causal=True, threads=threads)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    flops = p.flops() * len(times)
+    value = flops / total / 1e12
+    sample = f"one layer per step (B=1, Hq=16, Hkv=8, T=511, d=128, causal, all rows), float64 oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": 1, "Hq": 16, "Hkv": 8, "T": 511, "d": 128, "causal": True,
+                   "step": "1 of the 28 layers (float64 oracle on host cores)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- GPU
+
+def run_fa(args, rank, world, local_rank):
+    import torch
+    import exact_tiled_attention_flashattention_gb300 as fa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    p = workloads.CONFIGS[WORKLOAD].problem
+    L = 28
+    layers_host, layers_dev, outs = [], [], []
+    for layer in range(L):
+        q, k, v = workloads.qkv(layer, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
+        layers_host.append((q.pin_memory(), k.pin_memory(), v.pin_memory()))
+        layers_dev.append((q.to(dev), k.to(dev), v.to(dev)))
+        outs.append((torch.empty_like(layers_dev[-1][0]),
+                     torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)))
+    flops_call = p.flops()
+    flops_step = flops_call * L
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    def call(i, q, k, v, o, lse):
+        # stream=None: the binding takes torch's current stream at call time,
+        # which is the capture stream inside torch.cuda.graph().
+        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0, 0, 0,
+                  fa.FA_DTYPE_BF16, None)
+
+    def step():
+        for i in range(L):
+            q, k, v = layers_dev[i]
+            o, lse = outs[i]
+            call(i, q, k, v, o, lse)
+
+    # Eager warm-up (also configures kernel attributes before capture).
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    # The graph must hold the 28 launches: replay it on zeroed outputs.
+    outs[0][0].zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    if not bool(outs[0][0].abs().sum() > 0):
+        raise RuntimeError("CUDA graph capture recorded no attention launches")
+
+    sampler = ClockSampler(local_rank)
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    # Untimed soak so that clocks settle before the timed steps.
+    t_end = time.time() + args.soak
+    while time.time() < t_end:
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record()
+        graph.replay()
+        ev[s][1].record()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = sum(step_ms) / 1e3
+    if dist is not None:
+        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+        dist.barrier()
+    sampler.stop()
+
+    # End to end through the public call with host buffers.
+    host_out = [(torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
+                 torch.empty(l.shape, dtype=l.dtype, pin_memory=True)) for o, l in outs]
+    h2d = sum(t.numel() * t.element_size() for trio in layers_host for t in trio)
+    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in host_out)
+
+    def e2e_step():
+        for i in range(L):
+            qh, kh, vh = layers_host[i]
+            qd, kd, vd = layers_dev[i]
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            o, lse = outs[i]
+            call(i, qd, kd, vd, o, lse)
+            host_out[i][0].copy_(o, non_blocking=True)
+            host_out[i][1].copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    # Long-context causal prefill at T = 2044, 8192, 32768 (bf16), one call
+    # per measurement, L2 flushed before each.
+    peak_burst, peak_sustained, peak_kind = _peaks()
+    long_ctx = []
+    if not args.skip_long and rank == 0:
+        for name in LONG_CONTEXT:
+            w = workloads.CONFIGS[name]
+            lp = w.problem
+            q, k, v = workloads.qkv(w.seeds[0], lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, torch.bfloat16)
+            q, k, v = q.to(dev), k.to(dev), v.to(dev)
+            o = torch.empty_like(q)
+            lse = torch.empty((lp.B, lp.Hq, lp.Tq), dtype=torch.float32, device=dev)
+            reps = 20 if lp.Tq <= 8192 else 8
+            ms = []
+            for r in range(reps + 3):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fa.fa_fwd(q, k, v, o, lse, lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, lp.sm_scale, 0, 1, 0, None,
+                          None, 0, 0, 0, 0, fa.FA_DTYPE_BF16, None)
+                b.record()
+                torch.cuda.synchronize()
+                if r >= 3:
+                    ms.append(a.elapsed_time(b))
+            med = statistics.median(ms)
+            tf = lp.flops() / (med / 1e3) / 1e12
+            long_ctx.append({"workload": name, "T": lp.Tq, "ms": round(med, 4), "tflops": round(tf, 1),
+                             "frac_of_measured_peak": round(tf / peak_burst, 4)})
+            del q, k, v, o, lse
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        fl, secs, nl, thr = time_oracle_layers(args.cpu_seconds)
+        cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"layers 0..{nl - 1} of 28 of the same workload, all rows, float64 oracle "
+                         f"({secs:.1f} s)"}
+
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    traffic = None
+    prof = os.path.join(_ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                traffic = json.load(f).get(WORKLOAD)
+        except Exception:
+            traffic = None
+    avg_launch_s = (total_s / args.steps) / L
+    achieved = flops_call / avg_launch_s / 1e12
+    value = world * flops_step * args.steps / total_s / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "T": p.Tq, "d": p.d, "causal": True,
+                   "layers_per_step": L, "flops_per_step": flops_step, "launch": "CUDA graph of 28 fa_fwd calls",
+                   "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * flops_step * args.steps / e2e_s / 1e12, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(1e3 * e2e_s / args.steps, 4)},
+        "gpu_launches": L * args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_burst, 4), "traffic": traffic,
+                     "kernel": "fa_fwd_bf16_kernel<128>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
+        "clocks": sampler.summary(),
+        "long_context": long_ctx,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_only(args, local_rank):
+    """Profiling driver: ``--calls`` launches of one workload's first call
+    (inputs resident, nothing printed but a line of timings)."""
+    import torch
+    import exact_tiled_attention_flashattention_gb300 as fa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = workloads.CONFIGS[args.only]
+    p = w.problem
+    dt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
+    q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, dt)
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)
+    ms = []
+    for _ in range(args.calls):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, int(p.causal), p.window, None,
+                  None, 0, 0, 0, 0, fa.FA_DTYPE_BF16 if args.dtype == "bf16" else fa.FA_DTYPE_F32,
+                  torch.cuda.current_stream())
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    print(json.dumps({"only": args.only, "dtype": args.dtype, "ms": [round(x, 4) for x in ms],
+                      "tflops_last": p.flops() / (ms[-1] / 1e3) / 1e12}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fa", "reference"], default="fa")
+    ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of replays before timing")
+    ap.add_argument("--skip-long", action="store_true", help="skip the long-context measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=sorted(workloads.CONFIGS), help="profiling driver: one workload only")
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.only:
+        run_only(args, local_rank)
+    elif args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_fa(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,122 @@
+"""Python binding of libfa (the C ABI declared in include/fa.h).
+
+Argument marshalling only: every step of the attention forward runs in the
+CUDA kernels of ``libfa.so``.  There is no CPU fallback; importing the binding
+without the built library raises.
+
+``fa_fwd`` mirrors the C entry point name for name.  Tensor arguments may be
+torch tensors (their ``data_ptr()`` is passed) or integer device addresses;
+``stream`` may be a ``torch.cuda.Stream``, an integer handle or None (the
+current torch stream).  ``attention`` is a convenience wrapper that allocates
+``o`` and ``lse`` with torch and calls ``fa_fwd``.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+__all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_DTYPE_F32", "FA_DTYPE_BF16",
+           "FaError", "fa_fwd", "fa_last_error", "fa_version", "attention", "library_path", "load"]
+
+FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA = 0, 1, 2, 3, 4
+FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
+_STATUS = {0: "FA_OK", 1: "FA_EINVAL", 2: "FA_ESHAPE", 3: "FA_EUNSUPPORTED", 4: "FA_ECUDA"}
+
+_LIB_PATH = Path(__file__).resolve().parent / "libfa.so"
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def load():
+    """Load libfa.so (built by the repository's build step) and declare its
+    signatures.  Raises if the library has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _LIB_PATH.exists():
+        raise ImportError(f"{_LIB_PATH} is missing: build the CUDA library first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_float, i64, ctypes.c_int,
+                           i64, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.fa_last_error.restype = ctypes.c_char_p
+    lib.fa_last_error.argtypes = []
+    lib.fa_version.restype = ctypes.c_int
+    lib.fa_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    return x.data_ptr() or None
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+def fa_last_error() -> str:
+    return load().fa_last_error().decode()
+
+
+def fa_version() -> int:
+    return load().fa_version()
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, scale, q_offset, causal, window, sinks, mask, mask_sb,
+           mask_sh, mask_sq, mask_sk, dtype, stream=None, *, check=True) -> int:
+    """Call the C entry point; raises FaError on a non-OK status when ``check``."""
+    lib = load()
+    st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(Tq), int(Tk),
+                    int(d), float(scale), int(q_offset), int(bool(causal)), int(window), _ptr(sinks), _ptr(mask),
+                    int(mask_sb), int(mask_sh), int(mask_sq), int(mask_sk), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=None, mask=None,
+              mask_strides=(0, 0, 0, 0), with_lse=True, out=None, lse_out=None, stream=None):
+    """o [B,Hq,Tq,d] (q's dtype) and lse [B,Hq,Tq] (fp32) for CUDA tensors
+    q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (fp32 or bf16, contiguous).  ``mask`` is
+    an fp32 CUDA tensor addressed with ``mask_strides`` (elements)."""
+    import torch
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    if q.dtype == torch.float32:
+        dt = FA_DTYPE_F32
+    elif q.dtype == torch.bfloat16:
+        dt = FA_DTYPE_BF16
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k and v must be contiguous")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share a dtype")
+    o = out if out is not None else torch.empty_like(q)
+    lse = lse_out if lse_out is not None else (
+        torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if with_lse else None)
+    sc = (1.0 / d ** 0.5) if scale is None else scale
+    fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, sc, q_offset, causal, window, sinks, mask, *mask_strides, dt,
+           stream)
+    return o, lse

@@ -1,0 +1,37 @@
+// fa_internal.h -- parameters shared by the host layer and the kernels.
+// Not part of the public ABI (include/fa.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// One validated call of fa_fwd, in the form the kernels read it.
+struct Params {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;           // [B, Hq, Tq] or nullptr
+    const float *sinks;   // [Hq] or nullptr
+    const float *mask;    // strided, or nullptr
+    int64_t msb, msh, msq, msk;
+    int B, Hq, Hkv, Tq, Tk, d;
+    int group;            // Hq / Hkv
+    int q_offset;         // absolute position of query row 0
+    int causal;
+    int window;           // <= 0: none (clamped to int range by the host)
+    float scale;          // scale applied to q.k
+    float scale_log2;     // scale * log2(e)
+};
+
+// Visible key range [lo, hi) of query position p (absolute), before the mask.
+__host__ __device__ inline void visible_range(const Params &P, int64_t p, int64_t &lo, int64_t &hi) {
+    hi = P.causal ? (p + 1 < (int64_t)P.Tk ? p + 1 : (int64_t)P.Tk) : (int64_t)P.Tk;
+    lo = P.window > 0 ? (p - P.window + 1 > 0 ? p - P.window + 1 : 0) : 0;
+    if (hi < lo) hi = lo;
+}
+
+cudaError_t launch_f32(const Params &P, cudaStream_t stream);
+cudaError_t launch_bf16(const Params &P, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,101 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact tiled attention forward.
+ *
+ * One call computes, for every batch b, query head h and query row i,
+ *
+ *   o[b,h,i,:] = sum_{j in V_i} e^{s_ij} v_j / ( sum_{j in V_i} e^{s_ij} + e^{z_h} )
+ *   lse[b,h,i] = log( sum_{j in V_i} e^{s_ij} + e^{z_h} )
+ *   s_ij       = scale * q_i . k_j + mask[b,h,i,j]
+ *   V_i        = { j < Tk : (causal == 0 or j <= p_i) and (window <= 0 or j > p_i - window) }
+ *   p_i        = q_offset + i
+ *
+ * as defined on "FlashAttention forward in C" (section 2.1, "What is
+ * computed", and section 4, "The interface") with the strided additive mask of
+ * "Fused attention and softmax: fast and exact" ("What is computed").  The
+ * e^{z_h} term is present only when sinks are given.  Query head h reads KV
+ * head floor(h / (Hq / Hkv)).  A row with no visible key (after the mask) and
+ * no sink gives o = 0 and lse = -inf; with a sink it gives o = 0 and lse = z_h.
+ * The [Tq, Tk] score matrix is never stored: keys are walked one tile at a
+ * time under an online softmax ("FlashAttention forward in C", section 2.2).
+ *
+ * Layout (all tensors contiguous, row-major, element strides implied):
+ *   q, o   [B, Hq,  Tq, d]   in `dtype`
+ *   k, v   [B, Hkv, Tk, d]   in `dtype`
+ *   lse    [B, Hq,  Tq]      float32, or NULL to skip it
+ *   sinks  [Hq]              float32 raw logits (not scaled, not masked), or NULL
+ *   mask   float32, element (b,h,i,j) at mask[b*mask_sb + h*mask_sh + i*mask_sq + j*mask_sk];
+ *          strides in elements, >= 0, a stride of 0 broadcasts; NULL for no mask.
+ *          Entries may be finite or -inf; +inf and NaN are outside the domain.
+ * All pointers are DEVICE pointers on the current CUDA device.  q, k, v and o
+ * must be 16-byte aligned.  The caller owns every buffer; the library keeps
+ * no state between calls beyond cached kernel attributes and allocates no
+ * device memory.
+ *
+ * Arithmetic: FA_DTYPE_F32 computes in fp32 on the SIMT cores (FFMA) and
+ * writes fp32 o.  FA_DTYPE_BF16 reads bf16 q/k/v, forms S = Q K^T and O = P V
+ * on the tcgen05 tensor cores with fp32 accumulators in tensor memory, keeps
+ * the softmax statistics in fp32, rounds P to bf16 for the P.V product, and
+ * writes bf16 o (round to nearest even).  lse is fp32 in both.
+ *
+ * Execution: asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ * stream); results are valid once the stream has synchronised.
+ *
+ * Errors are reported before any launch and before anything is written:
+ *   FA_EINVAL        negative sizes or q_offset, a NULL q/o when B*Hq*Tq > 0,
+ *                    a NULL k/v when Tk > 0 (and B*Hq*Tq > 0), an unknown
+ *                    dtype, a non-finite scale, a negative mask stride, sizes
+ *                    whose element counts overflow.
+ *   FA_ESHAPE        Hq % Hkv != 0, Hkv > Hq, or Hkv == 0 with Hq > 0
+ *                    ("FlashAttention forward in C", section 4: TL_ESHAPE).
+ *   FA_EUNSUPPORTED  d odd or 0 ("Fused attention and softmax": d must be
+ *                    even), d > 256 for fp32, bf16 d not in {64, 128},
+ *                    Tq or Tk >= 2^30, pointers not 16-byte aligned.
+ *   FA_ECUDA         a CUDA error while configuring or launching.
+ * B*Hq*Tq == 0 is a no-op returning FA_OK.  Tk == 0 writes o = 0 and
+ * lse = -inf (or the sink).  fa_last_error() describes the last non-OK
+ * status returned on the calling thread.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_EINVAL = 1,
+    FA_ESHAPE = 2,
+    FA_EUNSUPPORTED = 3,
+    FA_ECUDA = 4
+} fa_status;
+
+typedef enum {
+    FA_DTYPE_F32 = 0,
+    FA_DTYPE_BF16 = 1
+} fa_dtype;
+
+/* The attention forward described above.  `dtype` is an fa_dtype value;
+ * `stream` is a cudaStream_t passed as void* so that this header needs no
+ * CUDA include. */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d,
+                 float scale, int64_t q_offset, int causal, int64_t window,
+                 const float *sinks,
+                 const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk,
+                 int dtype, void *stream);
+
+/* Message for the last non-OK status on this thread ("" if none).  The
+ * pointer stays valid until the next fa_* call on the same thread. */
+const char *fa_last_error(void);
+
+/* ABI version of this library (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

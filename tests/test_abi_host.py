@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI: the library loads, exports what
+include/fa.h declares, and rejects bad arguments before touching anything.
+
+No GPU is needed: every call below fails validation (or is a no-op) before
+any CUDA call, and ``o``/``lse`` are host canary buffers that must stay
+untouched ("FlashAttention forward in C", section 4: errors before any write).
+"""
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import exact_tiled_attention_flashattention_gb300 as fa
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+def _declared_functions():
+    text = (ROOT / "include" / "fa.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return fa.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert "fa_fwd" in names and "fa_last_error" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", str(fa.library_path())], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert fa.fa_version() >= 100
+
+
+class Canary:
+    """Host buffers standing in for o and lse; any write would show."""
+
+    def __init__(self, n=4096):
+        self.o = np.full(n, 12345.0, dtype=np.float32)
+        self.lse = np.full(n, 6789.0, dtype=np.float32)
+        self.q = np.zeros(n, dtype=np.float32)
+
+    def ptrs(self):
+        return self.q.ctypes.data, self.o.ctypes.data, self.lse.ctypes.data
+
+    def untouched(self):
+        return bool(np.all(self.o == 12345.0) and np.all(self.lse == 6789.0))
+
+
+def _call(c, **kw):
+    q, o, lse = c.ptrs()
+    args = dict(q=q, k=q, v=q, o=o, lse=lse, B=1, Hq=2, Hkv=1, Tq=4, Tk=4, d=8, scale=0.5, q_offset=0, causal=1,
+                window=0, sinks=None, mask=None, mask_sb=0, mask_sh=0, mask_sq=0, mask_sk=0, dtype=fa.FA_DTYPE_F32)
+    args.update(kw)
+    return fa.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["Hq"], args["Hkv"],
+                     args["Tq"], args["Tk"], args["d"], args["scale"], args["q_offset"], args["causal"],
+                     args["window"], args["sinks"], args["mask"], args["mask_sb"], args["mask_sh"], args["mask_sq"],
+                     args["mask_sk"], args["dtype"], 0, check=False)
+
+
+CASES = [
+    ("unknown dtype", dict(dtype=7), fa.FA_EINVAL),
+    ("negative B", dict(B=-1), fa.FA_EINVAL),
+    ("negative Tq", dict(Tq=-3), fa.FA_EINVAL),
+    ("negative Tk", dict(Tk=-1), fa.FA_EINVAL),
+    ("negative d", dict(d=-8), fa.FA_EINVAL),
+    ("negative q_offset", dict(q_offset=-1), fa.FA_EINVAL),
+    ("nan scale", dict(scale=float("nan")), fa.FA_EINVAL),
+    ("inf scale", dict(scale=float("inf")), fa.FA_EINVAL),
+    ("null q", dict(q=None), fa.FA_EINVAL),
+    ("null o", dict(o=None), fa.FA_EINVAL),
+    ("null k with Tk > 0", dict(k=None), fa.FA_EINVAL),
+    ("null v with Tk > 0", dict(v=None), fa.FA_EINVAL),
+    ("negative mask stride", dict(mask=1 << 20, mask_sq=-4), fa.FA_EINVAL),
+    ("overflowing sizes", dict(B=1 << 40, Hq=1 << 20, Hkv=1 << 20, Tq=1 << 20), fa.FA_EINVAL),
+    ("6 heads on 4 KV heads", dict(Hq=6, Hkv=4), fa.FA_ESHAPE),
+    ("Hkv > Hq", dict(Hq=2, Hkv=4), fa.FA_ESHAPE),
+    ("Hkv = 0", dict(Hkv=0), fa.FA_ESHAPE),
+    ("odd d", dict(d=7), fa.FA_EUNSUPPORTED),
+    ("zero d", dict(d=0), fa.FA_EUNSUPPORTED),
+    ("fp32 d > 256", dict(d=258), fa.FA_EUNSUPPORTED),
+    ("bf16 d = 96", dict(d=96, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
+    ("bf16 d = 32", dict(d=32, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
+    ("Tk >= 2^30", dict(Tk=1 << 30), fa.FA_EUNSUPPORTED),
+    ("Tq >= 2^30", dict(Tq=1 << 30, B=1, Hq=1, Hkv=1, d=2), fa.FA_EUNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,expected", CASES, ids=[c[0] for c in CASES])
+def test_rejected_before_any_write(lib, name, kw, expected):
+    c = Canary()
+    st = _call(c, **kw)
+    assert st == expected, (name, st, fa.fa_last_error())
+    assert fa.fa_last_error(), "a non-OK status must leave a message"
+    assert c.untouched()
+
+
+def test_unaligned_pointer_rejected(lib):
+    c = Canary()
+    q, o, lse = c.ptrs()
+    st = _call(c, q=q + 4)
+    assert st == fa.FA_EUNSUPPORTED and c.untouched()
+    st = _call(c, o=o + 8)
+    assert st == fa.FA_EUNSUPPORTED and c.untouched()
+
+
+@pytest.mark.parametrize("kw", [dict(Tq=0), dict(B=0), dict(Hq=0, Hkv=0)])
+def test_empty_problem_is_a_no_op(lib, kw):
+    c = Canary()
+    st = _call(c, **kw)
+    assert st == fa.FA_OK and c.untouched()
+
+
+def test_binding_raises_on_error(lib):
+    c = Canary()
+    q, o, lse = c.ptrs()
+    with pytest.raises(fa.FaError) as ei:
+        fa.fa_fwd(q, q, q, o, lse, 1, 6, 4, 4, 4, 8, 0.5, 0, 1, 0, None, None, 0, 0, 0, 0, fa.FA_DTYPE_F32, 0)
+    assert ei.value.status == fa.FA_ESHAPE
+    assert c.untouched()

@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Every workload shape of the method's statement is covered, in the launch
+configuration the benchmark times, plus tile-edge sweeps and degenerate
+cases.  Rows are compared element by element; at T = 8192 and 32768 on a
+deterministic row sample (first 256, last 256, every 127th row).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import compare, gpu_attention, oracle_attention, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _run_and_compare(q, k, v, dtype, ctx, rows=None, **kw):
+    o, lse = gpu_attention(q, k, v, **kw)
+    eo, el = oracle_attention(q, k, v, rows=rows, **kw)
+    if rows is not None:
+        o, lse = o[:, :, rows], lse[:, :, rows]
+    return compare(o, lse, eo, el, dtype, ctx)
+
+
+# ------------------------------------------------------------------ workloads
+
+def test_tile_crossing_d64_f32():
+    w = workloads.CONFIGS["tile_crossing_d64"]
+    p = w.problem
+    q, k, v = workloads.qkv(0, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float32)
+    _run_and_compare(q, k, v, torch.float32, "tile_crossing", scale=1.0 / 8.0, causal=True)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_prefill511_28_layers(dt):
+    p = workloads.CONFIGS["prefill511_gqa16x8_d128_x28"].problem
+    rows = np.arange(0, p.Tq, 7, dtype=np.int64)
+    for layer in range(28):
+        q, k, v = workloads.qkv(layer, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, DT[dt])
+        full = layer in (0, 27)
+        _run_and_compare(q, k, v, DT[dt], f"prefill511 {dt} layer {layer}", rows=None if full else rows,
+                         scale=p.sm_scale, causal=True)
+
+
+@pytest.mark.parametrize("name", ["longctx2044_gqa16x8_d128", "longctx8192_gqa16x8_d128",
+                                  "longctx32768_gqa16x8_d128"])
+def test_long_context_bf16(name):
+    w = workloads.CONFIGS[name]
+    p = w.problem
+    q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
+    rows = None if p.Tq <= 2044 else sample_rows(p.Tq)
+    _run_and_compare(q, k, v, torch.bfloat16, name, rows=rows, scale=p.sm_scale, causal=True)
+
+
+def _chunked(q, k, v, sinks, p, chunk):
+    """Feed the prompt as chunks with q_offset; keys so far per chunk."""
+    outs, lses = [], []
+    for start, n in workloads.chunk_ranges(p.Tq, chunk):
+        qc = q[:, :, start:start + n].contiguous()
+        kc = k[:, :, :start + n].contiguous()
+        vc = v[:, :, :start + n].contiguous()
+        o, lse = gpu_attention(qc, kc, vc, scale=p.sm_scale, q_offset=start, causal=True, window=p.window,
+                               sinks=sinks)
+        outs.append(o)
+        lses.append(lse)
+    return torch.cat(outs, dim=2), torch.cat(lses, dim=2)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_window_sinks_chunked(dt):
+    w = workloads.CONFIGS["window128_sinks_gqa32x4_d64_chunked"]
+    p = w.problem
+    q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, DT[dt])
+    z = workloads.sinks(w.extra["sink_seed"], p.Hq)
+    oc, lc = _chunked(q, k, v, z, p, w.extra["chunk"])
+    eo, el = oracle_attention(q, k, v, scale=p.sm_scale, causal=True, window=p.window, sinks=z)
+    compare(oc, lc, eo, el, DT[dt], f"window/sinks chunked {dt}")
+    # Bitwise chunk invariance: the same rows in one call.
+    o1, l1 = gpu_attention(q, k, v, scale=p.sm_scale, causal=True, window=p.window, sinks=z)
+    assert torch.equal(o1, oc), "chunked o differs from the single call"
+    assert torch.equal(l1, lc), "chunked lse differs from the single call"
+    # Weights sum to 1 - p_sink: with V == 1 every component is 1 - e^{z_h - lse}.
+    ones = torch.ones_like(v)
+    o2, l2 = gpu_attention(q, k, ones, scale=p.sm_scale, causal=True, window=p.window, sinks=z)
+    psink = torch.exp(z.double().view(1, -1, 1) - l2.double())
+    err = (o2.double() - (1.0 - psink)[..., None]).abs().max().item()
+    assert err <= (1e-5 if dt == "f32" else 8e-3), err
+
+
+def test_mask_batch_f32():
+    w = workloads.CONFIGS["mask_b4h8_t1024_d96"]
+    p = w.problem
+    q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float32)
+    m = workloads.strided_mask(w.extra["mask_seed"], p.Tq, p.Tk)
+    strides = (0, 0, p.Tk, 1)
+    o, lse = gpu_attention(q, k, v, scale=p.sm_scale, causal=False, mask=m, mask_strides=strides)
+    eo, el = oracle_attention(q, k, v, scale=p.sm_scale, causal=False, mask=m, mask_strides=strides)
+    compare(o, lse, eo, el, torch.float32, "mask batch")
+    empty_rows = [0, 63, 64, 127, 500, 511, 512, 1023]
+    assert torch.all(torch.isneginf(lse[:, :, empty_rows]))
+    assert torch.all(o[:, :, empty_rows] == 0)
+
+
+# ---------------------------------------------------------------- tile edges
+
+EDGE_T = [1, 2, 63, 64, 65, 127, 128, 129, 130, 255, 257]
+
+
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
+def test_edges_f32(d):
+    for T in EDGE_T:
+        q, k, v = workloads.qkv(T + d, 1, 2, 1, T, T, d, torch.float32)
+        _run_and_compare(q, k, v, torch.float32, f"edge f32 T={T} d={d}", scale=1 / math.sqrt(d), causal=True)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_edges_bf16(d):
+    for T in EDGE_T:
+        q, k, v = workloads.qkv(T + d, 1, 2, 1, T, T, d, torch.bfloat16)
+        _run_and_compare(q, k, v, torch.bfloat16, f"edge bf16 T={T} d={d}", scale=1 / math.sqrt(d), causal=True)
+
+
+FLAG_CASES = [
+    # (Hq, Hkv, Tq, Tk, causal, window, q_offset, sinks, mask)
+    (6, 2, 37, 37, True, 0, 0, False, False),      # GQA 6:2 causal prefill
+    (6, 1, 37, 37, True, 0, 0, False, False),      # MQA
+    (4, 2, 13, 37, True, 0, 24, False, False),     # a chunk at q_offset 24
+    (4, 2, 37, 37, True, 6, 0, False, False),      # window 6
+    (4, 2, 37, 37, False, 6, 0, False, False),     # window without causal
+    (4, 4, 200, 300, False, 0, 0, False, False),   # plain, Tq != Tk
+    (4, 2, 150, 300, True, 0, 150, True, False),   # sinks
+    (4, 2, 150, 300, True, 50, 150, True, True),   # everything
+    (2, 1, 1, 300, True, 0, 299, False, False),    # one decode row
+    (2, 1, 5, 3, True, 2, 10, False, False),       # window excludes every key: empty rows
+    (2, 1, 5, 3, True, 2, 10, True, False),        # ... with a sink
+    (2, 2, 300, 140, False, 0, 0, False, True),    # mask only
+]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("case", FLAG_CASES, ids=[str(i) for i in range(len(FLAG_CASES))])
+def test_flags(dt, case):
+    Hq, Hkv, Tq, Tk, causal, window, q_offset, use_sink, use_mask = case
+    d = 64
+    q, k, v = workloads.qkv(17, 2, Hq, Hkv, Tq, Tk, d, DT[dt])
+    z = workloads.sinks(3, Hq) if use_sink else None
+    mask = strides = None
+    if use_mask:
+        g = torch.Generator().manual_seed(5)
+        mask = torch.randn((2, Hq, Tq, Tk), generator=g)
+        mask[torch.rand((2, Hq, Tq, Tk), generator=g) < 0.2] = -math.inf
+        strides = (Hq * Tq * Tk, Tq * Tk, Tk, 1)
+    _run_and_compare(q, k, v, DT[dt], f"flags {case} {dt}", scale=0.125, causal=causal, window=window,
+                     q_offset=q_offset, sinks=z, mask=mask, mask_strides=strides or (0, 0, 0, 0))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_no_keys(dt):
+    # Tk == 0: o = 0, lse = -inf, or the sink logit with sinks.
+    q, _, _ = workloads.qkv(1, 1, 4, 2, 9, 0, 64, DT[dt])
+    kz = torch.zeros((1, 2, 0, 64), dtype=DT[dt])
+    o, lse = gpu_attention(q, kz, kz, scale=0.125, causal=False)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    z = workloads.sinks(2, 4)
+    o, lse = gpu_attention(q, kz, kz, scale=0.125, causal=False, sinks=z)
+    assert torch.all(o == 0)
+    # lse = z_h up to the fp32 rounding of the log2-domain round trip
+    assert torch.allclose(lse, z.view(1, 4, 1).expand_as(lse), rtol=0, atol=1e-6)
