@@ -107,6 +107,29 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in self.rows)}
 
 
+def time_graph(fn, reps, flush, warm=3):
+    """Median device time (ms) of ``fn`` replayed from a CUDA graph, with L2
+    flushed before every replay; events bracket the replay only."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for r in range(reps + warm):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if r >= warm:
+            ms.append(a.elapsed_time(b))
+    return statistics.median(ms), ms
+
+
 # ------------------------------------------------------------------ oracle
 
 def time_oracle_layers(max_seconds: float, max_layers: int = 28):
@@ -296,18 +319,12 @@ def run_fa(args, rank, world, local_rank):
             o = torch.empty_like(q)
             lse = torch.empty((lp.B, lp.Hq, lp.Tq), dtype=torch.float32, device=dev)
             reps = 20 if lp.Tq <= 8192 else 8
-            ms = []
-            for r in range(reps + 3):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
+
+            def one_call():
                 fa.fa_fwd(q, k, v, o, lse, lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, lp.sm_scale, 0, 1, 0, None,
                           None, 0, 0, 0, 0, fa.FA_DTYPE_BF16, None)
-                b.record()
-                torch.cuda.synchronize()
-                if r >= 3:
-                    ms.append(a.elapsed_time(b))
-            med = statistics.median(ms)
+
+            med, _ = time_graph(one_call, reps, flush)
             tf = lp.flops() / (med / 1e3) / 1e12
             long_ctx.append({"workload": name, "T": lp.Tq, "ms": round(med, 4), "tflops": round(tf, 1),
                              "frac_of_measured_peak": round(tf / peak_burst, 4)})
@@ -375,18 +392,22 @@ def run_only(args, local_rank):
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)
-    ms = []
-    for _ in range(args.calls):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
+    def one_call():
         fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, int(p.causal), p.window, None,
-                  None, 0, 0, 0, 0, fa.FA_DTYPE_BF16 if args.dtype == "bf16" else fa.FA_DTYPE_F32,
-                  torch.cuda.current_stream())
-        b.record()
+                  None, 0, 0, 0, 0, fa.FA_DTYPE_BF16 if args.dtype == "bf16" else fa.FA_DTYPE_F32, None)
+
+    if args.calls <= 3:
+        # few launches (profiling): plain calls, no graph
+        for _ in range(args.calls):
+            one_call()
         torch.cuda.synchronize()
-        ms.append(a.elapsed_time(b))
-    print(json.dumps({"only": args.only, "dtype": args.dtype, "ms": [round(x, 4) for x in ms],
-                      "tflops_last": p.flops() / (ms[-1] / 1e3) / 1e12}), flush=True)
+        print(json.dumps({"only": args.only, "dtype": args.dtype, "calls": args.calls}), flush=True)
+        return
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    med, ms = time_graph(one_call, args.calls, flush)
+    print(json.dumps({"only": args.only, "dtype": args.dtype, "ms_median": round(med, 4),
+                      "ms": [round(x, 4) for x in ms], "tflops": round(p.flops() / (med / 1e3) / 1e12, 1)}),
+          flush=True)
 
 
 def main():

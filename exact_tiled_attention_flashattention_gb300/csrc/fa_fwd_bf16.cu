@@ -1,35 +1,67 @@
 // fa_fwd_bf16.cu -- bf16 exact tiled attention on the tcgen05 tensor cores.
 //
-// One CTA owns one (batch, query head, 128-row query tile).  The score tile
-// S = Q K_t^T (128 x 128, fp32) and the output accumulator O (128 x d, fp32)
-// live in tensor memory; Q, K_t and V_t are staged in shared memory by TMA
-// with the 128-byte swizzle that tcgen05.mma reads directly.  Each query row
-// keeps a running max m and denominator l in registers and the online softmax
-// of "FlashAttention forward in C" (section 2.2) rescales O in tensor memory
-// by 2^(m_old - m_new) when the max grows.  P = 2^(s - m) is rounded to bf16
-// and written back to tensor memory, where it is the A operand of O += P V_t.
+// A CTA owns one 128-row query tile of one (batch, query head).  It walks the
+// key tiles its rows can see, 128 keys at absolute positions [128t, 128t+128)
+// each, under the online softmax of "FlashAttention forward in C" (section
+// 2.2), in base 2 (c = scale * log2 e):
+//
+//   S_t = Q K_t^T          tcgen05.mma, Q from TMEM (A operand), K_t from
+//                          shared memory (TMA, 128-byte swizzle), fp32
+//                          accumulator in TMEM
+//   P_t = 2^(S_t c - m)    softmax warps: tcgen05.ld of S_t, row max, ex2,
+//                          row sum; P rounded to bf16 and tcgen05.st back into
+//                          the first 64 columns of S_t's buffer
+//   O  += P_t V_t          tcgen05.mma, A = P_t from TMEM, B = V_t (MN-major)
+//
+// S is double-buffered in tensor memory (S_A, S_B), so the issuer computes
+// S_{t+1} while the softmax warps work on S_t; the tensor core and the
+// softmax overlap and a tile costs about max(softmax, S + PV) rather than
+// their sum.  S_{t+2} reuses the buffer of P_t and is issued after
+// O += P_t V_t: tcgen05.mma operations issued by one thread execute in order.
+//
+// The running max m of a row is raised lazily: only when a tile's max
+// exceeds it by more than 8 (log2 units) is O rescaled in TMEM by
+// 2^(m_old - m_new); otherwise the row keeps the old m, its weights stay
+// below 2^8 and the final O / l is the same quantity.  The rescale guard
+// follows "Fused attention and softmax: fast and exact" (the exact
+// definition, steps 2 and 5).
+//
+// K/V sharing: when the GQA group size is even, the two query heads of a KV
+// head at the same rows run as a cluster of two CTAs.  Each CTA loads half of
+// every K/V tile (64 of its 128 rows) with a multicast TMA that lands in both
+// CTAs' shared memory, and a ring slot is refilled only after both CTAs'
+// tensor cores released it (a multicast tcgen05.commit arrives on the slot's
+// barrier in both CTAs).  Every K/V byte is then read from L2 once per pair,
+// which halves the L2 traffic that otherwise bounds long sequences.
+//
+// Q lives in tensor memory: each softmax thread loads its query row from
+// global memory once and stores it (bf16 pairs) into its TMEM lane, so the
+// shared-memory bandwidth goes to K and V only: per tile the tensor core
+// reads K (S MMAs) and V (P.V MMAs) and TMA writes both, 128 KB in all, which
+// the shared memory sustains within the tile's tensor-core time.
 //
 // Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t = tensor-memory lane t;
-//              scale, mask, row max, exponentials, P, O rescale, epilogue
-//   warp 4     TMA producer: Q once, then K_t / V_t into a 2-stage ring
-//   warp 5     MMA issuer (one lane) and tensor-memory owner
-// The issuer runs one tile ahead: S_{t+1} = Q K_{t+1}^T is computed (into the
-// second S buffer) while the softmax warps work on S_t, then O += P_t V_t.
+//   warps 0-3   softmax: thread t = query row t = TMEM lane t; Q load;
+//               epilogue
+//   warp 4      TMA producer: the K and V tiles in the order the tensor core
+//               consumes them (K_0, K_1, V_0, K_2, V_1, ...) into a ring of
+//               shared-memory stages
+//   warp 5      MMA issuer (one lane) and tensor-memory owner
+// Tensor memory (512 columns allocated): S_A [0,128) S_B [128,256)
+// O [256, 256+d) Q [384, 384+d/2).
 //
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256, 256+d),
-// P [384, 448) as bf16 pairs.
+// A row's arithmetic does not depend on its query tile or on chunking through
+// q_offset: key tiles are absolute, a key the row cannot see gets weight 0 and
+// leaves m, l and O unchanged ("FlashAttention forward in C", section 2.4).
 //
-// Key tiles sit at absolute positions [128t, 128t + 128); keys a row cannot
-// see get p = 0 and leave its m, l and O unchanged, so a row's bits do not
-// depend on its query tile or on chunking through q_offset ("FlashAttention
-// forward in C", section 2.4).  The rescale guard follows "Fused attention
-// and softmax: fast and exact" (the exact definition, steps 2 and 5).
+// Launch: programmatic dependent launch lets the CTA prologue (barriers,
+// tensor-memory allocation, descriptor prefetch) overlap the previous kernel
+// in the stream; griddepcontrol.wait orders every global access after it.
 //
 // Every mbarrier wait is bounded (two seconds of wall time); a wait that runs
-// out sets a CTA-wide abort flag and the device watchdog word, all roles leave
-// their loops, in-flight copies and MMAs are drained with bounded waits, and
-// tensor memory is released before the CTA exits.
+// out sets a CTA-wide abort flag and the device watchdog word, every role
+// leaves its loop, in-flight copies and MMAs are drained with bounded waits,
+// and tensor memory is released before the CTA exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -46,326 +78,535 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBM = 128;  // query rows per tile = tensor-memory lanes
+constexpr int kBM = 128;  // query rows per CTA = tensor-memory lanes
 constexpr int kBN = 128;  // keys per tile
-constexpr int kStages = 2;
 constexpr int kThreads = 192;
+constexpr int kWarpTma = 4, kWarpMma = 5;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384;
+__host__ __device__ constexpr uint32_t col_s(int buf) { return 128u * buf; }  // S_A, S_B (and P)
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColQ = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kSwRowBytes = 128;  // one swizzled row: 64 bf16
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay below 2^8
+constexpr uint32_t kSwRowBytes = 128;      // one swizzled row: 64 bf16
+constexpr int kMaxStages = 7;
 
+// The K/V ring: each stage holds the two tiles one issuer step consumes
+// (V_j and K_{j+2}; the first stage K_0 and K_1), so one barrier wait and one
+// release cover both.
 template <int D>
 struct SmemLayout {
-    static constexpr int kBoxes = D / 64;                       // 64-column TMA boxes per tile
-    static constexpr uint32_t kQBytes = kBM * D * 2;
+    static constexpr int kBoxes = D / 64;  // 64-column TMA boxes per tile
     static constexpr uint32_t kKVBytes = kBN * D * 2;
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kQBytes;
-    static constexpr uint32_t kV = kK + kStages * kKVBytes;
-    static constexpr uint32_t kBar = kV + kStages * kKVBytes;  // barriers after the tiles
-    static constexpr uint32_t kTotal = kBar + 256;
+    static constexpr uint32_t kStageBytes = 2 * kKVBytes;
+    static constexpr int kStages = D == 128 ? 3 : 7;  // 192 KB / 224 KB
+    static constexpr uint32_t kRing = 0;
+    static constexpr uint32_t kBar = kRing + kStages * kStageBytes;
+    static constexpr uint32_t kTotal = kBar + 512;
+    static_assert(kStages <= kMaxStages, "ring too deep");
 };
 
 struct Barriers {
-    uint64_t q_full;
-    uint64_t k_full[kStages];
-    uint64_t v_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t s_free[2];
-    uint64_t p_full;
-    uint64_t o_ready;
+    uint64_t q_full;  // Q stored in tensor memory by the softmax threads
+    uint64_t full[kMaxStages], empty[kMaxStages];  // the K/V ring
+    uint64_t s_full[2];                            // S_A, S_B written
+    uint64_t p_full[2];                            // P in S_A, S_B written
+    uint64_t o_done;                               // O += P_{n-2} V_{n-2} completed (once)
+    uint64_t o_final;                              // the last O += P V completed
     uint64_t mma_drain;
     uint32_t tmem_base;
     int abort;
 };
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
+// Work unit of one CTA: one query tile; heaviest tiles first (under a causal
+// rule the last tiles see the most keys).
+struct Unit {
+    int b, h, g, bh;
+    int r0;  // first query row
+    int t_begin, n_tiles;
+};
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const Params P) {
-    using L = SmemLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Barriers &bar = *reinterpret_cast<Barriers *>(smem + L::kBar);
-    volatile int *abort = &bar.abort;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // Work unit: heaviest query tiles first (under a causal rule the last
-    // tiles see the most keys).
-    const int BH = P.B * P.Hq;
+template <int PAIR>
+__device__ __forceinline__ Unit decode_unit(const Params &P) {
+    Unit u;
     const int nqt = (P.Tq + kBM - 1) / kBM;
-    const int qt = nqt - 1 - (int)(blockIdx.x / BH);
-    const int bh = (int)(blockIdx.x % BH);
-    const int b = bh / P.Hq, h = bh % P.Hq, g = h / P.group;
-    const int r0 = qt * kBM;
-    const int64_t p_first = (int64_t)P.q_offset + r0;
-    const int64_t p_last = (int64_t)P.q_offset + min(r0 + kBM, P.Tq) - 1;
-    int64_t lo_a, hi_a, lo_b, hi_b;
-    visible_range(P, p_first, lo_a, hi_a);
-    visible_range(P, p_last, lo_b, hi_b);
-    const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
-    const int t_begin = (int)(klo / kBN);
-    const int n_tiles = khi > klo ? (int)((khi + kBN - 1) / kBN) - t_begin : 0;
-
-    if (threadIdx.x == 0) {
-        mbar_init(&bar.q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar.k_full[s], 1);
-            mbar_init(&bar.v_full[s], 1);
-            mbar_init(&bar.kv_empty[s], 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar.s_full[s], 1);
-            mbar_init(&bar.s_free[s], kBM);
-        }
-        mbar_init(&bar.p_full, kBM);
-        mbar_init(&bar.o_ready, 1);
-        mbar_init(&bar.mma_drain, 1);
-        bar.abort = 0;
-        mbar_init_fence();
-    }
-    if (warp == 5) {
-        tmem_alloc(&bar.tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = bar.tmem_base;
-
-    if (warp == 4) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0 && n_tiles > 0) {
-            const int kv_head = b * P.Hkv + g;
-            mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
-#pragma unroll
-            for (int c = 0; c < L::kBoxes; ++c)
-                tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, r0, bh);
-            int issued[kStages] = {};
-            for (int jj = 0; jj < n_tiles; ++jj) {
-                const int st = jj % kStages, u = jj / kStages;
-                if (u > 0 && !mbar_wait(&bar.kv_empty[st], (u - 1) & 1, abort)) break;
-                const int key0 = (t_begin + jj) * kBN;
-                mbar_arrive_expect_tx(&bar.k_full[st], L::kKVBytes);
-#pragma unroll
-                for (int c = 0; c < L::kBoxes; ++c)
-                    tma_load_3d(smem + L::kK + st * L::kKVBytes + c * (kBN * kSwRowBytes), &tmK, &bar.k_full[st],
-                                c * 64, key0, kv_head);
-                mbar_arrive_expect_tx(&bar.v_full[st], L::kKVBytes);
-#pragma unroll
-                for (int c = 0; c < L::kBoxes; ++c)
-                    tma_load_3d(smem + L::kV + st * L::kKVBytes + c * (kBN * kSwRowBytes), &tmV, &bar.v_full[st],
-                                c * 64, key0, kv_head);
-                ++issued[st];
-            }
-            if (*abort) {
-                // Drain: let every copy this thread issued land before the
-                // CTA (and its shared memory) goes away.
-                int never = 0;
-                mbar_wait(&bar.q_full, 0, &never, 200000000ull);
-                for (int s = 0; s < kStages; ++s)
-                    if (issued[s] > 0) {
-                        mbar_wait(&bar.k_full[s], (issued[s] - 1) & 1, &never, 200000000ull);
-                        mbar_wait(&bar.v_full[s], (issued[s] - 1) & 1, &never, 200000000ull);
-                    }
-            }
-        }
-    } else if (warp == 5) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && n_tiles > 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q, K both K-major
-            constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, 0, 1);    // P from TMEM, V MN-major
-            const uint32_t q_addr = smem_u32(smem + L::kQ);
-            if (mbar_wait(&bar.q_full, 0, abort)) {
-                for (int jj = 0; jj <= n_tiles; ++jj) {
-                    if (jj < n_tiles) {
-                        const int st = jj % kStages, sb = jj & 1;
-                        if (!mbar_wait(&bar.k_full[st], (jj / kStages) & 1, abort)) break;
-                        if (jj >= 2 && !mbar_wait(&bar.s_free[sb], ((jj - 2) >> 1) & 1, abort)) break;
-                        tc_fence_after();
-                        const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kKVBytes);
-                        const uint32_t d_tmem = tbase + (sb ? kColS1 : kColS0);
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * (kBM * kSwRowBytes) + (kk & 3) * 32;
-                            const uint64_t a = smem_desc_sw128(q_addr + off, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(k_addr + (kk >> 2) * (kBN * kSwRowBytes) + (kk & 3) * 32,
-                                                                16, 1024);
-                            mma_ss(d_tmem, a, bd, kIdS, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bar.s_full[sb]);
-                    }
-                    if (jj >= 1) {
-                        const int pj = jj - 1, st = pj % kStages;
-                        if (!mbar_wait(&bar.p_full, pj & 1, abort)) break;
-                        if (!mbar_wait(&bar.v_full[st], (pj / kStages) & 1, abort)) break;
-                        tc_fence_after();
-                        const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kKVBytes);
-#pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk) {
-                            // 16 keys = two 8-row swizzle atoms; the next 64
-                            // value columns sit one TMA box further on.
-                            const uint64_t bd = smem_desc_sw128(v_addr + kk * 16 * kSwRowBytes,
-                                                                kBN * kSwRowBytes, 1024);
-                            mma_ts(tbase + kColO, tbase + kColP + kk * 8, bd, kIdO, (pj > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&bar.o_ready);
-                        mma_commit(&bar.kv_empty[st]);
-                    }
-                }
-            }
-            // Every MMA issued above completes before tensor memory is freed.
-            mma_commit(&bar.mma_drain);
-            int never = 0;
-            mbar_wait(&bar.mma_drain, 0, &never, 200000000ull);
-        }
+    int qt;
+    if (PAIR == 2) {
+        // CTAs 2k and 2k+1 (one cluster) take query heads 2h' and 2h'+1 of one
+        // KV group at the same rows.
+        const int pairs = P.B * (P.Hq / 2);
+        const int unit = (int)(blockIdx.x >> 1);
+        qt = nqt - 1 - unit / pairs;
+        const int pr = unit % pairs;
+        u.b = pr / (P.Hq / 2);
+        u.h = 2 * (pr % (P.Hq / 2)) + (int)(blockIdx.x & 1);
+        u.bh = u.b * P.Hq + u.h;
     } else {
-        // ------------------------------------------------- softmax warps 0-3
-        const int row = threadIdx.x;  // query row within the tile = TMEM lane
-        const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
-        const int i = r0 + row;
-        const int64_t p = (int64_t)P.q_offset + i;
-        const bool has_sink = P.sinks != nullptr;
-        float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;
-        float l = has_sink ? 1.f : 0.f;
-        const float *mrow = P.mask ? P.mask + b * P.msb + h * P.msh + (int64_t)i * P.msq : nullptr;
-        bool ok = true;
+        const int BH = P.B * P.Hq;
+        qt = nqt - 1 - (int)(blockIdx.x / BH);
+        u.bh = (int)(blockIdx.x % BH);
+        u.b = u.bh / P.Hq;
+        u.h = u.bh % P.Hq;
+    }
+    u.g = u.h / P.group;
+    u.r0 = qt * kBM;
+    int64_t lo_a, hi_a, lo_b, hi_b;
+    visible_range(P, (int64_t)P.q_offset + u.r0, lo_a, hi_a);
+    visible_range(P, (int64_t)P.q_offset + min(u.r0 + kBM, P.Tq) - 1, lo_b, hi_b);
+    const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
+    if (khi > klo) {
+        u.t_begin = (int)(klo / kBN);
+        u.n_tiles = (int)((khi + kBN - 1) / kBN) - u.t_begin;
+    } else {
+        u.t_begin = 0;
+        u.n_tiles = 0;
+    }
+    return u;
+}
 
-        for (int jj = 0; jj < n_tiles && ok; ++jj) {
-            const int sb = jj & 1;
-            // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[sb], (jj >> 1) & 1, abort))) {
+// Position in the K/V ring: stage index and the parity of its current use.
+// Items are produced and consumed strictly in order, so both sides walk the
+// ring with a running position instead of dividing an item index.
+struct RingPos {
+    int st = 0;
+    uint32_t ph = 0;
+    template <int kStages>
+    __device__ __forceinline__ void advance() {
+        if (++st == kStages) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+
+// Shared-memory descriptors kept as 32-bit halves: the start-address field
+// sits in the low half, and every operand address used here stays below
+// 256 KB, so stepping through a tile is a 32-bit add of (offset >> 4).
+struct Desc {
+    uint32_t lo, hi;
+};
+
+__device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = smem_desc_sw128(saddr, lbo, sbo);
+    return Desc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+
+// S = Q K^T over d: D/16 MMAs of 128 x 128 x 16.  Q from tensor memory
+// (8 columns of bf16 pairs per 16-element step); K K-major with the 128-byte
+// swizzle: 16-element steps advance 32 bytes inside a 64-column box, then
+// jump to the next box.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_tmem, Desc k) {
+    constexpr uint32_t kId = idesc_bf16_f32(kBM, kBN, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ok = ((kk >> 2) * (kBN * kSwRowBytes) + (kk & 3) * 32) >> 4;
+        if (kk == 0)
+            mma_ts_c<0>(d_tmem, q_tmem + kk * 8, k.lo + ok, k.hi, kId);
+        else
+            mma_ts_c<1>(d_tmem, q_tmem + kk * 8, k.lo + ok, k.hi, kId);
+    }
+}
+
+// O += P V over the 128 keys of a tile: 8 MMAs of 128 x D x 16, P from tensor
+// memory (8 columns of bf16 pairs per step), V MN-major: 16 keys are two
+// 8-row swizzle atoms, the next 64 value columns one TMA box further on.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc v, uint32_t accumulate) {
+    constexpr uint32_t kId = idesc_bf16_f32(kBM, D, 0, 1);
+    mma_ts_r(o_tmem, p_tmem, v.lo, v.hi, kId, accumulate);
+#pragma unroll
+    for (int kk = 1; kk < kBN / 16; ++kk)
+        mma_ts_c<1>(o_tmem, p_tmem + kk * 8, v.lo + ((kk * 16 * kSwRowBytes) >> 4), v.hi, kId);
+}
+
+// TMA producer: the ring items in consumption order.  With PAIR == 2
+// this CTA loads rows [64 r, 64 r + 64) of every K/V box (r = cluster rank)
+// into both CTAs of the cluster.
+template <int D, int PAIR>
+__device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUtensorMap &tmV, const Params &P,
+                                              const Unit &U, uint8_t *smem, Barriers &bar) {
+    using L = SmemLayout<D>;
+    volatile int *abort = &bar.abort;
+    const int n = U.n_tiles;
+    const int kv_head = U.b * P.Hkv + U.g;
+    // One tile (K or V, rows key0..key0+127) into half `half` of stage st.
+    auto load_tile = [&](int st, int half, const CUtensorMap *map, int t) {
+        const int key0 = (U.t_begin + t) * kBN;
+#pragma unroll
+        for (int c = 0; c < L::kBoxes; ++c) {
+            uint8_t *dst = smem + L::kRing + st * L::kStageBytes + half * L::kKVBytes + c * (kBN * kSwRowBytes);
+            if (PAIR == 2) {
+                const int r = (int)(blockIdx.x & 1);
+                tma_load_3d_multicast(dst + r * (kBN / 2) * kSwRowBytes, map, &bar.full[st], c * 64,
+                                      key0 + r * (kBN / 2), kv_head, (uint16_t)0x3);
+            } else {
+                tma_load_3d(dst, map, &bar.full[st], c * 64, key0, kv_head);
+            }
+        }
+    };
+    int issued[kMaxStages] = {};
+    RingPos put;
+    bool first_pass = true;
+    // Stage use 0: K_0 (and K_1); use 1 + j: V_j (and K_{j+2}).
+    for (int use = 0; use <= n; ++use) {
+        const int st = put.st;
+        // From the second pass on, wait for the release of the stage's previous use.
+        if (!first_pass && !mbar_wait(&bar.empty[st], put.ph ^ 1u, abort)) break;
+        const bool second = use == 0 ? n > 1 : use + 1 < n;  // K_1, or K_{j+2}
+        mbar_arrive_expect_tx(&bar.full[st], (second ? 2 : 1) * L::kKVBytes);  // halves from both CTAs land here
+        if (use == 0) {
+            load_tile(st, 0, &tmK, 0);
+            if (second) load_tile(st, 1, &tmK, 1);
+        } else {
+            load_tile(st, 0, &tmV, use - 1);
+            if (second) load_tile(st, 1, &tmK, use + 1);
+        }
+        ++issued[st];
+        put.template advance<L::kStages>();
+        if (put.st == 0) first_pass = false;
+    }
+    if (*abort) {
+        // Drain: every copy issued above lands before shared memory goes away.
+        int never = 0;
+        for (int s = 0; s < L::kStages; ++s)
+            if (issued[s] > 0) mbar_wait(&bar.full[s], (issued[s] - 1) & 1, &never, 200000000ull);
+    }
+}
+
+// MMA issuer (one thread).  tcgen05.mma issue returns at about the tensor
+// core's execution rate (its queue holds two or so MMAs), so every barrier
+// operation between MMAs can idle the tensor core: per tile j the issuer
+// waits for P_j, issues O += P_j V_j, checks the next stage (V_{j+1}, K_{j+3})
+// in the shadow of those MMAs, issues S_{j+2}, then commits.
+template <int D, int PAIR>
+__device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers &bar, uint32_t tbase) {
+    using L = SmemLayout<D>;
+    volatile int *abort = &bar.abort;
+    const int n = U.n_tiles;
+    const uint32_t q_tmem = tbase + kColQ;
+    // Stage st starts (st * kStageBytes) >> 4 descriptor units after stage 0;
+    // its second tile kKVBytes >> 4 units further.
+    const Desc k0 = make_desc(smem_u32(smem + L::kRing), 16, 1024);
+    const Desc v0 = make_desc(smem_u32(smem + L::kRing), kBN * kSwRowBytes, 1024);
+    constexpr uint32_t kStageUnits = L::kStageBytes >> 4, kHalfUnits = L::kKVBytes >> 4;
+    // A stage is free once every CTA that reads it has finished with it.
+    auto release = [&](int st) {
+        if (PAIR == 2)
+            mma_commit_multicast(&bar.empty[st], (uint16_t)0x3);
+        else
+            mma_commit(&bar.empty[st]);
+    };
+    RingPos take;
+
+    bool ok = mbar_wait(&bar.q_full, 0, abort) && mbar_wait(&bar.full[take.st], take.ph, abort);
+    if (ok) {
+        // S_0 and S_1 before any softmax work.
+        tc_fence_after();
+        issue_qk<D>(tbase + col_s(0), q_tmem, Desc{k0.lo + take.st * kStageUnits, k0.hi});
+        mma_commit(&bar.s_full[0]);
+        if (n > 1) {
+            issue_qk<D>(tbase + col_s(1), q_tmem, Desc{k0.lo + take.st * kStageUnits + kHalfUnits, k0.hi});
+            mma_commit(&bar.s_full[1]);
+        }
+        release(take.st);
+        take.template advance<L::kStages>();
+        ok = mbar_wait(&bar.full[take.st], take.ph, abort);  // V_0 (and K_2)
+    }
+    for (int j = 0; ok && j < n; ++j) {
+        const int b = j & 1;
+        const bool next = j + 2 < n;
+        const int st = take.st;
+        if (!mbar_wait(&bar.p_full[b], (j >> 1) & 1, abort)) break;
+        tc_fence_after();
+        issue_pv<D>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + st * kStageUnits, v0.hi}, j > 0 ? 1u : 0u);
+        take.template advance<L::kStages>();
+        // The next stage, while the tensor core works through the queue.
+        if (j + 1 < n && !(ok = mbar_wait(&bar.full[take.st], take.ph, abort))) break;
+        // S_{j+2} into the buffer P_j came from (issued after P_j V_j).
+        if (next) {
+            issue_qk<D>(tbase + col_s(b), q_tmem, Desc{k0.lo + st * kStageUnits + kHalfUnits, k0.hi});
+            mma_commit(&bar.s_full[b]);  // covers O += P_j V_j as well
+        } else if (j + 1 == n) {
+            mma_commit(&bar.o_final);
+        } else {
+            mma_commit(&bar.o_done);  // j == n-2: no S after it
+        }
+        release(st);
+    }
+    // Every MMA issued above completes before tensor memory is freed.
+    mma_commit(&bar.mma_drain);
+    int never = 0;
+    mbar_wait(&bar.mma_drain, 0, &never, 200000000ull);
+}
+
+// Softmax warps 0-3: thread = query row = TMEM lane; epilogue.
+template <int D>
+__device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Barriers &bar, uint32_t tbase,
+                                             int warp) {
+    volatile int *abort = &bar.abort;
+    const int n = U.n_tiles;
+    const int row = threadIdx.x;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t o_addr = tbase + lane_off + kColO;
+    const int i = U.r0 + row;
+    const int64_t p = (int64_t)P.q_offset + i;
+    const int64_t p_first = (int64_t)P.q_offset + U.r0;
+    const int64_t p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
+    // Per-row visible key interval [vlo, vhi) before the additive mask.
+    int64_t vlo, vhi;
+    visible_range(P, p, vlo, vhi);
+    const float c = P.scale_log2;
+    const bool has_sink = P.sinks != nullptr;
+    float m = has_sink ? __ldg(P.sinks + U.h) * kLog2e : -INFINITY;  // log2 units
+    float l = has_sink ? 1.f : 0.f;
+    const float *mrow =
+        (P.mask != nullptr && i < P.Tq) ? P.mask + U.b * P.msb + U.h * P.msh + (int64_t)i * P.msq : nullptr;
+    bool ok = true;
+    // Tiles t (relative to t_begin) in [ti_lo, ti_hi) are interior: every key
+    // visible to every row of the CTA, and no additive mask.
+    int ti_lo = 0, ti_hi = 0;
+    if (P.mask == nullptr && c > 0.f) {
+        int64_t hi_key = P.Tk;                                   // j0 + kBN <= Tk
+        if (P.causal && p_first + 1 < hi_key) hi_key = p_first + 1;  // j0 + kBN - 1 <= p_first
+        int64_t lo_key = 0;                                      // j0 > p_last - window
+        if (P.window > 0 && p_last - P.window + 1 > 0) lo_key = p_last - P.window + 1;
+        const int64_t t_lo = (lo_key + kBN - 1) / kBN, t_hi = hi_key / kBN;
+        ti_lo = (int)(t_lo - U.t_begin);
+        ti_hi = (int)(t_hi - U.t_begin);
+    }
+
+    if (n > 0) {
+        // Q row i into this lane's TMEM columns [kColQ, kColQ + D/2): the
+        // bf16 pairs of memory are the packed A-operand layout already.
+        const uint4 *qrow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                            ((int64_t)U.bh * P.Tq + (i < P.Tq ? i : 0)) * D);
+        uint32_t qr[D / 2];
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e) {
+            const uint4 v = i < P.Tq ? __ldg(qrow + e) : make_uint4(0u, 0u, 0u, 0u);
+            qr[4 * e] = v.x;
+            qr[4 * e + 1] = v.y;
+            qr[4 * e + 2] = v.z;
+            qr[4 * e + 3] = v.w;
+        }
+        if constexpr (D == 128) {
+            tmem_store64(tbase + lane_off + kColQ, qr);
+        } else {
+            tmem_store32(tbase + lane_off + kColQ, qr);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.q_full);
+    }
+
+    for (int j = 0; j < n; ++j) {
+        const int b = j & 1;
+        const uint32_t s_addr = tbase + lane_off + col_s(b);
+        // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j >> 1) & 1, abort))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        uint32_t sr[kBN];
+        tmem_load128(s_addr, sr);
+        float *s = reinterpret_cast<float *>(sr);
+
+        float cs = c;  // multiplier from s[] to log2 units for this tile
+        if (j < ti_lo || j >= ti_hi) {
+            const int j0 = (U.t_begin + j) * kBN;
+            // The row's visible keys in this tile: [elo, ehi) (clamped).
+            const int64_t elo64 = vlo - j0, ehi64 = vhi - j0;
+            const int elo = elo64 < -1 ? -1 : (elo64 > kBN ? kBN : (int)elo64);
+            const int ehi = ehi64 < -1 ? -1 : (ehi64 > kBN ? kBN : (int)ehi64);
+            if (mrow != nullptr) {
+                // Additive mask: scores in log2 units; keys past Tk read a
+                // clamped (valid) address and are dropped by the interval.
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) {
+                    const int jj = min(j0 + e, P.Tk - 1);
+                    const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
+                    s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                }
+                cs = 1.f;
+            } else if (c <= 0.f) {
+                // A non-positive scale: scale first so that -inf marks the
+                // keys the row cannot see.
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
+                cs = 1.f;
+            } else {
+                // Boundary tile: keys outside the row's interval drop to -inf.
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
+            }
+        }
+        float bm;  // tile max of s[] * cs, in log2 units
+        {
+            static_assert(kBN == 128, "max chains assume 128 keys per tile");
+            float mx[8];  // eight independent chains of three-input max
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);  // keys 0..23
+#pragma unroll
+            for (int e = 24; e < 120; e += 16)  // keys 24..119
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[120 + c8]);  // keys 120..127
+            bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
+        }
+
+        // Lazy max: move m only when the tile exceeds it by the threshold
+        // (with m = -inf any finite tile max does, and 2^(-inf) = 0).
+        float alpha = 1.f;
+        if (bm > m + kRescaleThreshold) {
+            alpha = ex2_approx(m - bm);
+            m = bm;
+        }
+        const float shift = (m == -INFINITY) ? 0.f : m;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // O must hold P_{j-1} V_{j-1} before it is rescaled: the commit
+            // after S_{j+1} (issued after it) shows that, or, for the last
+            // tile, the commit after O += P_{n-2} V_{n-2}.
+            const bool via_s = j + 1 < n;
+            uint64_t *bo = via_s ? &bar.s_full[(j + 1) & 1] : &bar.o_done;
+            const uint32_t ph = via_s ? (uint32_t)(((j + 1) >> 1) & 1) : 0u;
+            if (!__all_sync(0xffffffffu, mbar_wait(bo, ph, abort))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float s[kBN];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t r[32];
-                tmem_load32(lane_addr + (sb ? kColS1 : kColS0) + c * 32, r);
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t orr[32];
+                tmem_load32(o_addr + cc * 32, orr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
-            }
-            tc_fence_before();
-            mbar_arrive(&bar.s_free[sb]);
-
-            const int j0 = (t_begin + jj) * kBN;
-            const bool full = (j0 + kBN <= P.Tk) && (!P.causal || (int64_t)(j0 + kBN - 1) <= p_first) &&
-                              (P.window <= 0 || (int64_t)j0 > p_last - P.window);
-            float bm = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < kBN; ++e) {
-                float v = s[e] * P.scale_log2;
-                if (mrow != nullptr && i < P.Tq && j0 + e < P.Tk)
-                    v = fmaf(__ldg(mrow + (int64_t)(j0 + e) * P.msk), kLog2e, v);
-                if (!full) {
-                    const int64_t j = j0 + e;
-                    const bool vis = j < P.Tk && (!P.causal || j <= p) && (P.window <= 0 || j > p - P.window);
-                    if (!vis) v = -INFINITY;
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 v = fmul2(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])),
+                                           make_float2(alpha, alpha));
+                    orr[e] = __float_as_uint(v.x);
+                    orr[e + 1] = __float_as_uint(v.y);
                 }
-                s[e] = v;
-                bm = fmaxf(bm, v);
+                tmem_store32(o_addr + cc * 32, orr);
             }
-            const float mnew = fmaxf(m, bm);
-            const float shift = (mnew == -INFINITY) ? 0.f : mnew;
-            const float alpha = (m == shift) ? 1.f : ex2(m - shift);
-
-            uint32_t pk[kBN / 2];
-            float rs = 0.f;
-#pragma unroll
-            for (int e = 0; e < kBN; e += 2) {
-                const float p0 = ex2(s[e] - shift), p1 = ex2(s[e + 1] - shift);
-                rs += p0 + p1;
-                pk[e / 2] = pack_bf16x2(p0, p1);
-            }
-
-            if (jj >= 1) {  // P_{t-1} consumed and O final for t-1
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar.o_ready, (jj - 1) & 1, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-#pragma unroll
-            for (int c = 0; c < kBN / 64; ++c) {
-                uint32_t r[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = pk[c * 32 + e];
-                tmem_store32(lane_addr + kColP + c * 32, r);
-            }
-            if (jj >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_load32(lane_addr + kColO + c * 32, r);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_store32(lane_addr + kColO + c * 32, r);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bar.p_full);
-            l = fmaf(alpha, l, rs);
-            m = mnew;
         }
 
-        if (ok && n_tiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_ready, (n_tiles - 1) & 1, abort));
-            tc_fence_after();
+        // p = 2^(s cs - shift), rounded to bf16 pairs; row sum in fp32.
+        const float2 cs2 = make_float2(cs, cs), nsh2 = make_float2(-shift, -shift);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int e = 0; e < kBN; e += 4) {
+            const float2 x0 = ffma2(make_float2(s[e], s[e + 1]), cs2, nsh2);
+            const float2 x1 = ffma2(make_float2(s[e + 2], s[e + 3]), cs2, nsh2);
+            const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+            const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+            acc0 = fadd2(acc0, p0);
+            acc1 = fadd2(acc1, p1);
+            pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
+            pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
         }
-        if (ok) {
-            // Epilogue: o = O / l (0 for an empty row), lse = (m + log2 l) ln 2.
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)bh * P.Tq + i) * D;
+        tmem_store64(s_addr, pk);
+        tc_fence_before();
+        mbar_arrive(&bar.p_full[b]);
+        const float2 a = fadd2(acc0, acc1);
+        l = fmaf(alpha, l, a.x + a.y);
+    }
+
+    if (ok && n > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0, abort));
+        tc_fence_after();
+    }
+    if (ok) {
+        // Epilogue: o = O / l (0 for an empty row), lse = (m + log2 l) ln 2.
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)U.bh * P.Tq + i) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                if (n_tiles > 0) {
-                    tmem_load32(lane_addr + kColO + c * 32, r);
-                } else {
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t orr[32];
+            if (n > 0) {
+                tmem_load32(o_addr + cc * 32, orr);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = 0u;
-                }
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-                if (i < P.Tq) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-                }
+                for (int e = 0; e < 32; ++e) orr[e] = 0u;
             }
-            if (P.lse != nullptr && i < P.Tq)
-                P.lse[(int64_t)bh * P.Tq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[e] = cvt_bf16x2(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+            if (i < P.Tq) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
         }
+        if (P.lse != nullptr && i < P.Tq) P.lse[(int64_t)U.bh * P.Tq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+}
+
+template <int D, int PAIR>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const Params P) {
+    using L = SmemLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Barriers &bar = *reinterpret_cast<Barriers *>(smem + L::kBar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Unit U = decode_unit<PAIR>(P);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar.q_full, kBM);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&bar.full[s], 1);
+            mbar_init(&bar.empty[s], PAIR);  // one release per CTA reading the slot
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar.s_full[s], 1);
+            mbar_init(&bar.p_full[s], kBM);
+        }
+        mbar_init(&bar.o_done, 1);
+        mbar_init(&bar.o_final, 1);
+        mbar_init(&bar.mma_drain, 1);
+        bar.abort = 0;
+        mbar_init_fence();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&bar.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    if (PAIR == 2)
+        cluster_sync();  // the peer's barriers exist before any multicast reaches them
+    else
+        __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = bar.tmem_base;
+    // Inputs may come from the previous kernel in the stream, and outputs may
+    // still be read by it.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp == kWarpTma) {
+        if (lane == 0 && U.n_tiles > 0) producer_role<D, PAIR>(tmK, tmV, P, U, smem, bar);
+    } else if (warp == kWarpMma) {
+        if (lane == 0 && U.n_tiles > 0) mma_role<D, PAIR>(U, smem, bar, tbase);
+    } else {
+        softmax_role<D>(P, U, bar, tbase, warp);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (*abort && threadIdx.x == 0) atomicOr(&g_watchdog, 1u);
-    if (warp == 5) {
+    // No CTA of a pair leaves while the other may still multicast into it.
+    if (PAIR == 2) cluster_sync();
+    if (bar.abort && threadIdx.x == 0) atomicOr(&g_watchdog, 1u);
+    if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
@@ -391,53 +632,66 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [heads, rows, d] bf16 viewed as a 3-D tensor; boxes of 64 columns x 128 rows
-// with the 128-byte swizzle; rows past `rows` read as zero.
-bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int rows, int heads) {
+// [heads, rows, d] bf16 viewed as a 3-D tensor; boxes of 64 columns x box_rows
+// rows with the 128-byte swizzle; rows past `rows` read as zero.
+bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int rows, int heads, int box_rows) {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int PAIR>
 cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tk, tv;
     // With Tk == 0 no key tile is ever loaded; the K/V maps only need to be valid.
     const void *kb = P.Tk > 0 ? P.k : P.q;
     const void *vb = P.Tk > 0 ? P.v : P.q;
     const int krows = P.Tk > 0 ? P.Tk : 1;
     const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
-    if (!make_map(enc, &tq, P.q, D, P.Tq, P.B * P.Hq) || !make_map(enc, &tk, kb, D, krows, kheads) ||
-        !make_map(enc, &tv, vb, D, krows, kheads))
+    if (!make_map(enc, &tk, kb, D, krows, kheads, kBN / PAIR) || !make_map(enc, &tv, vb, D, krows, kheads, kBN / PAIR))
         return cudaErrorInvalidValue;
-    // At least 116 KB so that one CTA holds an SM: the CTA takes all 512
-    // tensor-memory columns, and a second resident CTA would only wait in
-    // tcgen05.alloc.
-    const size_t smem = SmemLayout<D>::kTotal + 1024 > 116 * 1024 ? SmemLayout<D>::kTotal + 1024 : 116 * 1024;
+    // The CTA takes all 512 tensor-memory columns; the shared-memory request
+    // (the K/V ring fills it) keeps a second CTA off the SM.
+    constexpr size_t kSmem = SmemLayout<D>::kTotal + 1024;
+    static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "shared memory budget");
     static bool configured = false;
     if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(fa_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, PAIR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int nqt = (P.Tq + kBM - 1) / kBM;
-    const unsigned grid = (unsigned)nqt * (unsigned)(P.B * P.Hq);
-    fa_fwd_bf16_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nqt * (unsigned)(P.B * P.Hq));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = PAIR;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR>, tk, tv, P);
 }
 
 }  // namespace
 
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
-    if (P.d == 64) return launch_d<64>(P, stream);
-    return launch_d<128>(P, stream);
+    // Pairs of query heads share a KV head when the group size is even.
+    const bool pair = (P.group % 2) == 0;
+    if (P.d == 64) return pair ? launch_d<64, 2>(P, stream) : launch_d<64, 1>(P, stream);
+    return pair ? launch_d<128, 2>(P, stream) : launch_d<128, 1>(P, stream);
 }
 
 }  // namespace fa
