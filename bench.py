@@ -107,6 +107,35 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in self.rows)}
 
 
+def kernel_sources_digest() -> str:
+    """sha256 over the CUDA sources of the library (identifies the kernel
+    build a profile was taken with)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(_ROOT, "exact_tiled_attention_flashattention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def max_over_ranks(seconds: float, dist=None, device=None) -> float:
+    """The slowest rank's time: the whole job finishes when it does."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_step: int, steps: int, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank processes ``flops_per_step`` per step
+    (replicas, weak scaling), divided by the slowest rank's time."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 def time_graph(fn, reps, flush, warm=3):
     """Median device time (ms) of ``fn`` replayed from a CUDA graph, with L2
     flushed before every replay; events bracket the replay only."""
@@ -263,11 +292,8 @@ def run_fa(args, rank, world, local_rank):
         ev[s][1].record()
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_s = sum(step_ms) / 1e3
+    total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
     if dist is not None:
-        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
         dist.barrier()
     sampler.stop()
 
@@ -300,11 +326,7 @@ def run_fa(args, rank, world, local_rank):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
 
     # Long-context causal prefill at T = 2044, 8192, 32768 (bf16), one call
     # per measurement, L2 flushed before each.
@@ -347,14 +369,18 @@ def run_fa(args, rank, world, local_rank):
     traffic = None
     prof = os.path.join(_ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
+        # DRAM bytes per launch from an ncu capture, valid only while the
+        # kernel sources are the ones the capture was taken with.
         try:
             with open(prof) as f:
-                traffic = json.load(f).get(WORKLOAD)
+                rec = json.load(f).get(WORKLOAD)
+            if rec and rec.get("kernel_sources_sha256") == kernel_sources_digest():
+                traffic = rec.get("dram_bytes_per_launch")
         except Exception:
             traffic = None
     avg_launch_s = (total_s / args.steps) / L
     achieved = flops_call / avg_launch_s / 1e12
-    value = world * flops_step * args.steps / total_s / 1e12
+    value = job_throughput(world, flops_step, args.steps, total_s)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 4), "higher_is_better": True,
@@ -362,7 +388,7 @@ def run_fa(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "T": p.Tq, "d": p.d, "causal": True,
                    "layers_per_step": L, "flops_per_step": flops_step, "launch": "CUDA graph of 28 fa_fwd calls",
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(world * flops_step * args.steps / e2e_s / 1e12, 3), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(world, flops_step, args.steps, e2e_s), 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(1e3 * e2e_s / args.steps, 4)},
         "gpu_launches": L * args.steps,
