@@ -1,23 +1,21 @@
 // fa_fwd_bf16.cu -- bf16 exact tiled attention on the tcgen05 tensor cores.
 //
-// A CTA owns one 128-row query tile of one (batch, query head).  It walks the
-// key tiles its rows can see, 128 keys at absolute positions [128t, 128t+128)
-// each, under the online softmax of "FlashAttention forward in C" (section
-// 2.2), in base 2 (c = scale * log2 e):
+// Work unit: one 128-row query tile of one (batch, query head).  A unit walks
+// the key tiles its rows can see, 128 keys at absolute positions
+// [128t, 128t + 128) each, under the online softmax of "FlashAttention forward
+// in C" (section 2.2), in base 2 (c = scale * log2 e):
 //
-//   S_t = Q K_t^T          tcgen05.mma, Q from TMEM (A operand), K_t from
-//                          shared memory (TMA, 128-byte swizzle), fp32
-//                          accumulator in TMEM
+//   S_t = Q K_t^T          tcgen05.mma, Q and K_t from shared memory (TMA,
+//                          128-byte swizzle), fp32 accumulator in TMEM
 //   P_t = 2^(S_t c - m)    softmax warps: tcgen05.ld of S_t, row max, ex2,
 //                          row sum; P rounded to bf16 and tcgen05.st back into
 //                          the first 64 columns of S_t's buffer
 //   O  += P_t V_t          tcgen05.mma, A = P_t from TMEM, B = V_t (MN-major)
 //
 // S is double-buffered in tensor memory (S_A, S_B), so the issuer computes
-// S_{t+1} while the softmax warps work on S_t; the tensor core and the
-// softmax overlap and a tile costs about max(softmax, S + PV) rather than
-// their sum.  S_{t+2} reuses the buffer of P_t and is issued after
-// O += P_t V_t: tcgen05.mma operations issued by one thread execute in order.
+// S_{t+1} while the softmax warps work on S_t.  S_{t+2} reuses the buffer of
+// P_t and is issued after O += P_t V_t: tcgen05.mma operations issued by one
+// thread execute in order.
 //
 // The running max m of a row is raised lazily: only when a tile's max
 // exceeds it by more than 8 (log2 units) is O rescaled in TMEM by
@@ -26,37 +24,37 @@
 // follows "Fused attention and softmax: fast and exact" (the exact
 // definition, steps 2 and 5).
 //
+// Persistent schedule: one CTA (or CTA pair) per SM walks a list of units
+// sorted heaviest first (under a causal rule the last query tiles see the
+// most keys), taking them in snake order (round r takes group g, the next
+// round group G-1-g), so heavy and light units balance across SMs.  The K/V
+// ring, the S buffers and every barrier run on across units: the next unit's
+// K_0, K_1 and Q load while the current unit finishes, its S_0, S_1 run while
+// the softmax warps write the current unit's output.
+//
 // K/V sharing: when the GQA group size is even, the two query heads of a KV
 // head at the same rows run as a cluster of two CTAs.  Each CTA loads half of
 // every K/V tile (64 of its 128 rows) with a multicast TMA that lands in both
 // CTAs' shared memory, and a ring slot is refilled only after both CTAs'
 // tensor cores released it (a multicast tcgen05.commit arrives on the slot's
-// barrier in both CTAs).  Every K/V byte is then read from L2 once per pair,
-// which halves the L2 traffic that otherwise bounds long sequences.
-//
-// Q lives in tensor memory: each softmax thread loads its query row from
-// global memory once and stores it (bf16 pairs) into its TMEM lane, so the
-// shared-memory bandwidth goes to K and V only: per tile the tensor core
-// reads K (S MMAs) and V (P.V MMAs) and TMA writes both, 128 KB in all, which
-// the shared memory sustains within the tile's tensor-core time.
+// barrier in both CTAs).  Each ring stage holds the two tiles one issuer step
+// consumes (V_j and K_{j+2}; the unit's first stage K_0 and K_1).
 //
 // Warp roles (192 threads):
-//   warps 0-3   softmax: thread t = query row t = TMEM lane t; Q load;
-//               epilogue
-//   warp 4      TMA producer: the K and V tiles in the order the tensor core
-//               consumes them (K_0, K_1, V_0, K_2, V_1, ...) into a ring of
-//               shared-memory stages
+//   warps 0-3   softmax: thread t = query row t = TMEM lane t; epilogue
+//   warp 4      TMA producer (one lane)
 //   warp 5      MMA issuer (one lane) and tensor-memory owner
 // Tensor memory (512 columns allocated): S_A [0,128) S_B [128,256)
-// O [256, 256+d) Q [384, 384+d/2).
+// O [256, 256+d).
 //
-// A row's arithmetic does not depend on its query tile or on chunking through
-// q_offset: key tiles are absolute, a key the row cannot see gets weight 0 and
-// leaves m, l and O unchanged ("FlashAttention forward in C", section 2.4).
+// A row's arithmetic does not depend on its query tile, its unit's place in
+// the schedule or on chunking through q_offset: key tiles are absolute, a key
+// the row cannot see gets weight 0 and leaves m, l and O unchanged
+// ("FlashAttention forward in C", section 2.4).
 //
-// Launch: programmatic dependent launch lets the CTA prologue (barriers,
-// tensor-memory allocation, descriptor prefetch) overlap the previous kernel
-// in the stream; griddepcontrol.wait orders every global access after it.
+// Launch: programmatic dependent launch lets the CTA prologue overlap the
+// previous kernel in the stream; griddepcontrol.wait orders every global
+// access after it.
 //
 // Every mbarrier wait is bounded (two seconds of wall time); a wait that runs
 // out sets a CTA-wide abort flag and the device watchdog word, every role
@@ -78,96 +76,106 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBM = 128;  // query rows per CTA = tensor-memory lanes
+constexpr int kBM = 128;  // query rows per unit = tensor-memory lanes
 constexpr int kBN = 128;  // keys per tile
 constexpr int kThreads = 192;
 constexpr int kWarpTma = 4, kWarpMma = 5;
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int buf) { return 128u * buf; }  // S_A, S_B (and P)
 constexpr uint32_t kColO = 256;
-constexpr uint32_t kColQ = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay below 2^8
 constexpr uint32_t kSwRowBytes = 128;      // one swizzled row: 64 bf16
-constexpr int kMaxStages = 7;
+constexpr int kMaxStages = 6;
 
-// The K/V ring: each stage holds the two tiles one issuer step consumes
-// (V_j and K_{j+2}; the first stage K_0 and K_1), so one barrier wait and one
-// release cover both.
 template <int D>
 struct SmemLayout {
     static constexpr int kBoxes = D / 64;  // 64-column TMA boxes per tile
+    static constexpr uint32_t kQBytes = kBM * D * 2;
     static constexpr uint32_t kKVBytes = kBN * D * 2;
-    static constexpr uint32_t kStageBytes = 2 * kKVBytes;
-    static constexpr int kStages = D == 128 ? 3 : 7;  // 192 KB / 224 KB
-    static constexpr uint32_t kRing = 0;
+    static constexpr uint32_t kStageBytes = 2 * kKVBytes;  // two tiles per stage
+    static constexpr int kStages = D == 128 ? 3 : 6;       // 192 KB ring
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kRing = kQ + kQBytes;
     static constexpr uint32_t kBar = kRing + kStages * kStageBytes;
     static constexpr uint32_t kTotal = kBar + 512;
     static_assert(kStages <= kMaxStages, "ring too deep");
 };
 
 struct Barriers {
-    uint64_t q_full;  // Q stored in tensor memory by the softmax threads
+    uint64_t q_full;                               // Q of the unit landed
+    uint64_t q_empty;                              // the unit's last S done: Q buffer free
     uint64_t full[kMaxStages], empty[kMaxStages];  // the K/V ring
     uint64_t s_full[2];                            // S_A, S_B written
     uint64_t p_full[2];                            // P in S_A, S_B written
-    uint64_t o_done;                               // O += P_{n-2} V_{n-2} completed (once)
-    uint64_t o_final;                              // the last O += P V completed
+    uint64_t o_done;                               // O += P_{n-2} V_{n-2} completed
+    uint64_t o_final;                              // the unit's last O += P V completed
     uint64_t mma_drain;
     uint32_t tmem_base;
     int abort;
 };
 
-// Work unit of one CTA: one query tile; heaviest tiles first (under a causal
-// rule the last tiles see the most keys).
 struct Unit {
     int b, h, g, bh;
     int r0;  // first query row
     int t_begin, n_tiles;
 };
 
+// Units sorted heaviest first: unit u has query tile nqt-1-u/per_qt.  With
+// PAIR == 2 a unit covers query heads 2h' (cluster rank 0) and 2h'+1 (rank 1)
+// of one KV group; `rank` picks this CTA's head.
 template <int PAIR>
-__device__ __forceinline__ Unit decode_unit(const Params &P) {
-    Unit u;
+__device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
+    Unit U;
     const int nqt = (P.Tq + kBM - 1) / kBM;
-    int qt;
+    const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
+    const int qt = nqt - 1 - u / per_qt;
+    const int r = u % per_qt;
     if (PAIR == 2) {
-        // CTAs 2k and 2k+1 (one cluster) take query heads 2h' and 2h'+1 of one
-        // KV group at the same rows.
-        const int pairs = P.B * (P.Hq / 2);
-        const int unit = (int)(blockIdx.x >> 1);
-        qt = nqt - 1 - unit / pairs;
-        const int pr = unit % pairs;
-        u.b = pr / (P.Hq / 2);
-        u.h = 2 * (pr % (P.Hq / 2)) + (int)(blockIdx.x & 1);
-        u.bh = u.b * P.Hq + u.h;
+        U.b = r / (P.Hq / 2);
+        U.h = 2 * (r % (P.Hq / 2)) + rank;
     } else {
-        const int BH = P.B * P.Hq;
-        qt = nqt - 1 - (int)(blockIdx.x / BH);
-        u.bh = (int)(blockIdx.x % BH);
-        u.b = u.bh / P.Hq;
-        u.h = u.bh % P.Hq;
+        U.b = r / P.Hq;
+        U.h = r % P.Hq;
     }
-    u.g = u.h / P.group;
-    u.r0 = qt * kBM;
+    U.bh = U.b * P.Hq + U.h;
+    U.g = U.h / P.group;
+    U.r0 = qt * kBM;
     int64_t lo_a, hi_a, lo_b, hi_b;
-    visible_range(P, (int64_t)P.q_offset + u.r0, lo_a, hi_a);
-    visible_range(P, (int64_t)P.q_offset + min(u.r0 + kBM, P.Tq) - 1, lo_b, hi_b);
+    visible_range(P, (int64_t)P.q_offset + U.r0, lo_a, hi_a);
+    visible_range(P, (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1, lo_b, hi_b);
     const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
     if (khi > klo) {
-        u.t_begin = (int)(klo / kBN);
-        u.n_tiles = (int)((khi + kBN - 1) / kBN) - u.t_begin;
+        U.t_begin = (int)(klo / kBN);
+        U.n_tiles = (int)((khi + kBN - 1) / kBN) - U.t_begin;
     } else {
-        u.t_begin = 0;
-        u.n_tiles = 0;
+        U.t_begin = 0;
+        U.n_tiles = 0;
     }
-    return u;
+    return U;
+}
+
+// Snake order over groups: round r gives group g unit r*G + g (r even) or
+// r*G + G-1-g (r odd); -1 past the end.
+struct Schedule {
+    int units, groups, group;
+    __device__ __forceinline__ int unit_at(int r) const {
+        const int u = r * groups + ((r & 1) ? groups - 1 - group : group);
+        return u < units ? u : -1;
+    }
+};
+
+template <int PAIR>
+__device__ __forceinline__ Schedule make_schedule(const Params &P) {
+    const int nqt = (P.Tq + kBM - 1) / kBM;
+    const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
+    return Schedule{nqt * per_qt, (int)(gridDim.x / PAIR), (int)(blockIdx.x / PAIR)};
 }
 
 // Position in the K/V ring: stage index and the parity of its current use.
-// Items are produced and consumed strictly in order, so both sides walk the
-// ring with a running position instead of dividing an item index.
+// Stages are produced and consumed strictly in order, so both sides walk the
+// ring with a running position.
 struct RingPos {
     int st = 0;
     uint32_t ph = 0;
@@ -179,7 +187,6 @@ struct RingPos {
         }
     }
 };
-
 
 // Shared-memory descriptors kept as 32-bit halves: the start-address field
 // sits in the low half, and every operand address used here stays below
@@ -193,20 +200,20 @@ __device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t
     return Desc{(uint32_t)d, (uint32_t)(d >> 32)};
 }
 
-// S = Q K^T over d: D/16 MMAs of 128 x 128 x 16.  Q from tensor memory
-// (8 columns of bf16 pairs per 16-element step); K K-major with the 128-byte
-// swizzle: 16-element steps advance 32 bytes inside a 64-column box, then
-// jump to the next box.
+// S = Q K^T over d: D/16 MMAs of 128 x 128 x 16.  Q and K are K-major with
+// the 128-byte swizzle: 16-element steps advance 32 bytes inside a 64-column
+// box, then jump to the next box.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_tmem, Desc k) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, Desc q, Desc k) {
     constexpr uint32_t kId = idesc_bf16_f32(kBM, kBN, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t oq = ((kk >> 2) * (kBM * kSwRowBytes) + (kk & 3) * 32) >> 4;
         const uint32_t ok = ((kk >> 2) * (kBN * kSwRowBytes) + (kk & 3) * 32) >> 4;
         if (kk == 0)
-            mma_ts_c<0>(d_tmem, q_tmem + kk * 8, k.lo + ok, k.hi, kId);
+            mma_ss_c<0>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
         else
-            mma_ts_c<1>(d_tmem, q_tmem + kk * 8, k.lo + ok, k.hi, kId);
+            mma_ss_c<1>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
     }
 }
 
@@ -222,55 +229,74 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc 
         mma_ts_c<1>(o_tmem, p_tmem + kk * 8, v.lo + ((kk * 16 * kSwRowBytes) >> 4), v.hi, kId);
 }
 
-// TMA producer: the ring items in consumption order.  With PAIR == 2
-// this CTA loads rows [64 r, 64 r + 64) of every K/V box (r = cluster rank)
-// into both CTAs of the cluster.
+// TMA producer (one thread).  Per unit: the first stage (K_0, K_1), then Q
+// once the previous unit's last S has released the Q buffer, then the stages
+// (V_j, K_{j+2}).  With PAIR == 2 this CTA loads rows [64 r, 64 r + 64) of
+// every K/V box (r = cluster rank) into both CTAs of the cluster.
 template <int D, int PAIR>
-__device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUtensorMap &tmV, const Params &P,
-                                              const Unit &U, uint8_t *smem, Barriers &bar) {
+__device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                              const Params &P, uint8_t *smem, Barriers &bar) {
     using L = SmemLayout<D>;
     volatile int *abort = &bar.abort;
-    const int n = U.n_tiles;
-    const int kv_head = U.b * P.Hkv + U.g;
-    // One tile (K or V, rows key0..key0+127) into half `half` of stage st.
-    auto load_tile = [&](int st, int half, const CUtensorMap *map, int t) {
-        const int key0 = (U.t_begin + t) * kBN;
-#pragma unroll
-        for (int c = 0; c < L::kBoxes; ++c) {
-            uint8_t *dst = smem + L::kRing + st * L::kStageBytes + half * L::kKVBytes + c * (kBN * kSwRowBytes);
-            if (PAIR == 2) {
-                const int r = (int)(blockIdx.x & 1);
-                tma_load_3d_multicast(dst + r * (kBN / 2) * kSwRowBytes, map, &bar.full[st], c * 64,
-                                      key0 + r * (kBN / 2), kv_head, (uint16_t)0x3);
-            } else {
-                tma_load_3d(dst, map, &bar.full[st], c * 64, key0, kv_head);
-            }
-        }
-    };
+    const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
+    const Schedule sched = make_schedule<PAIR>(P);
     int issued[kMaxStages] = {};
+    int q_issued = 0;
     RingPos put;
     bool first_pass = true;
-    // Stage use 0: K_0 (and K_1); use 1 + j: V_j (and K_{j+2}).
-    for (int use = 0; use <= n; ++use) {
-        const int st = put.st;
-        // From the second pass on, wait for the release of the stage's previous use.
-        if (!first_pass && !mbar_wait(&bar.empty[st], put.ph ^ 1u, abort)) break;
-        const bool second = use == 0 ? n > 1 : use + 1 < n;  // K_1, or K_{j+2}
-        mbar_arrive_expect_tx(&bar.full[st], (second ? 2 : 1) * L::kKVBytes);  // halves from both CTAs land here
-        if (use == 0) {
-            load_tile(st, 0, &tmK, 0);
-            if (second) load_tile(st, 1, &tmK, 1);
-        } else {
-            load_tile(st, 0, &tmV, use - 1);
-            if (second) load_tile(st, 1, &tmK, use + 1);
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int u = sched.unit_at(r);
+        if (u < 0) break;
+        const Unit U = make_unit<PAIR>(P, u, rank);
+        const int n = U.n_tiles;
+        if (n == 0) continue;
+        const int kv_head = U.b * P.Hkv + U.g;
+        // One tile (K or V) into half `half` of stage st.
+        auto load_tile = [&](int st, int half, const CUtensorMap *map, int t) {
+            const int key0 = (U.t_begin + t) * kBN;
+#pragma unroll
+            for (int c = 0; c < L::kBoxes; ++c) {
+                uint8_t *dst = smem + L::kRing + st * L::kStageBytes + half * L::kKVBytes + c * (kBN * kSwRowBytes);
+                if (PAIR == 2)
+                    tma_load_3d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &bar.full[st], c * 64,
+                                          key0 + rank * (kBN / 2), kv_head, (uint16_t)0x3);
+                else
+                    tma_load_3d(dst, map, &bar.full[st], c * 64, key0, kv_head);
+            }
+        };
+        // Stage use 0: K_0 (and K_1); use 1 + j: V_j (and K_{j+2}).
+        for (int use = 0; use <= n; ++use) {
+            const int st = put.st;
+            // From the second pass on, wait for the release of the stage's previous use.
+            if (!first_pass && !(ok = mbar_wait(&bar.empty[st], put.ph ^ 1u, abort))) break;
+            const bool second = use == 0 ? n > 1 : use + 1 < n;
+            mbar_arrive_expect_tx(&bar.full[st], (second ? 2 : 1) * L::kKVBytes);  // halves from both CTAs
+            if (use == 0) {
+                load_tile(st, 0, &tmK, 0);
+                if (second) load_tile(st, 1, &tmK, 1);
+            } else {
+                load_tile(st, 0, &tmV, use - 1);
+                if (second) load_tile(st, 1, &tmK, use + 1);
+            }
+            ++issued[st];
+            put.template advance<L::kStages>();
+            if (put.st == 0) first_pass = false;
+            if (use == 0) {
+                // Q of this unit, once the previous unit's S MMAs are done with the buffer.
+                if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
+                mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
+#pragma unroll
+                for (int c = 0; c < L::kBoxes; ++c)
+                    tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.bh);
+                ++q_issued;
+            }
         }
-        ++issued[st];
-        put.template advance<L::kStages>();
-        if (put.st == 0) first_pass = false;
     }
     if (*abort) {
         // Drain: every copy issued above lands before shared memory goes away.
         int never = 0;
+        if (q_issued > 0) mbar_wait(&bar.q_full, (q_issued - 1) & 1, &never, 200000000ull);
         for (int s = 0; s < L::kStages; ++s)
             if (issued[s] > 0) mbar_wait(&bar.full[s], (issued[s] - 1) & 1, &never, 200000000ull);
     }
@@ -279,14 +305,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUte
 // MMA issuer (one thread).  tcgen05.mma issue returns at about the tensor
 // core's execution rate (its queue holds two or so MMAs), so every barrier
 // operation between MMAs can idle the tensor core: per tile j the issuer
-// waits for P_j, issues O += P_j V_j, checks the next stage (V_{j+1}, K_{j+3})
-// in the shadow of those MMAs, issues S_{j+2}, then commits.
+// waits for P_j, issues O += P_j V_j, checks the next stage in the shadow of
+// those MMAs, issues S_{j+2}, then commits.  The first P_j V_j of a unit
+// overwrites O; the softmax warps read the previous unit's O before they
+// release P_0, so O is free by then.
 template <int D, int PAIR>
-__device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers &bar, uint32_t tbase) {
+__device__ __forceinline__ void mma_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using L = SmemLayout<D>;
     volatile int *abort = &bar.abort;
-    const int n = U.n_tiles;
-    const uint32_t q_tmem = tbase + kColQ;
+    const Schedule sched = make_schedule<PAIR>(P);
+    const Desc qd = make_desc(smem_u32(smem + L::kQ), 16, 1024);
     // Stage st starts (st * kStageBytes) >> 4 descriptor units after stage 0;
     // its second tile kKVBytes >> 4 units further.
     const Desc k0 = make_desc(smem_u32(smem + L::kRing), 16, 1024);
@@ -300,41 +328,51 @@ __device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers 
             mma_commit(&bar.empty[st]);
     };
     RingPos take;
-
-    bool ok = mbar_wait(&bar.q_full, 0, abort) && mbar_wait(&bar.full[take.st], take.ph, abort);
-    if (ok) {
-        // S_0 and S_1 before any softmax work.
+    int gt = 0;     // tiles before this unit (global tile count)
+    int units = 0;  // non-empty units before this one
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int u = sched.unit_at(r);
+        if (u < 0) break;
+        const int n = make_unit<PAIR>(P, u, 0).n_tiles;  // the same for both CTAs of a pair
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(&bar.full[take.st], take.ph, abort) && mbar_wait(&bar.q_full, units & 1, abort))) break;
         tc_fence_after();
-        issue_qk<D>(tbase + col_s(0), q_tmem, Desc{k0.lo + take.st * kStageUnits, k0.hi});
-        mma_commit(&bar.s_full[0]);
+        // S_0 and S_1 before any softmax work of the unit.
+        issue_qk<D>(tbase + col_s(gt & 1), qd, Desc{k0.lo + take.st * kStageUnits, k0.hi});
+        mma_commit(&bar.s_full[gt & 1]);
         if (n > 1) {
-            issue_qk<D>(tbase + col_s(1), q_tmem, Desc{k0.lo + take.st * kStageUnits + kHalfUnits, k0.hi});
-            mma_commit(&bar.s_full[1]);
+            issue_qk<D>(tbase + col_s((gt + 1) & 1), qd, Desc{k0.lo + take.st * kStageUnits + kHalfUnits, k0.hi});
+            mma_commit(&bar.s_full[(gt + 1) & 1]);
         }
+        if (n <= 2) mma_commit(&bar.q_empty);  // the unit's last S is issued
         release(take.st);
         take.template advance<L::kStages>();
-        ok = mbar_wait(&bar.full[take.st], take.ph, abort);  // V_0 (and K_2)
-    }
-    for (int j = 0; ok && j < n; ++j) {
-        const int b = j & 1;
-        const bool next = j + 2 < n;
-        const int st = take.st;
-        if (!mbar_wait(&bar.p_full[b], (j >> 1) & 1, abort)) break;
-        tc_fence_after();
-        issue_pv<D>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + st * kStageUnits, v0.hi}, j > 0 ? 1u : 0u);
-        take.template advance<L::kStages>();
-        // The next stage, while the tensor core works through the queue.
-        if (j + 1 < n && !(ok = mbar_wait(&bar.full[take.st], take.ph, abort))) break;
-        // S_{j+2} into the buffer P_j came from (issued after P_j V_j).
-        if (next) {
-            issue_qk<D>(tbase + col_s(b), q_tmem, Desc{k0.lo + st * kStageUnits + kHalfUnits, k0.hi});
-            mma_commit(&bar.s_full[b]);  // covers O += P_j V_j as well
-        } else if (j + 1 == n) {
-            mma_commit(&bar.o_final);
-        } else {
-            mma_commit(&bar.o_done);  // j == n-2: no S after it
+        if (!(ok = mbar_wait(&bar.full[take.st], take.ph, abort))) break;  // V_0 (and K_2)
+        for (int j = 0; j < n; ++j) {
+            const int g = gt + j;
+            const int b = g & 1;
+            const int st = take.st;
+            if (!(ok = mbar_wait(&bar.p_full[b], (g >> 1) & 1, abort))) break;
+            tc_fence_after();
+            issue_pv<D>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + st * kStageUnits, v0.hi}, j > 0 ? 1u : 0u);
+            take.template advance<L::kStages>();
+            // The next stage, while the tensor core works through the queue.
+            if (j + 1 < n && !(ok = mbar_wait(&bar.full[take.st], take.ph, abort))) break;
+            if (j + 2 < n) {
+                // S_{j+2} into the buffer P_j came from (issued after P_j V_j).
+                issue_qk<D>(tbase + col_s(b), qd, Desc{k0.lo + st * kStageUnits + kHalfUnits, k0.hi});
+                mma_commit(&bar.s_full[b]);  // covers O += P_j V_j as well
+                if (j + 3 == n) mma_commit(&bar.q_empty);  // the unit's last S is issued
+            } else if (j + 1 == n) {
+                mma_commit(&bar.o_final);
+            } else {
+                mma_commit(&bar.o_done);  // j == n-2: no S after it
+            }
+            release(st);
         }
-        release(st);
+        gt += n;
+        ++units;
     }
     // Every MMA issued above completes before tensor memory is freed.
     mma_commit(&bar.mma_drain);
@@ -343,225 +381,210 @@ __device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers 
 }
 
 // Softmax warps 0-3: thread = query row = TMEM lane; epilogue.
-template <int D>
-__device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Barriers &bar, uint32_t tbase,
-                                             int warp) {
+template <int D, int PAIR>
+__device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uint32_t tbase, int warp) {
     volatile int *abort = &bar.abort;
-    const int n = U.n_tiles;
+    const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
+    const Schedule sched = make_schedule<PAIR>(P);
     const int row = threadIdx.x;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t o_addr = tbase + lane_off + kColO;
-    const int i = U.r0 + row;
-    const int64_t p = (int64_t)P.q_offset + i;
-    const int64_t p_first = (int64_t)P.q_offset + U.r0;
-    const int64_t p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
-    // Per-row visible key interval [vlo, vhi) before the additive mask.
-    int64_t vlo, vhi;
-    visible_range(P, p, vlo, vhi);
     const float c = P.scale_log2;
-    const bool has_sink = P.sinks != nullptr;
-    float m = has_sink ? __ldg(P.sinks + U.h) * kLog2e : -INFINITY;  // log2 units
-    float l = has_sink ? 1.f : 0.f;
-    const float *mrow =
-        (P.mask != nullptr && i < P.Tq) ? P.mask + U.b * P.msb + U.h * P.msh + (int64_t)i * P.msq : nullptr;
+    int gt = 0;       // tiles before this unit
+    int units = 0;    // non-empty units before this one
+    int od_uses = 0;  // units that committed o_done before this one
     bool ok = true;
-    // Tiles t (relative to t_begin) in [ti_lo, ti_hi) are interior: every key
-    // visible to every row of the CTA, and no additive mask.
-    int ti_lo = 0, ti_hi = 0;
-    if (P.mask == nullptr && c > 0.f) {
-        int64_t hi_key = P.Tk;                                   // j0 + kBN <= Tk
-        if (P.causal && p_first + 1 < hi_key) hi_key = p_first + 1;  // j0 + kBN - 1 <= p_first
-        int64_t lo_key = 0;                                      // j0 > p_last - window
-        if (P.window > 0 && p_last - P.window + 1 > 0) lo_key = p_last - P.window + 1;
-        const int64_t t_lo = (lo_key + kBN - 1) / kBN, t_hi = hi_key / kBN;
-        ti_lo = (int)(t_lo - U.t_begin);
-        ti_hi = (int)(t_hi - U.t_begin);
-    }
 
-    if (n > 0) {
-        // Q row i into this lane's TMEM columns [kColQ, kColQ + D/2): the
-        // bf16 pairs of memory are the packed A-operand layout already.
-        const uint4 *qrow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
-                                                            ((int64_t)U.bh * P.Tq + (i < P.Tq ? i : 0)) * D);
-        uint32_t qr[D / 2];
+    for (int r = 0; ok; ++r) {
+        const int u = sched.unit_at(r);
+        if (u < 0) break;
+        const Unit U = make_unit<PAIR>(P, u, rank);
+        const int n = U.n_tiles;
+        const int i = U.r0 + row;
+        const int64_t p = (int64_t)P.q_offset + i;
+        const int64_t p_first = (int64_t)P.q_offset + U.r0;
+        const int64_t p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
+        // Per-row visible key interval [vlo, vhi) before the additive mask.
+        int64_t vlo, vhi;
+        visible_range(P, p, vlo, vhi);
+        const bool has_sink = P.sinks != nullptr;
+        float m = has_sink ? __ldg(P.sinks + U.h) * kLog2e : -INFINITY;  // log2 units
+        float l = has_sink ? 1.f : 0.f;
+        const float *mrow =
+            (P.mask != nullptr && i < P.Tq) ? P.mask + U.b * P.msb + U.h * P.msh + (int64_t)i * P.msq : nullptr;
+        // Tiles j in [ti_lo, ti_hi) are interior: every key visible to every
+        // row of the unit, and no additive mask.
+        int ti_lo = 0, ti_hi = 0;
+        if (P.mask == nullptr && c > 0.f) {
+            int64_t hi_key = P.Tk;                                       // j0 + kBN <= Tk
+            if (P.causal && p_first + 1 < hi_key) hi_key = p_first + 1;  // j0 + kBN - 1 <= p_first
+            int64_t lo_key = 0;                                          // j0 > p_last - window
+            if (P.window > 0 && p_last - P.window + 1 > 0) lo_key = p_last - P.window + 1;
+            ti_lo = (int)((lo_key + kBN - 1) / kBN - U.t_begin);
+            ti_hi = (int)(hi_key / kBN - U.t_begin);
+        }
+
+        for (int j = 0; j < n; ++j) {
+            const int g = gt + j;
+            const int b = g & 1;
+            const uint32_t s_addr = tbase + lane_off + col_s(b);
+            // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (g >> 1) & 1, abort)))) break;
+            tc_fence_after();
+            uint32_t sr[kBN];
+            tmem_load128(s_addr, sr);
+            float *s = reinterpret_cast<float *>(sr);
+
+            float cs = c;  // multiplier from s[] to log2 units for this tile
+            if (j < ti_lo || j >= ti_hi) {
+                const int j0 = (U.t_begin + j) * kBN;
+                // The row's visible keys in this tile: [elo, ehi) (clamped).
+                const int64_t elo64 = vlo - j0, ehi64 = vhi - j0;
+                const int elo = elo64 < -1 ? -1 : (elo64 > kBN ? kBN : (int)elo64);
+                const int ehi = ehi64 < -1 ? -1 : (ehi64 > kBN ? kBN : (int)ehi64);
+                if (mrow != nullptr) {
+                    // Additive mask: scores in log2 units; keys past Tk read a
+                    // clamped (valid) address and are dropped by the interval.
 #pragma unroll
-        for (int e = 0; e < D / 8; ++e) {
-            const uint4 v = i < P.Tq ? __ldg(qrow + e) : make_uint4(0u, 0u, 0u, 0u);
-            qr[4 * e] = v.x;
-            qr[4 * e + 1] = v.y;
-            qr[4 * e + 2] = v.z;
-            qr[4 * e + 3] = v.w;
-        }
-        if constexpr (D == 128) {
-            tmem_store64(tbase + lane_off + kColQ, qr);
-        } else {
-            tmem_store32(tbase + lane_off + kColQ, qr);
-        }
-        tc_fence_before();
-        mbar_arrive(&bar.q_full);
-    }
-
-    for (int j = 0; j < n; ++j) {
-        const int b = j & 1;
-        const uint32_t s_addr = tbase + lane_off + col_s(b);
-        // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j >> 1) & 1, abort))) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        uint32_t sr[kBN];
-        tmem_load128(s_addr, sr);
-        float *s = reinterpret_cast<float *>(sr);
-
-        float cs = c;  // multiplier from s[] to log2 units for this tile
-        if (j < ti_lo || j >= ti_hi) {
-            const int j0 = (U.t_begin + j) * kBN;
-            // The row's visible keys in this tile: [elo, ehi) (clamped).
-            const int64_t elo64 = vlo - j0, ehi64 = vhi - j0;
-            const int elo = elo64 < -1 ? -1 : (elo64 > kBN ? kBN : (int)elo64);
-            const int ehi = ehi64 < -1 ? -1 : (ehi64 > kBN ? kBN : (int)ehi64);
-            if (mrow != nullptr) {
-                // Additive mask: scores in log2 units; keys past Tk read a
-                // clamped (valid) address and are dropped by the interval.
+                    for (int e = 0; e < kBN; ++e) {
+                        const int jj = min(j0 + e, P.Tk - 1);
+                        const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
+                        s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                    }
+                    cs = 1.f;
+                } else if (c <= 0.f) {
+                    // A non-positive scale: scale first so that -inf marks the
+                    // keys the row cannot see.
 #pragma unroll
-                for (int e = 0; e < kBN; ++e) {
-                    const int jj = min(j0 + e, P.Tk - 1);
-                    const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
-                    s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                    for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
+                    cs = 1.f;
+                } else {
+                    // Boundary tile: keys outside the row's interval drop to -inf.
+#pragma unroll
+                    for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
                 }
-                cs = 1.f;
-            } else if (c <= 0.f) {
-                // A non-positive scale: scale first so that -inf marks the
-                // keys the row cannot see.
-#pragma unroll
-                for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
-                cs = 1.f;
-            } else {
-                // Boundary tile: keys outside the row's interval drop to -inf.
-#pragma unroll
-                for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
             }
-        }
-        float bm;  // tile max of s[] * cs, in log2 units
-        {
-            static_assert(kBN == 128, "max chains assume 128 keys per tile");
-            float mx[8];  // eight independent chains of three-input max
+            float bm;  // tile max of s[] * cs, in log2 units
+            {
+                static_assert(kBN == 128, "max chains assume 128 keys per tile");
+                float mx[8];  // eight independent chains of three-input max
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);  // keys 0..23
+                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);  // keys 0..23
 #pragma unroll
-            for (int e = 24; e < 120; e += 16)  // keys 24..119
+                for (int e = 24; e < 120; e += 16)  // keys 24..119
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
+                    for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[120 + c8]);  // keys 120..127
-            bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
-        }
+                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[120 + c8]);  // keys 120..127
+                bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
+            }
 
-        // Lazy max: move m only when the tile exceeds it by the threshold
-        // (with m = -inf any finite tile max does, and 2^(-inf) = 0).
-        float alpha = 1.f;
-        if (bm > m + kRescaleThreshold) {
-            alpha = ex2_approx(m - bm);
-            m = bm;
-        }
-        const float shift = (m == -INFINITY) ? 0.f : m;
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-            // O must hold P_{j-1} V_{j-1} before it is rescaled: the commit
-            // after S_{j+1} (issued after it) shows that, or, for the last
-            // tile, the commit after O += P_{n-2} V_{n-2}.
-            const bool via_s = j + 1 < n;
-            uint64_t *bo = via_s ? &bar.s_full[(j + 1) & 1] : &bar.o_done;
-            const uint32_t ph = via_s ? (uint32_t)(((j + 1) >> 1) & 1) : 0u;
-            if (!__all_sync(0xffffffffu, mbar_wait(bo, ph, abort))) {
-                ok = false;
-                break;
+            // Lazy max: move m only when the tile exceeds it by the threshold
+            // (with m = -inf any finite tile max does, and 2^(-inf) = 0).
+            float alpha = 1.f;
+            if (bm > m + kRescaleThreshold) {
+                alpha = ex2_approx(m - bm);
+                m = bm;
             }
+            const float shift = (m == -INFINITY) ? 0.f : m;
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O must hold P_{j-1} V_{j-1} before it is rescaled: the commit
+                // after S_{j+1} (issued after it) shows that, or, for the last
+                // tile, the commit after O += P_{n-2} V_{n-2}.
+                const bool via_s = j + 1 < n;
+                uint64_t *bo = via_s ? &bar.s_full[(g + 1) & 1] : &bar.o_done;
+                const uint32_t ph = via_s ? (uint32_t)(((g + 1) >> 1) & 1) : (uint32_t)(od_uses & 1);
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bo, ph, abort)))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t orr[32];
+                    tmem_load32(o_addr + cc * 32, orr);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 v = fmul2(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])),
+                                               make_float2(alpha, alpha));
+                        orr[e] = __float_as_uint(v.x);
+                        orr[e + 1] = __float_as_uint(v.y);
+                    }
+                    tmem_store32(o_addr + cc * 32, orr);
+                }
+            }
+
+            // p = 2^(s cs - shift), rounded to bf16 pairs; row sum in fp32.
+            const float2 cs2 = make_float2(cs, cs), nsh2 = make_float2(-shift, -shift);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int e = 0; e < kBN; e += 4) {
+                const float2 x0 = ffma2(make_float2(s[e], s[e + 1]), cs2, nsh2);
+                const float2 x1 = ffma2(make_float2(s[e + 2], s[e + 3]), cs2, nsh2);
+                const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+                const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+                acc0 = fadd2(acc0, p0);
+                acc1 = fadd2(acc1, p1);
+                pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
+                pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
+            }
+            tmem_store64(s_addr, pk);
+            tc_fence_before();
+            mbar_arrive(&bar.p_full[b]);
+            const float2 a = fadd2(acc0, acc1);
+            l = fmaf(alpha, l, a.x + a.y);
+        }
+        if (!ok) break;
+
+        // Epilogue: o = O / l (0 for an empty row), lse = (m + log2 l) ln 2.
+        // O leaves tensor memory first: the next unit's first P V overwrites
+        // it once this thread has released that unit's P_0.
+        uint32_t ov[D];
+        if (n > 0) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t orr[32];
-                tmem_load32(o_addr + cc * 32, orr);
+            for (int cc = 0; cc < D / 32; ++cc)
+                tmem_load32(o_addr + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(ov + cc * 32));
+            tc_fence_before();
+        } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float2 v = fmul2(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])),
-                                           make_float2(alpha, alpha));
-                    orr[e] = __float_as_uint(v.x);
-                    orr[e + 1] = __float_as_uint(v.y);
-                }
-                tmem_store32(o_addr + cc * 32, orr);
-            }
+            for (int e = 0; e < D; ++e) ov[e] = 0u;
         }
-
-        // p = 2^(s cs - shift), rounded to bf16 pairs; row sum in fp32.
-        const float2 cs2 = make_float2(cs, cs), nsh2 = make_float2(-shift, -shift);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-        uint32_t pk[kBN / 2];
-#pragma unroll
-        for (int e = 0; e < kBN; e += 4) {
-            const float2 x0 = ffma2(make_float2(s[e], s[e + 1]), cs2, nsh2);
-            const float2 x1 = ffma2(make_float2(s[e + 2], s[e + 3]), cs2, nsh2);
-            const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-            const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-            acc0 = fadd2(acc0, p0);
-            acc1 = fadd2(acc1, p1);
-            pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
-            pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
-        }
-        tmem_store64(s_addr, pk);
-        tc_fence_before();
-        mbar_arrive(&bar.p_full[b]);
-        const float2 a = fadd2(acc0, acc1);
-        l = fmaf(alpha, l, a.x + a.y);
-    }
-
-    if (ok && n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, 0, abort));
-        tc_fence_after();
-    }
-    if (ok) {
-        // Epilogue: o = O / l (0 for an empty row), lse = (m + log2 l) ln 2.
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)U.bh * P.Tq + i) * D;
+        if (i < P.Tq) {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)U.bh * P.Tq + i) * D);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t orr[32];
-            if (n > 0) {
-                tmem_load32(o_addr + cc * 32, orr);
-            } else {
+            for (int e = 0; e < D / 8; ++e) {
+                uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) orr[e] = 0u;
+                for (int k = 0; k < 4; ++k)
+                    w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
+                                      __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
+                dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                w[e] = cvt_bf16x2(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
-            if (i < P.Tq) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-            }
+            if (P.lse != nullptr) P.lse[(int64_t)U.bh * P.Tq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
-        if (P.lse != nullptr && i < P.Tq) P.lse[(int64_t)U.bh * P.Tq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        gt += n;
+        if (n > 0) ++units;
+        if (n > 1) ++od_uses;
     }
 }
 
 template <int D, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                       const Params P) {
+    fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const Params P) {
     using L = SmemLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Barriers &bar = *reinterpret_cast<Barriers *>(smem + L::kBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Unit U = decode_unit<PAIR>(P);
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar.q_full, kBM);
+        mbar_init(&bar.q_full, 1);
+        mbar_init(&bar.q_empty, 1);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(&bar.full[s], 1);
-            mbar_init(&bar.empty[s], PAIR);  // one release per CTA reading the slot
+            mbar_init(&bar.empty[s], PAIR);  // one release per CTA reading the stage
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar.s_full[s], 1);
@@ -578,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
@@ -594,11 +618,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_launch_dependents();
 
     if (warp == kWarpTma) {
-        if (lane == 0 && U.n_tiles > 0) producer_role<D, PAIR>(tmK, tmV, P, U, smem, bar);
+        if (lane == 0) producer_role<D, PAIR>(tmQ, tmK, tmV, P, smem, bar);
     } else if (warp == kWarpMma) {
-        if (lane == 0 && U.n_tiles > 0) mma_role<D, PAIR>(U, smem, bar, tbase);
+        if (lane == 0) mma_role<D, PAIR>(P, smem, bar, tbase);
     } else {
-        softmax_role<D>(P, U, bar, tbase, warp);
+        softmax_role<D, PAIR>(P, bar, tbase, warp);
     }
 
     tc_fence_before();
@@ -644,17 +668,31 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 template <int D, int PAIR>
 cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    CUtensorMap tk, tv;
+    CUtensorMap tq, tk, tv;
     // With Tk == 0 no key tile is ever loaded; the K/V maps only need to be valid.
     const void *kb = P.Tk > 0 ? P.k : P.q;
     const void *vb = P.Tk > 0 ? P.v : P.q;
     const int krows = P.Tk > 0 ? P.Tk : 1;
     const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
-    if (!make_map(enc, &tk, kb, D, krows, kheads, kBN / PAIR) || !make_map(enc, &tv, vb, D, krows, kheads, kBN / PAIR))
+    if (!make_map(enc, &tq, P.q, D, P.Tq, P.B * P.Hq, kBM) || !make_map(enc, &tk, kb, D, krows, kheads, kBN / PAIR) ||
+        !make_map(enc, &tv, vb, D, krows, kheads, kBN / PAIR))
         return cudaErrorInvalidValue;
     // The CTA takes all 512 tensor-memory columns; the shared-memory request
     // (the K/V ring fills it) keeps a second CTA off the SM.
@@ -667,9 +705,14 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    // One CTA (pair) per SM, no more than there are units.
     const int nqt = (P.Tq + kBM - 1) / kBM;
+    const long long units = (long long)nqt * (PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq);
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const long long groups = units < sms / PAIR ? units : sms / PAIR;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)nqt * (unsigned)(P.B * P.Hq));
+    cfg.gridDim = dim3((unsigned)(groups * PAIR));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
@@ -682,7 +725,7 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR>, tk, tv, P);
+    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR>, tq, tk, tv, P);
 }
 
 }  // namespace
