@@ -159,6 +159,80 @@ def time_graph(fn, reps, flush, warm=3):
     return statistics.median(ms), ms
 
 
+# FP32 SIMT peak of the GB300: 152 SMs x 128 FFMA lanes x 2 FLOP x 2.07 GHz.
+FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def measure_other_paths(fa, dev, flush):
+    """fp32 28-layer prefill, fp32 masked batch, windowed-sink chunked prompt
+    (bf16 and fp32): device time per configuration from CUDA graphs."""
+    import torch
+    out = []
+
+    def entry(name, dtype, fn, flops, reps=10):
+        med, _ = time_graph(fn, reps, flush)
+        tf = flops / (med / 1e3) / 1e12
+        e = {"workload": name, "dtype": dtype, "ms": round(med, 4), "tflops": round(tf, 2)}
+        if dtype == "f32":
+            e["frac_of_fp32_simt_peak"] = round(tf / FP32_SIMT_PEAK_TFLOPS, 4)
+        out.append(e)
+
+    # 28 x 511-token layers in fp32
+    p = workloads.CONFIGS["prefill511_gqa16x8_d128_x28"].problem
+    layers = []
+    for layer in range(28):
+        q, k, v = workloads.qkv(layer, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float32)
+        layers.append((q.to(dev), k.to(dev), v.to(dev), torch.empty((p.B, p.Hq, p.Tq, p.d), device=dev),
+                       torch.empty((p.B, p.Hq, p.Tq), device=dev)))
+
+    def prefill_f32():
+        for q, k, v, o, lse in layers:
+            fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0, 0,
+                      0, fa.FA_DTYPE_F32, None)
+
+    entry("prefill511_gqa16x8_d128_x28", "f32", prefill_f32, 28 * p.flops(), reps=5)
+    del layers
+
+    # additive-mask batch, fp32
+    w = workloads.CONFIGS["mask_b4h8_t1024_d96"]
+    p = w.problem
+    q, k, v = [t.to(dev) for t in workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float32)]
+    m = workloads.strided_mask(w.extra["mask_seed"], p.Tq, p.Tk).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((p.B, p.Hq, p.Tq), device=dev)
+
+    def masked():
+        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 0, 0, None, m, 0, 0, p.Tk, 1,
+                  fa.FA_DTYPE_F32, None)
+
+    entry("mask_b4h8_t1024_d96", "f32", masked, p.flops())
+
+    # windowed GQA with sinks, 4096 tokens as chunks of 1000 (keys so far per chunk)
+    w = workloads.CONFIGS["window128_sinks_gqa32x4_d64_chunked"]
+    p = w.problem
+    z = workloads.sinks(w.extra["sink_seed"], p.Hq).to(dev)
+    for dt, code in (("bf16", fa.FA_DTYPE_BF16), ("f32", fa.FA_DTYPE_F32)):
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+        q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, tdt)
+        chunks, flops = [], 0
+        for start, n in workloads.chunk_ranges(p.Tq, w.extra["chunk"]):
+            cp = workloads.Problem(p.B, p.Hq, p.Hkv, n, start + n, p.d, causal=True, window=p.window,
+                                   q_offset=start)
+            flops += cp.flops()
+            chunks.append((start, n, q[:, :, start:start + n].contiguous().to(dev),
+                           k[:, :, :start + n].contiguous().to(dev), v[:, :, :start + n].contiguous().to(dev),
+                           torch.empty((p.B, p.Hq, n, p.d), dtype=tdt, device=dev),
+                           torch.empty((p.B, p.Hq, n), device=dev)))
+
+        def chunked():
+            for start, n, qc, kc, vc, oc, lc in chunks:
+                fa.fa_fwd(qc, kc, vc, oc, lc, p.B, p.Hq, p.Hkv, n, start + n, p.d, p.sm_scale, start, 1, p.window,
+                          z, None, 0, 0, 0, 0, code, None)
+
+        entry("window128_sinks_gqa32x4_d64_chunked", dt, chunked, flops)
+    return out
+
+
 # ------------------------------------------------------------------ oracle
 
 def time_oracle_layers(max_seconds: float, max_layers: int = 28):
@@ -352,6 +426,12 @@ def run_fa(args, rank, world, local_rank):
                              "frac_of_measured_peak": round(tf / peak_burst, 4)})
             del q, k, v, o, lse
 
+    # The other configurations of the hot path: the fp32 SIMT kernel and the
+    # windowed-sink chunked prompt, each timed from a CUDA graph.
+    others = []
+    if not args.skip_long and rank == 0:
+        others = measure_other_paths(fa, dev, flush)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         fl, secs, nl, thr = time_oracle_layers(args.cpu_seconds)
@@ -397,6 +477,7 @@ def run_fa(args, rank, world, local_rank):
                      "kernel": "fa_fwd_bf16_kernel<128>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
         "clocks": sampler.summary(),
         "long_context": long_ctx,
+        "other_paths": others,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
