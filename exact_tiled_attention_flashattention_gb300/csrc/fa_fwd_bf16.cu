@@ -12,10 +12,10 @@
 //                          the first 64 columns of S_t's buffer
 //   O  += P_t V_t          tcgen05.mma, A = P_t from TMEM, B = V_t (MN-major)
 //
-// S is double-buffered in tensor memory (S_A, S_B), so the issuer computes
-// S_{t+1} while the softmax warps work on S_t.  S_{t+2} reuses the buffer of
-// P_t and is issued after O += P_t V_t: tcgen05.mma operations issued by one
-// thread execute in order.
+// S has three buffers in tensor memory and two threads issue the MMAs: one
+// computes S_{t+1}, S_{t+2} while the softmax warps work on S_t, the other
+// accumulates O += P_t V_t.  S_{t+3} reuses the buffer of P_t and waits for
+// the completion of O += P_t V_t.
 //
 // The running max m of a row is raised lazily: only when a tile's max
 // exceeds it by more than 8 (log2 units) is O rescaled in TMEM by
@@ -28,24 +28,25 @@
 // sorted heaviest first (under a causal rule the last query tiles see the
 // most keys), taking them in snake order (round r takes group g, the next
 // round group G-1-g), so heavy and light units balance across SMs.  The K/V
-// ring, the S buffers and every barrier run on across units: the next unit's
-// K_0, K_1 and Q load while the current unit finishes, its S_0, S_1 run while
-// the softmax warps write the current unit's output.
+// rings, the S buffers and every barrier run on across units: the next unit's
+// K_0, K_1 and Q load while the current unit finishes, its first S tiles run
+// while the softmax warps write the current unit's output.
 //
 // K/V sharing: when the GQA group size is even, the two query heads of a KV
 // head at the same rows run as a cluster of two CTAs.  Each CTA loads half of
 // every K/V tile (64 of its 128 rows) with a multicast TMA that lands in both
 // CTAs' shared memory, and a ring slot is refilled only after both CTAs'
 // tensor cores released it (a multicast tcgen05.commit arrives on the slot's
-// barrier in both CTAs).  Each ring stage holds the two tiles one issuer step
-// consumes (V_j and K_{j+2}; the unit's first stage K_0 and K_1).
+// barrier in both CTAs).  K and V tiles have rings of their own, each read by
+// one issuing thread.
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3   softmax: thread t = query row t = TMEM lane t; epilogue
 //   warp 4      TMA producer (one lane)
-//   warp 5      MMA issuer (one lane) and tensor-memory owner
-// Tensor memory (512 columns allocated): S_A [0,128) S_B [128,256)
-// O [256, 256+d).
+//   warp 5      S = Q K^T issuer (one lane) and tensor-memory owner
+//   warp 6      O += P V issuer (one lane)
+// Tensor memory (512 columns allocated): S_0 [0,128) S_1 [128,256)
+// S_2 [256,384) O [384, 384+d).
 //
 // A row's arithmetic does not depend on its query tile, its unit's place in
 // the schedule or on chunking through q_offset: key tiles are absolute, a key
@@ -78,11 +79,12 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // query rows per unit = tensor-memory lanes
 constexpr int kBN = 128;  // keys per tile
-constexpr int kThreads = 192;
-constexpr int kWarpTma = 4, kWarpMma = 5;
+constexpr int kThreads = 224;
+constexpr int kWarpTma = 4, kWarpQk = 5, kWarpPv = 6;
 constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int buf) { return 128u * buf; }  // S_A, S_B (and P)
-constexpr uint32_t kColO = 256;
+constexpr int kSBufs = 3;                                                     // S (and P) buffers
+__host__ __device__ constexpr uint32_t col_s(int buf) { return 128u * buf; }  // S_0, S_1, S_2
+constexpr uint32_t kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay below 2^8
@@ -93,25 +95,26 @@ template <int D>
 struct SmemLayout {
     static constexpr int kBoxes = D / 64;  // 64-column TMA boxes per tile
     static constexpr uint32_t kQBytes = kBM * D * 2;
-    static constexpr uint32_t kKVBytes = kBN * D * 2;
-    static constexpr uint32_t kStageBytes = 2 * kKVBytes;  // two tiles per stage
-    static constexpr int kStages = D == 128 ? 3 : 6;       // 192 KB ring
+    static constexpr uint32_t kKVBytes = kBN * D * 2;     // one K or V tile (a ring stage)
+    static constexpr int kStages = D == 128 ? 3 : 6;      // per ring: 96 KB each
     static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kRing = kQ + kQBytes;
-    static constexpr uint32_t kBar = kRing + kStages * kStageBytes;
+    static constexpr uint32_t kKRing = kQ + kQBytes;
+    static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
+    static constexpr uint32_t kBar = kVRing + kStages * kKVBytes;
     static constexpr uint32_t kTotal = kBar + 512;
     static_assert(kStages <= kMaxStages, "ring too deep");
 };
 
 struct Barriers {
-    uint64_t q_full;                               // Q of the unit landed
-    uint64_t q_empty;                              // the unit's last S done: Q buffer free
-    uint64_t full[kMaxStages], empty[kMaxStages];  // the K/V ring
-    uint64_t s_full[2];                            // S_A, S_B written
-    uint64_t p_full[2];                            // P in S_A, S_B written
-    uint64_t o_done;                               // O += P_{n-2} V_{n-2} completed
-    uint64_t o_final;                              // the unit's last O += P V completed
-    uint64_t mma_drain;
+    uint64_t q_full;                                   // Q of the unit landed
+    uint64_t q_empty;                                  // the unit's last S done: Q buffer free
+    uint64_t k_full[kMaxStages], k_empty[kMaxStages];  // the K ring
+    uint64_t v_full[kMaxStages], v_empty[kMaxStages];  // the V ring
+    uint64_t s_full[kSBufs];                           // S written into buffer b
+    uint64_t p_full[kSBufs];                           // P written over S in buffer b
+    uint64_t o_done[kSBufs];                           // O += P V from buffer b completed
+    uint64_t o_final;                                  // the unit's last O += P V completed
+    uint64_t drain[2];                                 // issuers' last MMAs completed
     uint32_t tmem_base;
     int abort;
 };
@@ -229,9 +232,9 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc 
         mma_ts_c<1>(o_tmem, p_tmem + kk * 8, v.lo + ((kk * 16 * kSwRowBytes) >> 4), v.hi, kId);
 }
 
-// TMA producer (one thread).  Per unit: the first stage (K_0, K_1), then Q
-// once the previous unit's last S has released the Q buffer, then the stages
-// (V_j, K_{j+2}).  With PAIR == 2 this CTA loads rows [64 r, 64 r + 64) of
+// TMA producer (one thread).  Per unit: K_0 and K_1, then Q once the previous
+// unit's last S has released the Q buffer, then V_j and K_{j+2} in turn, each
+// into its own ring.  With PAIR == 2 this CTA loads rows [64 r, 64 r + 64) of
 // every K/V box (r = cluster rank) into both CTAs of the cluster.
 template <int D, int PAIR>
 __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
@@ -240,10 +243,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
     const Schedule sched = make_schedule<PAIR>(P);
-    int issued[kMaxStages] = {};
+    int k_issued[kMaxStages] = {}, v_issued[kMaxStages] = {};
     int q_issued = 0;
-    RingPos put;
-    bool first_pass = true;
+    RingPos kput, vput;
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
@@ -252,132 +254,148 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         const int n = U.n_tiles;
         if (n == 0) continue;
         const int kv_head = U.b * P.Hkv + U.g;
-        // One tile (K or V) into half `half` of stage st.
-        auto load_tile = [&](int st, int half, const CUtensorMap *map, int t) {
+        // Tile t of the unit into the next stage of a ring; the stage is
+        // refilled once every CTA reading it released its previous use.
+        auto load_tile = [&](uint32_t ring, uint64_t *full, uint64_t *empty, int *issued, RingPos &pos,
+                             const CUtensorMap *map, int t) -> bool {
+            const int st = pos.st;
+            if (issued[st] > 0 && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
+            mbar_arrive_expect_tx(&full[st], L::kKVBytes);  // halves from both CTAs
             const int key0 = (U.t_begin + t) * kBN;
 #pragma unroll
             for (int c = 0; c < L::kBoxes; ++c) {
-                uint8_t *dst = smem + L::kRing + st * L::kStageBytes + half * L::kKVBytes + c * (kBN * kSwRowBytes);
+                uint8_t *dst = smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes);
                 if (PAIR == 2)
-                    tma_load_3d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &bar.full[st], c * 64,
+                    tma_load_3d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * 64,
                                           key0 + rank * (kBN / 2), kv_head, (uint16_t)0x3);
                 else
-                    tma_load_3d(dst, map, &bar.full[st], c * 64, key0, kv_head);
-            }
-        };
-        // Stage use 0: K_0 (and K_1); use 1 + j: V_j (and K_{j+2}).
-        for (int use = 0; use <= n; ++use) {
-            const int st = put.st;
-            // From the second pass on, wait for the release of the stage's previous use.
-            if (!first_pass && !(ok = mbar_wait(&bar.empty[st], put.ph ^ 1u, abort))) break;
-            const bool second = use == 0 ? n > 1 : use + 1 < n;
-            mbar_arrive_expect_tx(&bar.full[st], (second ? 2 : 1) * L::kKVBytes);  // halves from both CTAs
-            if (use == 0) {
-                load_tile(st, 0, &tmK, 0);
-                if (second) load_tile(st, 1, &tmK, 1);
-            } else {
-                load_tile(st, 0, &tmV, use - 1);
-                if (second) load_tile(st, 1, &tmK, use + 1);
+                    tma_load_3d(dst, map, &full[st], c * 64, key0, kv_head);
             }
             ++issued[st];
-            put.template advance<L::kStages>();
-            if (put.st == 0) first_pass = false;
-            if (use == 0) {
-                // Q of this unit, once the previous unit's S MMAs are done with the buffer.
-                if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
-                mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
+            pos.template advance<L::kStages>();
+            return true;
+        };
+        auto load_k = [&](int t) { return load_tile(L::kKRing, bar.k_full, bar.k_empty, k_issued, kput, &tmK, t); };
+        auto load_v = [&](int t) { return load_tile(L::kVRing, bar.v_full, bar.v_empty, v_issued, vput, &tmV, t); };
+        if (!(ok = load_k(0))) break;
+        if (n > 1 && !(ok = load_k(1))) break;
+        // Q of this unit, once the previous unit's S MMAs are done with the buffer.
+        if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
+        mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
 #pragma unroll
-                for (int c = 0; c < L::kBoxes; ++c)
-                    tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.bh);
-                ++q_issued;
-            }
+        for (int c = 0; c < L::kBoxes; ++c)
+            tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.bh);
+        ++q_issued;
+        for (int j = 0; j < n && ok; ++j) {
+            ok = load_v(j);
+            if (ok && j + 2 < n) ok = load_k(j + 2);
         }
     }
     if (*abort) {
         // Drain: every copy issued above lands before shared memory goes away.
         int never = 0;
         if (q_issued > 0) mbar_wait(&bar.q_full, (q_issued - 1) & 1, &never, 200000000ull);
-        for (int s = 0; s < L::kStages; ++s)
-            if (issued[s] > 0) mbar_wait(&bar.full[s], (issued[s] - 1) & 1, &never, 200000000ull);
+        for (int s = 0; s < L::kStages; ++s) {
+            if (k_issued[s] > 0) mbar_wait(&bar.k_full[s], (k_issued[s] - 1) & 1, &never, 200000000ull);
+            if (v_issued[s] > 0) mbar_wait(&bar.v_full[s], (v_issued[s] - 1) & 1, &never, 200000000ull);
+        }
     }
 }
 
-// MMA issuer (one thread).  tcgen05.mma issue returns at about the tensor
-// core's execution rate (its queue holds two or so MMAs), so every barrier
-// operation between MMAs can idle the tensor core: per tile j the issuer
-// waits for P_j, issues O += P_j V_j, checks the next stage in the shadow of
-// those MMAs, issues S_{j+2}, then commits.  The first P_j V_j of a unit
-// overwrites O; the softmax warps read the previous unit's O before they
-// release P_0, so O is free by then.
+// The tensor core is fed by two issuing threads, so that the barrier work of
+// one (waits and commits, a few hundred cycles each, during which a single
+// issuer's queue of two or so MMAs runs dry) is covered by the other's MMAs.
+// Tile k of the CTA's walk (k counts across units) uses S buffer k % 3:
+//   QK issuer   S_k = Q K_k^T into buffer k % 3 once O += P_{k-3} V_{k-3}
+//               (the buffer's previous content) has completed
+//   PV issuer   O += P_k V_k once the softmax warps have written P_k
+// The QK issuer runs up to two tiles ahead, so the softmax warps find the
+// next S ready.  Each ring has one reader per CTA, so stage releases cannot
+// cross phases.
+
+// A ring stage is free once every CTA that reads it has finished with it.
+template <int PAIR>
+__device__ __forceinline__ void release_stage(uint64_t *empty) {
+    if (PAIR == 2)
+        mma_commit_multicast(empty, (uint16_t)0x3);
+    else
+        mma_commit(empty);
+}
+
 template <int D, int PAIR>
-__device__ __forceinline__ void mma_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
+__device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using L = SmemLayout<D>;
     volatile int *abort = &bar.abort;
     const Schedule sched = make_schedule<PAIR>(P);
     const Desc qd = make_desc(smem_u32(smem + L::kQ), 16, 1024);
-    // Stage st starts (st * kStageBytes) >> 4 descriptor units after stage 0;
-    // its second tile kKVBytes >> 4 units further.
-    const Desc k0 = make_desc(smem_u32(smem + L::kRing), 16, 1024);
-    const Desc v0 = make_desc(smem_u32(smem + L::kRing), kBN * kSwRowBytes, 1024);
-    constexpr uint32_t kStageUnits = L::kStageBytes >> 4, kHalfUnits = L::kKVBytes >> 4;
-    // A stage is free once every CTA that reads it has finished with it.
-    auto release = [&](int st) {
-        if (PAIR == 2)
-            mma_commit_multicast(&bar.empty[st], (uint16_t)0x3);
-        else
-            mma_commit(&bar.empty[st]);
-    };
+    const Desc k0 = make_desc(smem_u32(smem + L::kKRing), 16, 1024);
+    constexpr uint32_t kTileUnits = L::kKVBytes >> 4;  // one stage, in descriptor units
     RingPos take;
-    int gt = 0;     // tiles before this unit (global tile count)
-    int units = 0;  // non-empty units before this one
+    RingPos sb;              // S buffer of the next tile and the parity of its use
+    bool first_use = true;   // no buffer has been used yet on this pass
+    int units = 0;           // non-empty units before this one
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
         const int n = make_unit<PAIR>(P, u, 0).n_tiles;  // the same for both CTAs of a pair
         if (n == 0) continue;
-        if (!(ok = mbar_wait(&bar.full[take.st], take.ph, abort) && mbar_wait(&bar.q_full, units & 1, abort))) break;
-        tc_fence_after();
-        // S_0 and S_1 before any softmax work of the unit.
-        issue_qk<D>(tbase + col_s(gt & 1), qd, Desc{k0.lo + take.st * kStageUnits, k0.hi});
-        mma_commit(&bar.s_full[gt & 1]);
-        if (n > 1) {
-            issue_qk<D>(tbase + col_s((gt + 1) & 1), qd, Desc{k0.lo + take.st * kStageUnits + kHalfUnits, k0.hi});
-            mma_commit(&bar.s_full[(gt + 1) & 1]);
-        }
-        if (n <= 2) mma_commit(&bar.q_empty);  // the unit's last S is issued
-        release(take.st);
-        take.template advance<L::kStages>();
-        if (!(ok = mbar_wait(&bar.full[take.st], take.ph, abort))) break;  // V_0 (and K_2)
+        if (!(ok = mbar_wait(&bar.q_full, units & 1, abort))) break;
         for (int j = 0; j < n; ++j) {
-            const int g = gt + j;
-            const int b = g & 1;
-            const int st = take.st;
-            if (!(ok = mbar_wait(&bar.p_full[b], (g >> 1) & 1, abort))) break;
+            const int b = sb.st;
+            if (!(ok = mbar_wait(&bar.k_full[take.st], take.ph, abort))) break;
+            // the buffer's previous use: O += P V from it completed
+            if (!first_use && !(ok = mbar_wait(&bar.o_done[b], sb.ph ^ 1u, abort))) break;
             tc_fence_after();
-            issue_pv<D>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + st * kStageUnits, v0.hi}, j > 0 ? 1u : 0u);
+            issue_qk<D>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
+            mma_commit(&bar.s_full[b]);
+            if (j + 1 == n) mma_commit(&bar.q_empty);  // the unit's last S is issued
+            release_stage<PAIR>(&bar.k_empty[take.st]);
             take.template advance<L::kStages>();
-            // The next stage, while the tensor core works through the queue.
-            if (j + 1 < n && !(ok = mbar_wait(&bar.full[take.st], take.ph, abort))) break;
-            if (j + 2 < n) {
-                // S_{j+2} into the buffer P_j came from (issued after P_j V_j).
-                issue_qk<D>(tbase + col_s(b), qd, Desc{k0.lo + st * kStageUnits + kHalfUnits, k0.hi});
-                mma_commit(&bar.s_full[b]);  // covers O += P_j V_j as well
-                if (j + 3 == n) mma_commit(&bar.q_empty);  // the unit's last S is issued
-            } else if (j + 1 == n) {
-                mma_commit(&bar.o_final);
-            } else {
-                mma_commit(&bar.o_done);  // j == n-2: no S after it
-            }
-            release(st);
+            sb.template advance<kSBufs>();
+            if (sb.st == 0) first_use = false;
         }
-        gt += n;
         ++units;
     }
     // Every MMA issued above completes before tensor memory is freed.
-    mma_commit(&bar.mma_drain);
+    mma_commit(&bar.drain[0]);
     int never = 0;
-    mbar_wait(&bar.mma_drain, 0, &never, 200000000ull);
+    mbar_wait(&bar.drain[0], 0, &never, 200000000ull);
+}
+
+// The first O += P_0 V_0 of a unit overwrites O; the softmax warps read the
+// previous unit's O before they release P_0, so O is free by then.
+template <int D, int PAIR>
+__device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
+    using L = SmemLayout<D>;
+    volatile int *abort = &bar.abort;
+    const Schedule sched = make_schedule<PAIR>(P);
+    const Desc v0 = make_desc(smem_u32(smem + L::kVRing), kBN * kSwRowBytes, 1024);
+    constexpr uint32_t kTileUnits = L::kKVBytes >> 4;
+    RingPos take;
+    RingPos sb;  // S buffer holding P of the next tile and the parity of its use
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+        const int u = sched.unit_at(r);
+        if (u < 0) break;
+        const int n = make_unit<PAIR>(P, u, 0).n_tiles;
+        if (n == 0) continue;
+        for (int j = 0; j < n; ++j) {
+            const int b = sb.st;
+            if (!(ok = mbar_wait(&bar.v_full[take.st], take.ph, abort))) break;
+            if (!(ok = mbar_wait(&bar.p_full[b], sb.ph, abort))) break;
+            tc_fence_after();
+            issue_pv<D>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + take.st * kTileUnits, v0.hi}, j > 0 ? 1u : 0u);
+            mma_commit(&bar.o_done[b]);
+            if (j + 1 == n) mma_commit(&bar.o_final);
+            release_stage<PAIR>(&bar.v_empty[take.st]);
+            take.template advance<L::kStages>();
+            sb.template advance<kSBufs>();
+        }
+    }
+    mma_commit(&bar.drain[1]);
+    int never = 0;
+    mbar_wait(&bar.drain[1], 0, &never, 200000000ull);
 }
 
 // Softmax warps 0-3: thread = query row = TMEM lane; epilogue.
@@ -390,9 +408,8 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t o_addr = tbase + lane_off + kColO;
     const float c = P.scale_log2;
-    int gt = 0;       // tiles before this unit
-    int units = 0;    // non-empty units before this one
-    int od_uses = 0;  // units that committed o_done before this one
+    RingPos sb;     // S buffer of the current tile and the parity of its use
+    int units = 0;  // non-empty units before this one
     bool ok = true;
 
     for (int r = 0; ok; ++r) {
@@ -425,11 +442,10 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
         }
 
         for (int j = 0; j < n; ++j) {
-            const int g = gt + j;
-            const int b = g & 1;
+            const int b = sb.st;
             const uint32_t s_addr = tbase + lane_off + col_s(b);
             // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (g >> 1) & 1, abort)))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], sb.ph, abort)))) break;
             tc_fence_after();
             uint32_t sr[kBN];
             tmem_load128(s_addr, sr);
@@ -488,13 +504,10 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
             }
             const float shift = (m == -INFINITY) ? 0.f : m;
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled: the commit
-                // after S_{j+1} (issued after it) shows that, or, for the last
-                // tile, the commit after O += P_{n-2} V_{n-2}.
-                const bool via_s = j + 1 < n;
-                uint64_t *bo = via_s ? &bar.s_full[(g + 1) & 1] : &bar.o_done;
-                const uint32_t ph = via_s ? (uint32_t)(((g + 1) >> 1) & 1) : (uint32_t)(od_uses & 1);
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bo, ph, abort)))) break;
+                // O must hold P_{j-1} V_{j-1} (previous buffer) before it is rescaled.
+                const int bp = b == 0 ? kSBufs - 1 : b - 1;
+                const uint32_t php = b == 0 ? sb.ph ^ 1u : sb.ph;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_done[bp], php, abort)))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
@@ -531,6 +544,7 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
             mbar_arrive(&bar.p_full[b]);
             const float2 a = fadd2(acc0, acc1);
             l = fmaf(alpha, l, a.x + a.y);
+            sb.template advance<kSBufs>();
         }
         if (!ok) break;
 
@@ -563,9 +577,7 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
             }
             if (P.lse != nullptr) P.lse[(int64_t)U.bh * P.Tq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
-        gt += n;
         if (n > 0) ++units;
-        if (n > 1) ++od_uses;
     }
 }
 
@@ -583,20 +595,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar.q_full, 1);
         mbar_init(&bar.q_empty, 1);
         for (int s = 0; s < L::kStages; ++s) {
-            mbar_init(&bar.full[s], 1);
-            mbar_init(&bar.empty[s], PAIR);  // one release per CTA reading the stage
+            mbar_init(&bar.k_full[s], 1);
+            mbar_init(&bar.v_full[s], 1);
+            mbar_init(&bar.k_empty[s], PAIR);  // one release per CTA reading the stage
+            mbar_init(&bar.v_empty[s], PAIR);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kSBufs; ++s) {
             mbar_init(&bar.s_full[s], 1);
             mbar_init(&bar.p_full[s], kBM);
+            mbar_init(&bar.o_done[s], 1);
         }
-        mbar_init(&bar.o_done, 1);
         mbar_init(&bar.o_final, 1);
-        mbar_init(&bar.mma_drain, 1);
+        mbar_init(&bar.drain[0], 1);
+        mbar_init(&bar.drain[1], 1);
         bar.abort = 0;
         mbar_init_fence();
     }
-    if (warp == kWarpMma) {
+    if (warp == kWarpQk) {
         tmem_alloc(&bar.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -619,8 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kWarpTma) {
         if (lane == 0) producer_role<D, PAIR>(tmQ, tmK, tmV, P, smem, bar);
-    } else if (warp == kWarpMma) {
-        if (lane == 0) mma_role<D, PAIR>(P, smem, bar, tbase);
+    } else if (warp == kWarpQk) {
+        if (lane == 0) qk_role<D, PAIR>(P, smem, bar, tbase);
+    } else if (warp == kWarpPv) {
+        if (lane == 0) pv_role<D, PAIR>(P, smem, bar, tbase);
     } else {
         softmax_role<D, PAIR>(P, bar, tbase, warp);
     }
@@ -630,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // No CTA of a pair leaves while the other may still multicast into it.
     if (PAIR == 2) cluster_sync();
     if (bar.abort && threadIdx.x == 0) atomicOr(&g_watchdog, 1u);
-    if (warp == kWarpMma) {
+    if (warp == kWarpQk) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
