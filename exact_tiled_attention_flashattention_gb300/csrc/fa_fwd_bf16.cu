@@ -40,11 +40,12 @@
 // barrier in both CTAs).  K and V tiles have rings of their own, each read by
 // one issuing thread.
 //
-// Warp roles (224 threads):
-//   warps 0-3   softmax: thread t = query row t = TMEM lane t; epilogue
-//   warp 4      TMA producer (one lane)
-//   warp 5      S = Q K^T issuer (one lane) and tensor-memory owner
-//   warp 6      O += P V issuer (one lane)
+// Warp roles (352 threads):
+//   warps 0-7   softmax and epilogue: two threads per query row (= TMEM
+//               lane), each with half of the row's keys and of O's columns
+//   warp 8      TMA producer (one lane)
+//   warp 9      S = Q K^T issuer (one lane) and tensor-memory owner
+//   warp 10     O += P V issuer (one lane)
 // Tensor memory (512 columns allocated): S_0 [0,128) S_1 [128,256)
 // S_2 [256,384) O [384, 384+d).
 //
@@ -79,8 +80,9 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // query rows per unit = tensor-memory lanes
 constexpr int kBN = 128;  // keys per tile
-constexpr int kThreads = 224;
-constexpr int kWarpTma = 4, kWarpQk = 5, kWarpPv = 6;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 352;
+constexpr int kWarpTma = 8, kWarpQk = 9, kWarpPv = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                                                     // S (and P) buffers
 __host__ __device__ constexpr uint32_t col_s(int buf) { return 128u * buf; }  // S_0, S_1, S_2
@@ -398,16 +400,25 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
     mbar_wait(&bar.drain[1], 0, &never, 200000000ull);
 }
 
-// Softmax warps 0-3: thread = query row = TMEM lane; epilogue.
+// Softmax warps 0-7 and epilogue: two threads per query row.  Warp w covers
+// the 16 tensor-memory lanes from 32 (w % 4) + 16 (w / 4); in it lanes l and
+// l + 16 hold the same row, the first and second half of each tile's keys and
+// of O's columns.  Row max and row sum combine through one shuffle, and the
+// two warps on a scheduler partition hide each other's latencies.
 template <int D, int PAIR>
-__device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uint32_t tbase, int warp) {
+__device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uint32_t tbase, int warp, int lane) {
+    constexpr int kHK = kBN / 2;  // keys per thread per tile
+    constexpr int kHD = D / 2;    // O columns per thread
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
     const Schedule sched = make_schedule<PAIR>(P);
-    const int row = threadIdx.x;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int half = lane >> 4;
+    const int lane0 = 32 * (warp & 3) + 16 * (warp >> 2);  // first tensor-memory lane of the warp
+    const int row = lane0 + (lane & 15);
+    const uint32_t lane_off = (uint32_t)lane0 << 16;
     const uint32_t o_addr = tbase + lane_off + kColO;
     const float c = P.scale_log2;
+    const bool o_v8 = (reinterpret_cast<uintptr_t>(P.o) & 31u) == 0;  // 32-byte stores possible
     RingPos sb;     // S buffer of the current tile and the parity of its use
     int units = 0;  // non-empty units before this one
     bool ok = true;
@@ -426,7 +437,7 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
         visible_range(P, p, vlo, vhi);
         const bool has_sink = P.sinks != nullptr;
         float m = has_sink ? __ldg(P.sinks + U.h) * kLog2e : -INFINITY;  // log2 units
-        float l = has_sink ? 1.f : 0.f;
+        float l = (has_sink && half == 0) ? 1.f : 0.f;                   // this thread's share of the sum
         const float *mrow =
             (P.mask != nullptr && i < P.Tq) ? P.mask + U.b * P.msb + U.h * P.msh + (int64_t)i * P.msq : nullptr;
         // Tiles j in [ti_lo, ti_hi) are interior: every key visible to every
@@ -447,23 +458,23 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
             // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], sb.ph, abort)))) break;
             tc_fence_after();
-            uint32_t sr[kBN];
-            tmem_load128(s_addr, sr);
+            uint32_t sr[kHK];
+            tmem_load_pair64<kHK>(s_addr, sr);
             float *s = reinterpret_cast<float *>(sr);
 
             float cs = c;  // multiplier from s[] to log2 units for this tile
             if (j < ti_lo || j >= ti_hi) {
-                const int j0 = (U.t_begin + j) * kBN;
-                // The row's visible keys in this tile: [elo, ehi) (clamped).
-                const int64_t elo64 = vlo - j0, ehi64 = vhi - j0;
-                const int elo = elo64 < -1 ? -1 : (elo64 > kBN ? kBN : (int)elo64);
-                const int ehi = ehi64 < -1 ? -1 : (ehi64 > kBN ? kBN : (int)ehi64);
+                const int k0 = (U.t_begin + j) * kBN + half * kHK;  // this thread's first key
+                // The row's visible keys among this thread's: [elo, ehi) (clamped).
+                const int64_t elo64 = vlo - k0, ehi64 = vhi - k0;
+                const int elo = elo64 < -1 ? -1 : (elo64 > kHK ? kHK : (int)elo64);
+                const int ehi = ehi64 < -1 ? -1 : (ehi64 > kHK ? kHK : (int)ehi64);
                 if (mrow != nullptr) {
                     // Additive mask: scores in log2 units; keys past Tk read a
                     // clamped (valid) address and are dropped by the interval.
 #pragma unroll
-                    for (int e = 0; e < kBN; ++e) {
-                        const int jj = min(j0 + e, P.Tk - 1);
+                    for (int e = 0; e < kHK; ++e) {
+                        const int jj = min(k0 + e, P.Tk - 1);
                         const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
                         s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
                     }
@@ -472,27 +483,28 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
                     // A non-positive scale: scale first so that -inf marks the
                     // keys the row cannot see.
 #pragma unroll
-                    for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
+                    for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
                     cs = 1.f;
                 } else {
                     // Boundary tile: keys outside the row's interval drop to -inf.
 #pragma unroll
-                    for (int e = 0; e < kBN; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
+                    for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
                 }
             }
-            float bm;  // tile max of s[] * cs, in log2 units
+            float bm;  // tile max of s[] * cs over the whole row, in log2 units
             {
-                static_assert(kBN == 128, "max chains assume 128 keys per tile");
+                static_assert(kHK == 64, "max chains assume 64 keys per thread");
                 float mx[8];  // eight independent chains of three-input max
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);  // keys 0..23
 #pragma unroll
-                for (int e = 24; e < 120; e += 16)  // keys 24..119
+                for (int e = 24; e < 56; e += 16)  // keys 24..55
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[120 + c8]);  // keys 120..127
+                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[56 + c8]);  // keys 56..63
                 bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));  // the row's other half
             }
 
             // Lazy max: move m only when the tile exceeds it by the threshold
@@ -510,9 +522,9 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_done[bp], php, abort)))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < kHD; cc += 32) {
                     uint32_t orr[32];
-                    tmem_load32(o_addr + cc * 32, orr);
+                    tmem_load_pair32<kHD>(o_addr + cc, orr);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const float2 v = fmul2(make_float2(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])),
@@ -520,16 +532,16 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
                         orr[e] = __float_as_uint(v.x);
                         orr[e + 1] = __float_as_uint(v.y);
                     }
-                    tmem_store32(o_addr + cc * 32, orr);
+                    tmem_store_pair32<kHD>(o_addr + cc, orr);
                 }
             }
 
             // p = 2^(s cs - shift), rounded to bf16 pairs; row sum in fp32.
             const float2 cs2 = make_float2(cs, cs), nsh2 = make_float2(-shift, -shift);
             float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-            uint32_t pk[kBN / 2];
+            uint32_t pk[kHK / 2];
 #pragma unroll
-            for (int e = 0; e < kBN; e += 4) {
+            for (int e = 0; e < kHK; e += 4) {
                 const float2 x0 = ffma2(make_float2(s[e], s[e + 1]), cs2, nsh2);
                 const float2 x1 = ffma2(make_float2(s[e + 2], s[e + 3]), cs2, nsh2);
                 const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
@@ -539,9 +551,11 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
                 pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
                 pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
             }
-            tmem_store64(s_addr, pk);
+            // P of keys [64 h, 64 h + 64) into columns [32 h, 32 h + 32) of the buffer.
+            tmem_store_pair32<kHK / 2>(s_addr, pk);
             tc_fence_before();
-            mbar_arrive(&bar.p_full[b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.p_full[b]);  // one arrival per warp
             const float2 a = fadd2(acc0, acc1);
             l = fmaf(alpha, l, a.x + a.y);
             sb.template advance<kSBufs>();
@@ -550,32 +564,47 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
 
         // Epilogue: o = O / l (0 for an empty row), lse = (m + log2 l) ln 2.
         // O leaves tensor memory first: the next unit's first P V overwrites
-        // it once this thread has released that unit's P_0.
-        uint32_t ov[D];
+        // it once every warp has released that unit's P_0.
+        const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
+        uint32_t ov[kHD];
         if (n > 0) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc)
-                tmem_load32(o_addr + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(ov + cc * 32));
+            for (int cc = 0; cc < kHD; cc += 32)
+                tmem_load_pair32<kHD>(o_addr + cc, *reinterpret_cast<uint32_t(*)[32]>(ov + cc));
             tc_fence_before();
         } else {
 #pragma unroll
-            for (int e = 0; e < D; ++e) ov[e] = 0u;
+            for (int e = 0; e < kHD; ++e) ov[e] = 0u;
         }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
         if (i < P.Tq) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)U.bh * P.Tq + i) * D);
+            // This thread's half of the row: D bytes of bf16.
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)U.bh * P.Tq + i) * D + half * kHD;
+            if (o_v8) {
 #pragma unroll
-            for (int e = 0; e < D / 8; ++e) {
-                uint32_t w[4];
+                for (int e = 0; e < kHD / 16; ++e) {
+                    uint32_t w[8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
-                                      __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
-                dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int k = 0; k < 8; ++k)
+                        w[k] = cvt_bf16x2(__uint_as_float(ov[16 * e + 2 * k]) * inv,
+                                          __uint_as_float(ov[16 * e + 2 * k + 1]) * inv);
+                    st_global_v8(dst + 16 * e, w);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kHD / 8; ++e) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
+                                          __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
+                    reinterpret_cast<uint4 *>(dst)[e] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
             }
-            if (P.lse != nullptr) P.lse[(int64_t)U.bh * P.Tq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            if (P.lse != nullptr && half == 0)
+                P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         }
         if (n > 0) ++units;
     }
@@ -602,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kSBufs; ++s) {
             mbar_init(&bar.s_full[s], 1);
-            mbar_init(&bar.p_full[s], kBM);
+            mbar_init(&bar.p_full[s], kSoftmaxWarps);  // one arrival per softmax warp
             mbar_init(&bar.o_done[s], 1);
         }
         mbar_init(&bar.o_final, 1);
@@ -639,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpPv) {
         if (lane == 0) pv_role<D, PAIR>(P, smem, bar, tbase);
     } else {
-        softmax_role<D, PAIR>(P, bar, tbase, warp);
+        softmax_role<D, PAIR>(P, bar, tbase, warp, lane);
     }
 
     tc_fence_before();
