@@ -159,6 +159,38 @@ def time_graph(fn, reps, flush, warm=3):
     return statistics.median(ms), ms
 
 
+def measure_long_context(fa, dev, flush, name, peak_burst, peak_sustained, local_rank):
+    import torch
+    w = workloads.CONFIGS[name]
+    lp = w.problem
+    one_set = 2 * lp.d * lp.B * (2 * lp.Tq * lp.Hq + 2 * lp.Tk * lp.Hkv)  # bytes of q, o, k, v (bf16)
+    n_seq = max(1, min(8, -(-2 * L2_FLUSH_BYTES // one_set)))  # footprint >= 2x the flush size
+    sets = []
+    for i in range(n_seq):
+        q, k, v = workloads.qkv(w.seeds[0] + 1000 * i, lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, torch.bfloat16)
+        sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty((lp.B, lp.Hq, lp.Tq, lp.d), dtype=torch.bfloat16,
+                     device=dev), torch.empty((lp.B, lp.Hq, lp.Tq), dtype=torch.float32, device=dev)))
+
+    def call(t):
+        q, k, v, o, lse = t
+        fa.fa_fwd(q, k, v, o, lse, lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, lp.sm_scale, 0, 1, 0, None, None, 0, 0,
+                  0, 0, fa.FA_DTYPE_BF16, None)
+
+    reps = 20 if lp.Tq <= 8192 else 8
+    sampler = ClockSampler(local_rank)
+    med, _ = time_graph(lambda: call(sets[0]), reps, flush)
+    seq_med, _ = time_graph(lambda: [call(t) for t in sets], max(3, reps // n_seq), flush)
+    sampler.stop()
+    per_call = seq_med / n_seq
+    tf = lp.flops() / (med / 1e3) / 1e12
+    tf_seq = lp.flops() / (per_call / 1e3) / 1e12
+    return {"workload": name, "T": lp.Tq, "ms": round(med, 4), "tflops": round(tf, 1),
+            "frac_of_measured_peak": round(tf / peak_burst, 4),
+            "ms_per_call_in_sequence": round(per_call, 4), "calls_in_sequence": n_seq,
+            "tflops_in_sequence": round(tf_seq, 1), "frac_in_sequence": round(tf_seq / peak_burst, 4),
+            "frac_in_sequence_of_sustained": round(tf_seq / peak_sustained, 4), "clocks": sampler.summary()}
+
+
 # FP32 SIMT peak of the GB300: 152 SMs x 128 FFMA lanes x 2 FLOP x 2.07 GHz.
 FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
@@ -402,29 +434,16 @@ def run_fa(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
 
-    # Long-context causal prefill at T = 2044, 8192, 32768 (bf16), one call
-    # per measurement, L2 flushed before each.
+    # Long-context causal prefill at T = 2044, 8192, 32768 (bf16).  "ms": one
+    # call per measurement, L2 flushed before each (graph launch latency
+    # included).  "ms_per_call_in_sequence": calls back to back on distinct
+    # inputs (as successive layers would run) whose total exceeds L2, L2
+    # flushed before each sequence; the time per call.
     peak_burst, peak_sustained, peak_kind = _peaks()
     long_ctx = []
     if not args.skip_long and rank == 0:
         for name in LONG_CONTEXT:
-            w = workloads.CONFIGS[name]
-            lp = w.problem
-            q, k, v = workloads.qkv(w.seeds[0], lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, torch.bfloat16)
-            q, k, v = q.to(dev), k.to(dev), v.to(dev)
-            o = torch.empty_like(q)
-            lse = torch.empty((lp.B, lp.Hq, lp.Tq), dtype=torch.float32, device=dev)
-            reps = 20 if lp.Tq <= 8192 else 8
-
-            def one_call():
-                fa.fa_fwd(q, k, v, o, lse, lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, lp.sm_scale, 0, 1, 0, None,
-                          None, 0, 0, 0, 0, fa.FA_DTYPE_BF16, None)
-
-            med, _ = time_graph(one_call, reps, flush)
-            tf = lp.flops() / (med / 1e3) / 1e12
-            long_ctx.append({"workload": name, "T": lp.Tq, "ms": round(med, 4), "tflops": round(tf, 1),
-                             "frac_of_measured_peak": round(tf / peak_burst, 4)})
-            del q, k, v, o, lse
+            long_ctx.append(measure_long_context(fa, dev, flush, name, peak_burst, peak_sustained, local_rank))
 
     # The other configurations of the hot path: the fp32 SIMT kernel and the
     # windowed-sink chunked prompt, each timed from a CUDA graph.
@@ -474,7 +493,7 @@ def run_fa(args, rank, world, local_rank):
         "gpu_launches": L * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_burst, 4), "traffic": traffic,
-                     "kernel": "fa_fwd_bf16_kernel<128>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
+                     "kernel": "fa_fwd_bf16_kernel<128, 2>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
         "clocks": sampler.summary(),
         "long_context": long_ctx,
         "other_paths": others,
@@ -511,10 +530,12 @@ def run_only(args, local_rank):
         print(json.dumps({"only": args.only, "dtype": args.dtype, "calls": args.calls}), flush=True)
         return
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local_rank)
     med, ms = time_graph(one_call, args.calls, flush)
+    sampler.stop()
     print(json.dumps({"only": args.only, "dtype": args.dtype, "ms_median": round(med, 4),
-                      "ms": [round(x, 4) for x in ms], "tflops": round(p.flops() / (med / 1e3) / 1e12, 1)}),
-          flush=True)
+                      "ms": [round(x, 4) for x in ms], "tflops": round(p.flops() / (med / 1e3) / 1e12, 1),
+                      "clocks": sampler.summary()}), flush=True)
 
 
 def main():
