@@ -98,11 +98,13 @@ struct SmemLayout {
     static constexpr int kBoxes = D / 64;  // 64-column TMA boxes per tile
     static constexpr uint32_t kQBytes = kBM * D * 2;
     static constexpr uint32_t kKVBytes = kBN * D * 2;     // one K or V tile (a ring stage)
-    static constexpr int kStages = D == 128 ? 3 : 6;      // per ring: 96 KB each
+    static constexpr int kStages = D == 128 ? 3 : 6;      // K ring: 96 KB
+    static constexpr int kVStages = kStages - 1;          // V ring: 64 or 80 KB
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKRing = kQ + kQBytes;
     static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
-    static constexpr uint32_t kBar = kVRing + kStages * kKVBytes;
+    static constexpr uint32_t kOStage = kVRing + kVStages * kKVBytes;  // O tile, bf16, for the TMA store
+    static constexpr uint32_t kBar = kOStage + kQBytes;
     static constexpr uint32_t kTotal = kBar + 512;
     static_assert(kStages <= kMaxStages, "ring too deep");
 };
@@ -116,6 +118,8 @@ struct Barriers {
     uint64_t p_full[kSBufs];                           // P written over S in buffer b
     uint64_t o_done[kSBufs];                           // O += P V from buffer b completed
     uint64_t o_final;                                  // the unit's last O += P V completed
+    uint64_t ep_free;                                  // the O staging tile may be written
+    uint64_t ep_full;                                  // the O staging tile is written
     uint64_t drain[2];                                 // issuers' last MMAs completed
     uint32_t tmem_base;
     int abort;
@@ -193,6 +197,15 @@ struct RingPos {
     }
 };
 
+// Bits [lo, hi) of a 32-bit word set (bounds clamped to [0, 32]).
+__device__ __forceinline__ uint32_t bit_range32(int lo, int hi) {
+    lo = min(max(lo, 0), 32);
+    hi = min(max(hi, 0), 32);
+    const uint32_t below_hi = hi >= 32 ? ~0u : ((1u << hi) - 1u);
+    const uint32_t below_lo = lo >= 32 ? ~0u : ((1u << lo) - 1u);
+    return hi > lo ? (below_hi & ~below_lo) : 0u;
+}
+
 // Shared-memory descriptors kept as 32-bit halves: the start-address field
 // sits in the low half, and every operand address used here stays below
 // 256 KB, so stepping through a tile is a 32-bit add of (offset >> 4).
@@ -258,7 +271,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         const int kv_head = U.b * P.Hkv + U.g;
         // Tile t of the unit into the next stage of a ring; the stage is
         // refilled once every CTA reading it released its previous use.
-        auto load_tile = [&](uint32_t ring, uint64_t *full, uint64_t *empty, int *issued, RingPos &pos,
+        auto load_tile = [&](uint32_t ring, int stages, uint64_t *full, uint64_t *empty, int *issued, RingPos &pos,
                              const CUtensorMap *map, int t) -> bool {
             const int st = pos.st;
             if (issued[st] > 0 && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
@@ -274,11 +287,18 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
                     tma_load_3d(dst, map, &full[st], c * 64, key0, kv_head);
             }
             ++issued[st];
-            pos.template advance<L::kStages>();
+            if (++pos.st == stages) {
+                pos.st = 0;
+                pos.ph ^= 1u;
+            }
             return true;
         };
-        auto load_k = [&](int t) { return load_tile(L::kKRing, bar.k_full, bar.k_empty, k_issued, kput, &tmK, t); };
-        auto load_v = [&](int t) { return load_tile(L::kVRing, bar.v_full, bar.v_empty, v_issued, vput, &tmV, t); };
+        auto load_k = [&](int t) {
+            return load_tile(L::kKRing, L::kStages, bar.k_full, bar.k_empty, k_issued, kput, &tmK, t);
+        };
+        auto load_v = [&](int t) {
+            return load_tile(L::kVRing, L::kVStages, bar.v_full, bar.v_empty, v_issued, vput, &tmV, t);
+        };
         if (!(ok = load_k(0))) break;
         if (n > 1 && !(ok = load_k(1))) break;
         // Q of this unit, once the previous unit's S MMAs are done with the buffer.
@@ -391,7 +411,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
             mma_commit(&bar.o_done[b]);
             if (j + 1 == n) mma_commit(&bar.o_final);
             release_stage<PAIR>(&bar.v_empty[take.st]);
-            take.template advance<L::kStages>();
+            take.template advance<L::kVStages>();
             sb.template advance<kSBufs>();
         }
     }
@@ -406,9 +426,12 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
 // of O's columns.  Row max and row sum combine through one shuffle, and the
 // two warps on a scheduler partition hide each other's latencies.
 template <int D, int PAIR>
-__device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uint32_t tbase, int warp, int lane) {
+__device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Params &P, uint8_t *smem, Barriers &bar,
+                                             uint32_t tbase, int warp, int lane) {
+    using L = SmemLayout<D>;
     constexpr int kHK = kBN / 2;  // keys per thread per tile
     constexpr int kHD = D / 2;    // O columns per thread
+    static_assert(kHD == 32 || kHD == 64, "a thread's O columns fill half or all of a 64-column box");
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
     const Schedule sched = make_schedule<PAIR>(P);
@@ -418,9 +441,9 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
     const uint32_t lane_off = (uint32_t)lane0 << 16;
     const uint32_t o_addr = tbase + lane_off + kColO;
     const float c = P.scale_log2;
-    const bool o_v8 = (reinterpret_cast<uintptr_t>(P.o) & 31u) == 0;  // 32-byte stores possible
     RingPos sb;     // S buffer of the current tile and the parity of its use
     int units = 0;  // non-empty units before this one
+    int eps = 0;    // epilogues before this one
     bool ok = true;
 
     for (int r = 0; ok; ++r) {
@@ -433,8 +456,13 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
         const int64_t p_first = (int64_t)P.q_offset + U.r0;
         const int64_t p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
         // Per-row visible key interval [vlo, vhi) before the additive mask.
-        int64_t vlo, vhi;
-        visible_range(P, p, vlo, vhi);
+        int vlo, vhi;  // within [0, Tk]
+        {
+            int64_t lo64, hi64;
+            visible_range(P, p, lo64, hi64);
+            vlo = (int)lo64;
+            vhi = (int)hi64;
+        }
         const bool has_sink = P.sinks != nullptr;
         float m = has_sink ? __ldg(P.sinks + U.h) * kLog2e : -INFINITY;  // log2 units
         float l = (has_sink && half == 0) ? 1.f : 0.f;                   // this thread's share of the sum
@@ -466,9 +494,8 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
             if (j < ti_lo || j >= ti_hi) {
                 const int k0 = (U.t_begin + j) * kBN + half * kHK;  // this thread's first key
                 // The row's visible keys among this thread's: [elo, ehi) (clamped).
-                const int64_t elo64 = vlo - k0, ehi64 = vhi - k0;
-                const int elo = elo64 < -1 ? -1 : (elo64 > kHK ? kHK : (int)elo64);
-                const int ehi = ehi64 < -1 ? -1 : (ehi64 > kHK ? kHK : (int)ehi64);
+                const int elo = min(max(vlo - k0, 0), kHK), ehi = min(max(vhi - k0, 0), kHK);
+                auto visible = [&](int e) { return e >= elo && e < ehi; };
                 if (mrow != nullptr) {
                     // Additive mask: scores in log2 units; keys past Tk read a
                     // clamped (valid) address and are dropped by the interval.
@@ -476,19 +503,19 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
                     for (int e = 0; e < kHK; ++e) {
                         const int jj = min(k0 + e, P.Tk - 1);
                         const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
-                        s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                        s[e] = visible(e) ? x : -INFINITY;
                     }
                     cs = 1.f;
                 } else if (c <= 0.f) {
                     // A non-positive scale: scale first so that -inf marks the
                     // keys the row cannot see.
 #pragma unroll
-                    for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
+                    for (int e = 0; e < kHK; ++e) s[e] = visible(e) ? s[e] * c : -INFINITY;
                     cs = 1.f;
                 } else {
                     // Boundary tile: keys outside the row's interval drop to -inf.
 #pragma unroll
-                    for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
+                    for (int e = 0; e < kHK; ++e) s[e] = visible(e) ? s[e] : -INFINITY;
                 }
             }
             float bm;  // tile max of s[] * cs over the whole row, in log2 units
@@ -563,57 +590,75 @@ __device__ __forceinline__ void softmax_role(const Params &P, Barriers &bar, uin
         if (!ok) break;
 
         // Epilogue: o = O / l (0 for an empty row), lse = (m + log2 l) ln 2.
-        // O leaves tensor memory first: the next unit's first P V overwrites
-        // it once every warp has released that unit's P_0.
+        // O goes out through shared memory and a TMA store: the staging tile
+        // is [D / 64 boxes][128 rows][128 bytes] with the 128-byte swizzle
+        // (16-byte chunk c of row r at chunk c ^ (r % 8)); rows past Tq are
+        // clipped by the store.  The previous unit's store must have read the
+        // tile before it is rewritten.  O leaves tensor memory before this
+        // thread's warp releases the next unit's P_0 (whose P V overwrites O).
         const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
-        uint32_t ov[kHD];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
         if (n > 0) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < kHD; cc += 32)
-                tmem_load_pair32<kHD>(o_addr + cc, *reinterpret_cast<uint32_t(*)[32]>(ov + cc));
-            tc_fence_before();
-        } else {
-#pragma unroll
-            for (int e = 0; e < kHD; ++e) ov[e] = 0u;
         }
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        if (i < P.Tq) {
-            // This thread's half of the row: D bytes of bf16.
-            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(P.o) + ((int64_t)U.bh * P.Tq + i) * D + half * kHD;
-            if (o_v8) {
+        if (threadIdx.x == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&bar.ep_free);
+        }
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_free, eps & 1, abort)))) break;
+        {
+            const int col0 = half * kHD;  // this thread's first O column
+            uint8_t *box = smem + L::kOStage + (col0 / 64) * (kBM * kSwRowBytes) + row * kSwRowBytes;
 #pragma unroll
-                for (int e = 0; e < kHD / 16; ++e) {
-                    uint32_t w[8];
+            for (int cc = 0; cc < kHD; cc += 32) {
+                uint32_t ov[32];
+                if (n > 0) {
+                    tmem_load_pair32<kHD>(o_addr + cc, ov);
+                } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        w[k] = cvt_bf16x2(__uint_as_float(ov[16 * e + 2 * k]) * inv,
-                                          __uint_as_float(ov[16 * e + 2 * k + 1]) * inv);
-                    st_global_v8(dst + 16 * e, w);
+                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
                 }
-            } else {
 #pragma unroll
-                for (int e = 0; e < kHD / 8; ++e) {
+                for (int e = 0; e < 4; ++e) {
                     uint32_t w[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
                                           __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
-                    reinterpret_cast<uint4 *>(dst)[e] = make_uint4(w[0], w[1], w[2], w[3]);
+                    const int chunk = ((col0 % 64 + cc) / 8 + e) ^ (row & 7);
+                    *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            if (P.lse != nullptr && half == 0)
-                P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+            if (n > 0) tc_fence_before();
         }
+        fence_proxy_async_smem();  // the TMA store reads what this thread wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.ep_full);
+        if (warp == 0) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_full, eps & 1, abort)))) break;
+            if (lane == 0) {
+#pragma unroll
+                for (int cb = 0; cb < L::kBoxes; ++cb)
+                    tma_store_3d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.bh);
+                bulk_commit_group();
+            }
+        }
+        ++eps;
+        if (i < P.Tq && P.lse != nullptr && half == 0)
+            P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         if (n > 0) ++units;
     }
+    // The stores have read the staging tile before shared memory goes away
+    // (their global writes are complete when the grid is).
+    if (threadIdx.x == 0) bulk_wait_read_all();
 }
 
 template <int D, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const Params P) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       const Params P) {
     using L = SmemLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -635,6 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar.o_done[s], 1);
         }
         mbar_init(&bar.o_final, 1);
+        mbar_init(&bar.ep_free, 1);
+        mbar_init(&bar.ep_full, kSoftmaxWarps);
         mbar_init(&bar.drain[0], 1);
         mbar_init(&bar.drain[1], 1);
         bar.abort = 0;
@@ -648,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     if (PAIR == 2)
@@ -668,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpPv) {
         if (lane == 0) pv_role<D, PAIR>(P, smem, bar, tbase);
     } else {
-        softmax_role<D, PAIR>(P, bar, tbase, warp, lane);
+        softmax_role<D, PAIR>(tmO, P, smem, bar, tbase, warp, lane);
     }
 
     tc_fence_before();
@@ -731,14 +779,14 @@ template <int D, int PAIR>
 cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     // With Tk == 0 no key tile is ever loaded; the K/V maps only need to be valid.
     const void *kb = P.Tk > 0 ? P.k : P.q;
     const void *vb = P.Tk > 0 ? P.v : P.q;
     const int krows = P.Tk > 0 ? P.Tk : 1;
     const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
     if (!make_map(enc, &tq, P.q, D, P.Tq, P.B * P.Hq, kBM) || !make_map(enc, &tk, kb, D, krows, kheads, kBN / PAIR) ||
-        !make_map(enc, &tv, vb, D, krows, kheads, kBN / PAIR))
+        !make_map(enc, &tv, vb, D, krows, kheads, kBN / PAIR) || !make_map(enc, &to, P.o, D, P.Tq, P.B * P.Hq, kBM))
         return cudaErrorInvalidValue;
     // The CTA takes all 512 tensor-memory columns; the shared-memory request
     // (the K/V ring fills it) keeps a second CTA off the SM.
@@ -771,7 +819,7 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR>, tq, tk, tv, P);
+    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR>, tq, tk, tv, to, P);
 }
 
 }  // namespace
