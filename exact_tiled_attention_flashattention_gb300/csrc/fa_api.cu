@@ -75,8 +75,8 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
     if (d == 0 || (d & 1)) return fail(FA_EUNSUPPORTED, "d=%lld: d must be even and positive", (long long)d);
     if (dtype == FA_DTYPE_F32 && d > 256)
         return fail(FA_EUNSUPPORTED, "fp32 path supports d <= 256 (got %lld)", (long long)d);
-    if (dtype == FA_DTYPE_BF16 && d != 64 && d != 128)
-        return fail(FA_EUNSUPPORTED, "bf16 path supports d in {64, 128} (got %lld)", (long long)d);
+    if (dtype == FA_DTYPE_BF16 && (d % 8 != 0 || d > 128))
+        return fail(FA_EUNSUPPORTED, "bf16 path supports d a multiple of 8 up to 128 (got %lld)", (long long)d);
     if (Tq >= kMaxLen || Tk >= kMaxLen || q_offset >= kMaxLen)
         return fail(FA_EUNSUPPORTED, "Tq, Tk and q_offset must be below 2^30");
     if (B * Hq >= (int64_t(1) << 24)) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^24");

@@ -785,8 +785,12 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     const void *vb = P.Tk > 0 ? P.v : P.q;
     const int krows = P.Tk > 0 ? P.Tk : 1;
     const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
-    if (!make_map(enc, &tq, P.q, D, P.Tq, P.B * P.Hq, kBM) || !make_map(enc, &tk, kb, D, krows, kheads, kBN / PAIR) ||
-        !make_map(enc, &tv, vb, D, krows, kheads, kBN / PAIR) || !make_map(enc, &to, P.o, D, P.Tq, P.B * P.Hq, kBM))
+    // The maps carry the true head dimension d <= D: columns [d, D) of Q, K
+    // and V load as zero (leaving S exact and O's extra columns zero), and the
+    // O store drops them.
+    if (!make_map(enc, &tq, P.q, P.d, P.Tq, P.B * P.Hq, kBM) ||
+        !make_map(enc, &tk, kb, P.d, krows, kheads, kBN / PAIR) ||
+        !make_map(enc, &tv, vb, P.d, krows, kheads, kBN / PAIR) || !make_map(enc, &to, P.o, P.d, P.Tq, P.B * P.Hq, kBM))
         return cudaErrorInvalidValue;
     // The CTA takes all 512 tensor-memory columns; the shared-memory request
     // (the K/V ring fills it) keeps a second CTA off the SM.
@@ -827,7 +831,8 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
     // Pairs of query heads share a KV head when the group size is even.
     const bool pair = (P.group % 2) == 0;
-    if (P.d == 64) return pair ? launch_d<64, 2>(P, stream) : launch_d<64, 1>(P, stream);
+    // d is a multiple of 8 up to 128: the 64- or 128-column kernel, padded.
+    if (P.d <= 64) return pair ? launch_d<64, 2>(P, stream) : launch_d<64, 1>(P, stream);
     return pair ? launch_d<128, 2>(P, stream) : launch_d<128, 1>(P, stream);
 }
 

@@ -48,7 +48,8 @@
  *   FA_ESHAPE        Hq % Hkv != 0, Hkv > Hq, or Hkv == 0 with Hq > 0
  *                    ("FlashAttention forward in C", section 4: TL_ESHAPE).
  *   FA_EUNSUPPORTED  d odd or 0 ("Fused attention and softmax": d must be
- *                    even), d > 256 for fp32, bf16 d not in {64, 128},
+ *                    even), d > 256 for fp32, bf16 d not a multiple of 8
+ *                    or above 128 (rows must be 16-byte multiples for TMA),
  *                    Tq or Tk >= 2^30, pointers not 16-byte aligned.
  *   FA_ECUDA         a CUDA error while configuring or launching.
  * B*Hq*Tq == 0 is a no-op returning FA_OK.  Tk == 0 writes o = 0 and

@@ -91,8 +91,8 @@ CASES = [
     ("odd d", dict(d=7), fa.FA_EUNSUPPORTED),
     ("zero d", dict(d=0), fa.FA_EUNSUPPORTED),
     ("fp32 d > 256", dict(d=258), fa.FA_EUNSUPPORTED),
-    ("bf16 d = 96", dict(d=96, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
-    ("bf16 d = 32", dict(d=32, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
+    ("bf16 d = 100 (not a multiple of 8)", dict(d=100, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
+    ("bf16 d = 136 (> 128)", dict(d=136, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
     ("Tk >= 2^30", dict(Tk=1 << 30), fa.FA_EUNSUPPORTED),
     ("Tq >= 2^30", dict(Tq=1 << 30, B=1, Hq=1, Hkv=1, d=2), fa.FA_EUNSUPPORTED),
 ]

@@ -92,6 +92,23 @@ def test_window_sinks_chunked(dt):
     assert err <= (1e-5 if dt == "f32" else 8e-3), err
 
 
+def test_mask_batch_bf16_d96():
+    # The additive-mask batch (d = 96) on the bf16 path: d = 96 runs on the
+    # 128-column kernel with the extra columns loaded as zero.
+    w = workloads.CONFIGS["mask_b4h8_t1024_d96"]
+    p = w.problem
+    q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
+    m = workloads.strided_mask(w.extra["mask_seed"], p.Tq, p.Tk)
+    strides = (0, 0, p.Tk, 1)
+    rows = np.arange(0, p.Tq, 5, dtype=np.int64)
+    o, lse = gpu_attention(q, k, v, scale=p.sm_scale, causal=False, mask=m, mask_strides=strides)
+    eo, el = oracle_attention(q, k, v, rows=rows, scale=p.sm_scale, causal=False, mask=m, mask_strides=strides)
+    compare(o[:, :, rows], lse[:, :, rows], eo, el, torch.bfloat16, "mask batch bf16 d96")
+    empty_rows = [0, 63, 64, 127, 500, 511, 512, 1023]
+    assert torch.all(torch.isneginf(lse[:, :, empty_rows]))
+    assert torch.all(o[:, :, empty_rows] == 0)
+
+
 def test_mask_batch_f32():
     w = workloads.CONFIGS["mask_b4h8_t1024_d96"]
     p = w.problem
@@ -118,7 +135,7 @@ def test_edges_f32(d):
         _run_and_compare(q, k, v, torch.float32, f"edge f32 T={T} d={d}", scale=1 / math.sqrt(d), causal=True)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 80, 96, 128])
 def test_edges_bf16(d):
     for T in EDGE_T:
         q, k, v = workloads.qkv(T + d, 1, 2, 1, T, T, d, torch.bfloat16)
