@@ -103,6 +103,7 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
     P.Tk = (int)Tk;
     P.d = (int)d;
     P.group = (int)(Hq / Hkv);
+    P.splits = 1;
     P.q_offset = (int)q_offset;
     P.causal = causal ? 1 : 0;
     // A window wider than every possible distance is no window.

@@ -105,6 +105,10 @@ struct SmemLayout {
     static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
     static constexpr uint32_t kOStage = kVRing + kVStages * kKVBytes;  // O tile, bf16, for the TMA store
     static constexpr uint32_t kBar = kOStage + kQBytes;
+    // Packed-row split merge: O partials (fp32, padded rows) over the K ring,
+    // (m, l) per row over the V ring.
+    static constexpr int kOPartStride = D + 4;
+    static_assert(kBM * kOPartStride * 4 <= kStages * kKVBytes, "O partials fit the K ring");
     static constexpr uint32_t kTotal = kBar + 512;
     static_assert(kStages <= kMaxStages, "ring too deep");
 };
@@ -125,9 +129,21 @@ struct Barriers {
     int abort;
 };
 
+// The two ways rows are mapped onto 128-row tiles.
+//   kPrefill  a unit is one 128-row query tile of one (batch, query head);
+//             persistent grid, heaviest units first.
+//   kDecode   all group * Tq query rows of a KV head (heads of a GQA group are
+//             contiguous in q and o) form one tile, so K and V are read once
+//             per KV head; the unit's key range is split over the CTAs of a
+//             cluster, which merge their partial (m, l, O) through
+//             distributed shared memory.
+constexpr int kPrefill = 0, kDecode = 1;
+
 struct Unit {
     int b, h, g, bh;
-    int r0;  // first query row
+    int kv_head;  // K/V tensor-map head coordinate: b * Hkv + g
+    int q_head;   // Q/O tensor-map head coordinate
+    int r0;       // Q/O tensor-map row of the tile's first row
     int t_begin, n_tiles;
 };
 
@@ -150,6 +166,8 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     }
     U.bh = U.b * P.Hq + U.h;
     U.g = U.h / P.group;
+    U.kv_head = U.b * P.Hkv + U.g;
+    U.q_head = U.bh;
     U.r0 = qt * kBM;
     int64_t lo_a, hi_a, lo_b, hi_b;
     visible_range(P, (int64_t)P.q_offset + U.r0, lo_a, hi_a);
@@ -165,6 +183,46 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     return U;
 }
 
+// Packed-row unit of this CTA: KV head blockIdx.x / splits of the batch, key
+// tiles [t_begin, t_begin + n_tiles) = this CTA's share (cluster rank
+// blockIdx.x % splits) of the tiles the rows at positions q_offset ..
+// q_offset + Tq - 1 can see.
+__device__ __forceinline__ Unit decode_unit(const Params &P) {
+    Unit U;
+    const int cid = (int)blockIdx.x / P.splits, rank = (int)blockIdx.x % P.splits;
+    U.b = cid / P.Hkv;
+    U.g = cid % P.Hkv;
+    U.h = U.g * P.group;
+    U.bh = U.b * P.Hq + U.h;
+    U.kv_head = cid;
+    U.q_head = cid;
+    U.r0 = 0;
+    int64_t lo_a, hi_a, lo_b, hi_b;
+    visible_range(P, (int64_t)P.q_offset, lo_a, hi_a);
+    visible_range(P, (int64_t)P.q_offset + P.Tq - 1, lo_b, hi_b);
+    const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
+    U.t_begin = 0;
+    U.n_tiles = 0;
+    if (khi > klo) {
+        const int tb = (int)(klo / kBN), te = (int)((khi + kBN - 1) / kBN);
+        const int chunk = (te - tb + P.splits - 1) / P.splits;
+        const int b0 = tb + rank * chunk, b1 = min(te, b0 + chunk);
+        if (b1 > b0) {
+            U.t_begin = b0;
+            U.n_tiles = b1 - b0;
+        }
+    }
+    return U;
+}
+
+template <int MODE, int PAIR>
+__device__ __forceinline__ Unit get_unit(const Params &P, int u, int rank) {
+    if constexpr (MODE == kDecode)
+        return decode_unit(P);
+    else
+        return make_unit<PAIR>(P, u, rank);
+}
+
 // Snake order over groups: round r gives group g unit r*G + g (r even) or
 // r*G + G-1-g (r odd); -1 past the end.
 struct Schedule {
@@ -175,8 +233,9 @@ struct Schedule {
     }
 };
 
-template <int PAIR>
+template <int MODE, int PAIR>
 __device__ __forceinline__ Schedule make_schedule(const Params &P) {
+    if constexpr (MODE == kDecode) return Schedule{1, 1, 0};  // one unit per CTA
     const int nqt = (P.Tq + kBM - 1) / kBM;
     const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
     return Schedule{nqt * per_qt, (int)(gridDim.x / PAIR), (int)(blockIdx.x / PAIR)};
@@ -196,15 +255,6 @@ struct RingPos {
         }
     }
 };
-
-// Bits [lo, hi) of a 32-bit word set (bounds clamped to [0, 32]).
-__device__ __forceinline__ uint32_t bit_range32(int lo, int hi) {
-    lo = min(max(lo, 0), 32);
-    hi = min(max(hi, 0), 32);
-    const uint32_t below_hi = hi >= 32 ? ~0u : ((1u << hi) - 1u);
-    const uint32_t below_lo = lo >= 32 ? ~0u : ((1u << lo) - 1u);
-    return hi > lo ? (below_hi & ~below_lo) : 0u;
-}
 
 // Shared-memory descriptors kept as 32-bit halves: the start-address field
 // sits in the low half, and every operand address used here stays below
@@ -251,13 +301,13 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc 
 // unit's last S has released the Q buffer, then V_j and K_{j+2} in turn, each
 // into its own ring.  With PAIR == 2 this CTA loads rows [64 r, 64 r + 64) of
 // every K/V box (r = cluster rank) into both CTAs of the cluster.
-template <int D, int PAIR>
+template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                               const Params &P, uint8_t *smem, Barriers &bar) {
     using L = SmemLayout<D>;
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
-    const Schedule sched = make_schedule<PAIR>(P);
+    const Schedule sched = make_schedule<MODE, PAIR>(P);
     int k_issued[kMaxStages] = {}, v_issued[kMaxStages] = {};
     int q_issued = 0;
     RingPos kput, vput;
@@ -265,10 +315,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const Unit U = make_unit<PAIR>(P, u, rank);
+        const Unit U = get_unit<MODE, PAIR>(P, u, rank);
         const int n = U.n_tiles;
         if (n == 0) continue;
-        const int kv_head = U.b * P.Hkv + U.g;
+        const int kv_head = U.kv_head;
         // Tile t of the unit into the next stage of a ring; the stage is
         // refilled once every CTA reading it released its previous use.
         auto load_tile = [&](uint32_t ring, int stages, uint64_t *full, uint64_t *empty, int *issued, RingPos &pos,
@@ -306,7 +356,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
 #pragma unroll
         for (int c = 0; c < L::kBoxes; ++c)
-            tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.bh);
+            tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.q_head);
         ++q_issued;
         for (int j = 0; j < n && ok; ++j) {
             ok = load_v(j);
@@ -344,11 +394,11 @@ __device__ __forceinline__ void release_stage(uint64_t *empty) {
         mma_commit(empty);
 }
 
-template <int D, int PAIR>
+template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using L = SmemLayout<D>;
     volatile int *abort = &bar.abort;
-    const Schedule sched = make_schedule<PAIR>(P);
+    const Schedule sched = make_schedule<MODE, PAIR>(P);
     const Desc qd = make_desc(smem_u32(smem + L::kQ), 16, 1024);
     const Desc k0 = make_desc(smem_u32(smem + L::kKRing), 16, 1024);
     constexpr uint32_t kTileUnits = L::kKVBytes >> 4;  // one stage, in descriptor units
@@ -360,7 +410,7 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const int n = make_unit<PAIR>(P, u, 0).n_tiles;  // the same for both CTAs of a pair
+        const int n = get_unit<MODE, PAIR>(P, u, 0).n_tiles;  // the same for both CTAs of a pair
         if (n == 0) continue;
         if (!(ok = mbar_wait(&bar.q_full, units & 1, abort))) break;
         for (int j = 0; j < n; ++j) {
@@ -387,11 +437,11 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
 
 // The first O += P_0 V_0 of a unit overwrites O; the softmax warps read the
 // previous unit's O before they release P_0, so O is free by then.
-template <int D, int PAIR>
+template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using L = SmemLayout<D>;
     volatile int *abort = &bar.abort;
-    const Schedule sched = make_schedule<PAIR>(P);
+    const Schedule sched = make_schedule<MODE, PAIR>(P);
     const Desc v0 = make_desc(smem_u32(smem + L::kVRing), kBN * kSwRowBytes, 1024);
     constexpr uint32_t kTileUnits = L::kKVBytes >> 4;
     RingPos take;
@@ -400,7 +450,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const int n = make_unit<PAIR>(P, u, 0).n_tiles;
+        const int n = get_unit<MODE, PAIR>(P, u, 0).n_tiles;
         if (n == 0) continue;
         for (int j = 0; j < n; ++j) {
             const int b = sb.st;
@@ -425,7 +475,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
 // l + 16 hold the same row, the first and second half of each tile's keys and
 // of O's columns.  Row max and row sum combine through one shuffle, and the
 // two warps on a scheduler partition hide each other's latencies.
-template <int D, int PAIR>
+template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Params &P, uint8_t *smem, Barriers &bar,
                                              uint32_t tbase, int warp, int lane) {
     using L = SmemLayout<D>;
@@ -434,7 +484,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
     static_assert(kHD == 32 || kHD == 64, "a thread's O columns fill half or all of a 64-column box");
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
-    const Schedule sched = make_schedule<PAIR>(P);
+    const Schedule sched = make_schedule<MODE, PAIR>(P);
     const int half = lane >> 4;
     const int lane0 = 32 * (warp & 3) + 16 * (warp >> 2);  // first tensor-memory lane of the warp
     const int row = lane0 + (lane & 15);
@@ -449,25 +499,40 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const Unit U = make_unit<PAIR>(P, u, rank);
+        const Unit U = get_unit<MODE, PAIR>(P, u, rank);
         const int n = U.n_tiles;
-        const int i = U.r0 + row;
+        // The row's query head h and its row i in that head.  Prefill: the
+        // unit's head, consecutive rows.  Packed rows: row = (h - g group) Tq + i,
+        // and rows from group * Tq on are padding that sees no key.
+        int h = U.h, i = U.r0 + row;
+        bool live;  // the row holds a query
+        int64_t p_first = (int64_t)P.q_offset + U.r0, p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
+        if constexpr (MODE == kDecode) {
+            live = row < P.group * P.Tq;
+            const int hl = live ? row / P.Tq : 0;
+            h = U.g * P.group + hl;
+            i = live ? row - hl * P.Tq : 0;
+            p_first = P.q_offset;
+            p_last = (int64_t)P.q_offset + P.Tq - 1;
+        } else {
+            live = i < P.Tq;
+        }
         const int64_t p = (int64_t)P.q_offset + i;
-        const int64_t p_first = (int64_t)P.q_offset + U.r0;
-        const int64_t p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
         // Per-row visible key interval [vlo, vhi) before the additive mask.
-        int vlo, vhi;  // within [0, Tk]
-        {
+        int vlo = 0, vhi = 0;  // within [0, Tk]
+        if (MODE != kDecode || live) {
             int64_t lo64, hi64;
             visible_range(P, p, lo64, hi64);
             vlo = (int)lo64;
             vhi = (int)hi64;
         }
         const bool has_sink = P.sinks != nullptr;
-        float m = has_sink ? __ldg(P.sinks + U.h) * kLog2e : -INFINITY;  // log2 units
-        float l = (has_sink && half == 0) ? 1.f : 0.f;                   // this thread's share of the sum
+        // The sink joins the sum once: in the first CTA of a split key range.
+        const bool sink_here = has_sink && half == 0 && (MODE != kDecode || (int)blockIdx.x % P.splits == 0);
+        float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;  // log2 units
+        float l = sink_here ? 1.f : 0.f;                                // this thread's share of the sum
         const float *mrow =
-            (P.mask != nullptr && i < P.Tq) ? P.mask + U.b * P.msb + U.h * P.msh + (int64_t)i * P.msq : nullptr;
+            (P.mask != nullptr && live) ? P.mask + U.b * P.msb + h * P.msh + (int64_t)i * P.msq : nullptr;
         // Tiles j in [ti_lo, ti_hi) are interior: every key visible to every
         // row of the unit, and no additive mask.
         int ti_lo = 0, ti_hi = 0;
@@ -602,14 +667,13 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
         }
-        if (threadIdx.x == 0) {
-            bulk_wait_read_all();
-            mbar_arrive(&bar.ep_free);
-        }
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_free, eps & 1, abort)))) break;
-        {
-            const int col0 = half * kHD;  // this thread's first O column
-            uint8_t *box = smem + L::kOStage + (col0 / 64) * (kBM * kSwRowBytes) + row * kSwRowBytes;
+        if constexpr (MODE == kDecode) {
+            // This CTA's partial result over its share of the keys:
+            // unnormalised O (fp32, rows of kOPartStride floats) and (m, l) per
+            // row, in the K/V ring space (no copy or MMA is in flight any
+            // more).  The CTAs of the cluster merge them after the roles end.
+            float *opart = reinterpret_cast<float *>(smem + L::kKRing);
+            float2 *stats = reinterpret_cast<float2 *>(smem + L::kVRing);
 #pragma unroll
             for (int cc = 0; cc < kHD; cc += 32) {
                 uint32_t ov[32];
@@ -619,34 +683,63 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = 0u;
                 }
+                if (live) {
+                    float4 *dst = reinterpret_cast<float4 *>(opart + row * L::kOPartStride + half * kHD + cc);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
-                                          __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
-                    const int chunk = ((col0 % 64 + cc) / 8 + e) ^ (row & 7);
-                    *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                             __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
                 }
             }
             if (n > 0) tc_fence_before();
-        }
-        fence_proxy_async_smem();  // the TMA store reads what this thread wrote
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.ep_full);
-        if (warp == 0) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_full, eps & 1, abort)))) break;
-            if (lane == 0) {
-#pragma unroll
-                for (int cb = 0; cb < L::kBoxes; ++cb)
-                    tma_store_3d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.bh);
-                bulk_commit_group();
+            if (live && half == 0) stats[row] = make_float2(m, lt);
+        } else {
+            if (threadIdx.x == 0) {
+                bulk_wait_read_all();
+                mbar_arrive(&bar.ep_free);
             }
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_free, eps & 1, abort)))) break;
+            {
+                const int col0 = half * kHD;  // this thread's first O column
+                uint8_t *box = smem + L::kOStage + (col0 / 64) * (kBM * kSwRowBytes) + row * kSwRowBytes;
+    #pragma unroll
+                for (int cc = 0; cc < kHD; cc += 32) {
+                    uint32_t ov[32];
+                    if (n > 0) {
+                        tmem_load_pair32<kHD>(o_addr + cc, ov);
+                    } else {
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                    }
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w[4];
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
+                                              __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
+                        const int chunk = ((col0 % 64 + cc) / 8 + e) ^ (row & 7);
+                        *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                if (n > 0) tc_fence_before();
+            }
+            fence_proxy_async_smem();  // the TMA store reads what this thread wrote
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.ep_full);
+            if (warp == 0) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_full, eps & 1, abort)))) break;
+                if (lane == 0) {
+    #pragma unroll
+                    for (int cb = 0; cb < L::kBoxes; ++cb)
+                        tma_store_3d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.bh);
+                    bulk_commit_group();
+                }
+            }
+            ++eps;
+            if (i < P.Tq && P.lse != nullptr && half == 0)
+                P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         }
-        ++eps;
-        if (i < P.Tq && P.lse != nullptr && half == 0)
-            P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         if (n > 0) ++units;
     }
     // The stores have read the staging tile before shared memory goes away
@@ -654,7 +747,40 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
     if (threadIdx.x == 0) bulk_wait_read_all();
 }
 
-template <int D, int PAIR>
+// Packed-row split merge (after every CTA of the cluster wrote its partial):
+// for each (row, column), with (m_s, l_s, O_s) the partials of the cluster's
+// S CTAs,  M = max m_s,  w_s = 2^(m_s - M),  o = sum w_s O_s / sum w_s l_s,
+// lse = (M + log2 sum w_s l_s) ln 2 -- the rescale of the online softmax
+// applied across key ranges.  With one CTA (w = 1) this is the plain epilogue,
+// bit for bit.  The (row, column) pairs are spread over all threads of the
+// cluster; o and lse go straight to global memory.
+template <int D>
+__device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
+    using L = SmemLayout<D>;
+    const int S = P.splits, rank = (int)blockIdx.x % S, cid = (int)blockIdx.x / S;
+    const int R = P.group * P.Tq;
+    const uint32_t op0 = smem_u32(smem + L::kKRing), st0 = smem_u32(smem + L::kVRing);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P.o) + (int64_t)cid * R * P.d;
+    float *lse_out = P.lse != nullptr ? P.lse + (int64_t)cid * R : nullptr;
+    for (int e = rank * kThreads + (int)threadIdx.x; e < R * P.d; e += S * kThreads) {
+        const int row = e / P.d, col = e - row * P.d;
+        float M = -INFINITY;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ld_cluster_f32(map_to_rank(st0 + row * 8, sp)));
+        float lsum = 0.f, acc = 0.f;
+        for (int sp = 0; sp < S; ++sp) {
+            const float2 ml = ld_cluster_f32x2(map_to_rank(st0 + row * 8, sp));
+            const float w = ml.x == M ? 1.f : ex2_approx(ml.x - M);  // 0 for an empty partial
+            const float ov = ld_cluster_f32(map_to_rank(op0 + (row * L::kOPartStride + col) * 4, sp));
+            lsum = sp == 0 ? w * ml.y : fmaf(w, ml.y, lsum);
+            acc = sp == 0 ? w * ov : fmaf(w, ov, acc);
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        out[(int64_t)row * P.d + col] = __float2bfloat16_rn(acc * inv);
+        if (col == 0 && lse_out != nullptr) lse_out[row] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+    }
+}
+
+template <int D, int PAIR, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -702,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // the peer's barriers exist before any multicast reaches them
     else
         __syncthreads();
+    static_assert(MODE == kPrefill || PAIR == 1, "packed rows run without K/V multicast");
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
     // Inputs may come from the previous kernel in the stream, and outputs may
@@ -710,19 +837,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_launch_dependents();
 
     if (warp == kWarpTma) {
-        if (lane == 0) producer_role<D, PAIR>(tmQ, tmK, tmV, P, smem, bar);
+        if (lane == 0) producer_role<D, PAIR, MODE>(tmQ, tmK, tmV, P, smem, bar);
     } else if (warp == kWarpQk) {
-        if (lane == 0) qk_role<D, PAIR>(P, smem, bar, tbase);
+        if (lane == 0) qk_role<D, PAIR, MODE>(P, smem, bar, tbase);
     } else if (warp == kWarpPv) {
-        if (lane == 0) pv_role<D, PAIR>(P, smem, bar, tbase);
+        if (lane == 0) pv_role<D, PAIR, MODE>(P, smem, bar, tbase);
     } else {
-        softmax_role<D, PAIR>(tmO, P, smem, bar, tbase, warp, lane);
+        softmax_role<D, PAIR, MODE>(tmO, P, smem, bar, tbase, warp, lane);
     }
 
     tc_fence_before();
     __syncthreads();
-    // No CTA of a pair leaves while the other may still multicast into it.
-    if (PAIR == 2) cluster_sync();
+    if constexpr (MODE == kDecode) {
+        cluster_sync();  // every CTA's partial is written
+        if (!bar.abort) merge_partials<D>(P, smem);
+        cluster_sync();  // no CTA leaves while a peer reads its partial
+    } else if (PAIR == 2) {
+        // No CTA of a pair leaves while the other may still multicast into it.
+        cluster_sync();
+    }
     if (bar.abort && threadIdx.x == 0) atomicOr(&g_watchdog, 1u);
     if (warp == kWarpQk) {
         __syncwarp();
@@ -798,7 +931,7 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "shared memory budget");
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, PAIR>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, PAIR, kPrefill>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -823,7 +956,77 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR>, tq, tk, tv, to, P);
+    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR, kPrefill>, tq, tk, tv, to, P);
+}
+
+// Key tiles seen by the rows at positions q_offset .. q_offset + Tq - 1.
+int packed_tiles(const Params &P) {
+    int64_t lo_a, hi_a, lo_b, hi_b;
+    visible_range(P, (int64_t)P.q_offset, lo_a, hi_a);
+    visible_range(P, (int64_t)P.q_offset + P.Tq - 1, lo_b, hi_b);
+    const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
+    if (khi <= klo) return 0;
+    return (int)((khi + kBN - 1) / kBN - klo / kBN);
+}
+
+// Packed rows (group * Tq <= 128): one cluster of `splits` CTAs per (batch,
+// KV head).  The split count depends only on the key range, never on B or on
+// the device, so a row's result does not depend on the batch it sits in; a
+// range of fewer than 4 tiles is not split (and then matches the prefill
+// kernel bit for bit).  At most 16 CTAs (the largest cluster), at least two
+// tiles each; a device that cannot hold a cluster of that size halves it.
+template <int D>
+cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    Params P = P0;
+    const int n = packed_tiles(P);
+    int S = n < 4 ? 1 : (n / 2 < 16 ? n / 2 : 16);
+    const int R = P.group * P.Tq;
+    CUtensorMap tq, tk, tv, to;
+    const void *kb = P.Tk > 0 ? P.k : P.q;
+    const void *vb = P.Tk > 0 ? P.v : P.q;
+    const int krows = P.Tk > 0 ? P.Tk : 1;
+    const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
+    // q and o viewed as [B * Hkv, group * Tq, d]: a KV group's heads are contiguous.
+    if (!make_map(enc, &tq, P.q, P.d, R, P.B * P.Hkv, kBM) || !make_map(enc, &tk, kb, P.d, krows, kheads, kBN) ||
+        !make_map(enc, &tv, vb, P.d, krows, kheads, kBN) || !make_map(enc, &to, P.o, P.d, R, P.B * P.Hkv, kBM))
+        return cudaErrorInvalidValue;
+    constexpr size_t kSmem = SmemLayout<D>::kTotal + 1024;
+    auto kernel = fa_fwd_bf16_kernel<D, 1, kDecode>;
+    static bool configured = false;
+    static int max_splits = 16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        // The largest cluster the device can hold with this footprint.
+        for (max_splits = 16; max_splits > 1; max_splits /= 2) {
+            int clusters = 0;
+            cfg.gridDim = dim3((unsigned)max_splits);
+            attr[1].val.clusterDim.x = (unsigned)max_splits;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0) break;
+            (void)cudaGetLastError();
+        }
+        configured = true;
+    }
+    while (S > max_splits) S = (S + 1) / 2;
+    P.splits = S;
+    cfg.gridDim = dim3((unsigned)(P.B * P.Hkv * S));
+    attr[1].val.clusterDim.x = (unsigned)S;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, P);
 }
 
 }  // namespace
@@ -832,6 +1035,8 @@ cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
     // Pairs of query heads share a KV head when the group size is even.
     const bool pair = (P.group % 2) == 0;
     // d is a multiple of 8 up to 128: the 64- or 128-column kernel, padded.
+    // All query rows of a KV group in one tile: the packed-row kernel.
+    if ((int64_t)P.group * P.Tq <= kBM) return P.d <= 64 ? launch_packed<64>(P, stream) : launch_packed<128>(P, stream);
     if (P.d <= 64) return pair ? launch_d<64, 2>(P, stream) : launch_d<64, 1>(P, stream);
     return pair ? launch_d<128, 2>(P, stream) : launch_d<128, 1>(P, stream);
 }

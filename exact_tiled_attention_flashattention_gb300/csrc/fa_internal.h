@@ -22,6 +22,7 @@ struct Params {
     int window;           // <= 0: none (clamped to int range by the host)
     float scale;          // scale applied to q.k
     float scale_log2;     // scale * log2(e)
+    int splits;           // bf16 packed-row path: CTAs that split a key range (set by its launcher)
 };
 
 // Visible key range [lo, hi) of query position p (absolute), before the mask.

@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Problem", "qkv", "sinks", "strided_mask", "CONFIGS", "chunk_ranges"]
+__all__ = ["Problem", "qkv", "sinks", "strided_mask", "CONFIGS", "DECODE", "chunk_ranges"]
 
 
 @dataclass(frozen=True)
@@ -130,4 +130,25 @@ CONFIGS = {
     "mask_b4h8_t1024_d96": Workload(
         "mask_b4h8_t1024_d96", Problem(4, 8, 8, 1024, 1024, 96, causal=False),
         ("f32",), seeds=(5,), extra={"mask_seed": 11}),
+}
+
+
+# Decode steps (one new token per sequence: Tq = 1 at q_offset = Tk - 1, causal),
+# "FlashAttention forward in C" section 2.1: the same flags serve a decode
+# step.  Geometries: the 16q/8kv d=128 model of the prefill configurations at
+# its three context lengths, a batch of 8 such sequences, and the 9q/3kv d=64
+# model of the CPU flash-attention page after a 128-token prefill and 200
+# decode steps.  These are not among the benchmark's headline configurations;
+# they measure the split-KV decode path.
+DECODE = {
+    "decode_gqa16x8_d128_k2044": Workload(
+        "decode_gqa16x8_d128_k2044", Problem(1, 16, 8, 1, 2044, 128, q_offset=2043), ("bf16",), seeds=(200,)),
+    "decode_gqa16x8_d128_k8192": Workload(
+        "decode_gqa16x8_d128_k8192", Problem(1, 16, 8, 1, 8192, 128, q_offset=8191), ("bf16",), seeds=(201,)),
+    "decode_gqa16x8_d128_k32768": Workload(
+        "decode_gqa16x8_d128_k32768", Problem(1, 16, 8, 1, 32768, 128, q_offset=32767), ("bf16",), seeds=(202,)),
+    "decode_b8_gqa16x8_d128_k8192": Workload(
+        "decode_b8_gqa16x8_d128_k8192", Problem(8, 16, 8, 1, 8192, 128, q_offset=8191), ("bf16",), seeds=(203,)),
+    "decode_gqa9x3_d64_k328": Workload(
+        "decode_gqa9x3_d64_k328", Problem(1, 9, 3, 1, 328, 64, q_offset=327), ("bf16",), seeds=(204,)),
 }
