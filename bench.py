@@ -191,6 +191,51 @@ def measure_long_context(fa, dev, flush, name, peak_burst, peak_sustained, local
             "frac_in_sequence_of_sustained": round(tf_seq / peak_sustained, 4), "clocks": sampler.summary()}
 
 
+def _hbm_peak():
+    try:
+        with open(os.path.join(_ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def measure_decode(fa, dev, flush, local_rank):
+    """Decode steps (Tq = 1 at q_offset = Tk - 1) on the packed-row split-KV
+    path: per call in a sequence of calls on distinct inputs, each read cold
+    (L2 flushed before the sequence, no input read twice), against the HBM
+    roofline: algorithmic bytes = Q + K + V + O (bf16) + lse (fp32)."""
+    import torch
+    peak_gbs, peak_kind = _hbm_peak()
+    out = []
+    for name, w in workloads.DECODE.items():
+        p = w.problem
+        kv_bytes = 2 * p.B * p.Hkv * p.Tk * p.d * 2
+        alg = kv_bytes + 2 * p.B * p.Hq * p.Tq * p.d * 2 + 4 * p.B * p.Hq * p.Tq
+        n_seq = max(2, min(16, -(-2 * L2_FLUSH_BYTES // kv_bytes)))
+        sets = []
+        for i in range(n_seq):
+            q, k, v = workloads.qkv(w.seeds[0] + 1000 * i, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
+            sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty((p.B, p.Hq, p.Tq, p.d), dtype=torch.bfloat16,
+                         device=dev), torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)))
+
+        def seq():
+            for q, k, v, o, lse in sets:
+                fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, 1, 0, None,
+                          None, 0, 0, 0, 0, fa.FA_DTYPE_BF16, None)
+
+        sampler = ClockSampler(local_rank)
+        med, _ = time_graph(seq, 10, flush)
+        sampler.stop()
+        per_call = med / n_seq
+        gbs = alg / (per_call / 1e3) / 1e9
+        out.append({"workload": name, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Tk": p.Tk, "d": p.d,
+                    "us_per_call": round(per_call * 1e3, 2), "calls_in_sequence": n_seq,
+                    "algorithmic_bytes": alg, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
+                    "hbm_peak_kind": peak_kind, "clocks": sampler.summary()})
+        del sets
+    return out
+
+
 # FP32 SIMT peak of the GB300: 152 SMs x 128 FFMA lanes x 2 FLOP x 2.07 GHz.
 FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
@@ -448,8 +493,10 @@ def run_fa(args, rank, world, local_rank):
     # The other configurations of the hot path: the fp32 SIMT kernel and the
     # windowed-sink chunked prompt, each timed from a CUDA graph.
     others = []
+    decode = []
     if not args.skip_long and rank == 0:
         others = measure_other_paths(fa, dev, flush)
+        decode = measure_decode(fa, dev, flush, local_rank)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -497,6 +544,7 @@ def run_fa(args, rank, world, local_rank):
         "clocks": sampler.summary(),
         "long_context": long_ctx,
         "other_paths": others,
+        "decode": decode,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -511,7 +559,7 @@ def run_only(args, local_rank):
     import exact_tiled_attention_flashattention_gb300 as fa
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = workloads.CONFIGS[args.only]
+    w = {**workloads.CONFIGS, **workloads.DECODE}[args.only]
     p = w.problem
     dt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
     q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, dt)
@@ -519,8 +567,8 @@ def run_only(args, local_rank):
     o = torch.empty_like(q)
     lse = torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)
     def one_call():
-        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, int(p.causal), p.window, None,
-                  None, 0, 0, 0, 0, fa.FA_DTYPE_BF16 if args.dtype == "bf16" else fa.FA_DTYPE_F32, None)
+        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, int(p.causal), p.window,
+                  None, None, 0, 0, 0, 0, fa.FA_DTYPE_BF16 if args.dtype == "bf16" else fa.FA_DTYPE_F32, None)
 
     if args.calls <= 3:
         # few launches (profiling): plain calls, no graph
@@ -548,7 +596,8 @@ def main():
     ap.add_argument("--skip-long", action="store_true", help="skip the long-context measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=sorted(workloads.CONFIGS), help="profiling driver: one workload only")
+    ap.add_argument("--only", choices=sorted({**workloads.CONFIGS, **workloads.DECODE}),
+                    help="profiling driver: one workload only")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16")
     args = ap.parse_args()

@@ -93,24 +93,36 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay below 2^8
 constexpr uint32_t kSwRowBytes = 128;      // one swizzled row: 64 bf16
 constexpr int kMaxStages = 6;
 
-template <int D>
+// The two ways rows are mapped onto 128-row tiles.
+//   kPrefill  a unit is one 128-row query tile of one (batch, query head);
+//             persistent grid, heaviest units first.
+//   kDecode   all group * Tq query rows of a KV head (heads of a GQA group are
+//             contiguous in q and o) form one tile, so K and V are read once
+//             per KV head; the unit's key range is split over the CTAs of a
+//             cluster, which merge their partial (m, l, O) through
+//             distributed shared memory.
+constexpr int kPrefill = 0, kDecode = 1;
+
+template <int D, int MODE>
 struct SmemLayout {
     static constexpr int kBoxes = D / 64;  // 64-column TMA boxes per tile
     static constexpr uint32_t kQBytes = kBM * D * 2;
     static constexpr uint32_t kKVBytes = kBN * D * 2;     // one K or V tile (a ring stage)
     static constexpr int kStages = D == 128 ? 3 : 6;      // K ring: 96 KB
-    static constexpr int kVStages = kStages - 1;          // V ring: 64 or 80 KB
+    // V ring: one stage fewer in prefill, where the O tile is staged for its
+    // TMA store; packed rows write O from registers and take the full ring.
+    static constexpr int kVStages = MODE == kDecode ? kStages : kStages - 1;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKRing = kQ + kQBytes;
     static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
     static constexpr uint32_t kOStage = kVRing + kVStages * kKVBytes;  // O tile, bf16, for the TMA store
-    static constexpr uint32_t kBar = kOStage + kQBytes;
+    static constexpr uint32_t kBar = kOStage + (MODE == kDecode ? 0u : kQBytes);
     // Packed-row split merge: O partials (fp32, padded rows) over the K ring,
     // (m, l) per row over the V ring.
     static constexpr int kOPartStride = D + 4;
     static_assert(kBM * kOPartStride * 4 <= kStages * kKVBytes, "O partials fit the K ring");
     static constexpr uint32_t kTotal = kBar + 512;
-    static_assert(kStages <= kMaxStages, "ring too deep");
+    static_assert(kStages <= kMaxStages && kVStages <= kMaxStages, "ring too deep");
 };
 
 struct Barriers {
@@ -129,15 +141,6 @@ struct Barriers {
     int abort;
 };
 
-// The two ways rows are mapped onto 128-row tiles.
-//   kPrefill  a unit is one 128-row query tile of one (batch, query head);
-//             persistent grid, heaviest units first.
-//   kDecode   all group * Tq query rows of a KV head (heads of a GQA group are
-//             contiguous in q and o) form one tile, so K and V are read once
-//             per KV head; the unit's key range is split over the CTAs of a
-//             cluster, which merge their partial (m, l, O) through
-//             distributed shared memory.
-constexpr int kPrefill = 0, kDecode = 1;
 
 struct Unit {
     int b, h, g, bh;
@@ -304,7 +307,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc 
 template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                               const Params &P, uint8_t *smem, Barriers &bar) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
     const Schedule sched = make_schedule<MODE, PAIR>(P);
@@ -396,7 +399,7 @@ __device__ __forceinline__ void release_stage(uint64_t *empty) {
 
 template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
     const Schedule sched = make_schedule<MODE, PAIR>(P);
     const Desc qd = make_desc(smem_u32(smem + L::kQ), 16, 1024);
@@ -439,7 +442,7 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
 // previous unit's O before they release P_0, so O is free by then.
 template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
     const Schedule sched = make_schedule<MODE, PAIR>(P);
     const Desc v0 = make_desc(smem_u32(smem + L::kVRing), kBN * kSwRowBytes, 1024);
@@ -478,7 +481,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
 template <int D, int PAIR, int MODE>
 __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Params &P, uint8_t *smem, Barriers &bar,
                                              uint32_t tbase, int warp, int lane) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, MODE>;
     constexpr int kHK = kBN / 2;  // keys per thread per tile
     constexpr int kHD = D / 2;    // O columns per thread
     static_assert(kHD == 32 || kHD == 64, "a thread's O columns fill half or all of a 64-column box");
@@ -756,7 +759,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
 // cluster; o and lse go straight to global memory.
 template <int D>
 __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, kDecode>;
     const int S = P.splits, rank = (int)blockIdx.x % S, cid = (int)blockIdx.x / S;
     const int R = P.group * P.Tq;
     const uint32_t op0 = smem_u32(smem + L::kKRing), st0 = smem_u32(smem + L::kVRing);
@@ -785,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        const Params P) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, MODE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Barriers &bar = *reinterpret_cast<Barriers *>(smem + L::kBar);
@@ -927,7 +930,7 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     // The CTA takes all 512 tensor-memory columns; the shared-memory request
     // (the K/V ring fills it) keeps a second CTA off the SM.
-    constexpr size_t kSmem = SmemLayout<D>::kTotal + 1024;
+    constexpr size_t kSmem = SmemLayout<D, kPrefill>::kTotal + 1024;
     static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "shared memory budget");
     static bool configured = false;
     if (!configured) {
@@ -970,18 +973,18 @@ int packed_tiles(const Params &P) {
 }
 
 // Packed rows (group * Tq <= 128): one cluster of `splits` CTAs per (batch,
-// KV head).  The split count depends only on the key range, never on B or on
-// the device, so a row's result does not depend on the batch it sits in; a
-// range of fewer than 4 tiles is not split (and then matches the prefill
-// kernel bit for bit).  At most 16 CTAs (the largest cluster), at least two
-// tiles each; a device that cannot hold a cluster of that size halves it.
+// KV head).  The split count is the largest that keeps every cluster of the
+// call resident at once (a second wave would double the time) with at least
+// two key tiles per CTA; a range of fewer than 4 tiles is not split (and then
+// matches the prefill kernel bit for bit).  It depends on B * Hkv and on the
+// device's cluster capacity, so split rows are not batch-invariant: the
+// split trades invariance for parallelism.
 template <int D>
 cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     Params P = P0;
     const int n = packed_tiles(P);
-    int S = n < 4 ? 1 : (n / 2 < 16 ? n / 2 : 16);
     const int R = P.group * P.Tq;
     CUtensorMap tq, tk, tv, to;
     const void *kb = P.Tk > 0 ? P.k : P.q;
@@ -992,10 +995,12 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     if (!make_map(enc, &tq, P.q, P.d, R, P.B * P.Hkv, kBM) || !make_map(enc, &tk, kb, P.d, krows, kheads, kBN) ||
         !make_map(enc, &tv, vb, P.d, krows, kheads, kBN) || !make_map(enc, &to, P.o, P.d, R, P.B * P.Hkv, kBM))
         return cudaErrorInvalidValue;
-    constexpr size_t kSmem = SmemLayout<D>::kTotal + 1024;
+    constexpr size_t kSmem = SmemLayout<D, kDecode>::kTotal + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
     auto kernel = fa_fwd_bf16_kernel<D, 1, kDecode>;
+    constexpr int kMaxSplits = 16;
     static bool configured = false;
-    static int max_splits = 16;
+    static int capacity[kMaxSplits + 1] = {};  // clusters of s CTAs resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
@@ -1012,19 +1017,29 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        // The largest cluster the device can hold with this footprint.
-        for (max_splits = 16; max_splits > 1; max_splits /= 2) {
+        for (int sp = 1; sp <= kMaxSplits; ++sp) {
             int clusters = 0;
-            cfg.gridDim = dim3((unsigned)max_splits);
-            attr[1].val.clusterDim.x = (unsigned)max_splits;
-            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0) break;
-            (void)cudaGetLastError();
+            cfg.gridDim = dim3((unsigned)sp);
+            attr[1].val.clusterDim.x = (unsigned)sp;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+                (void)cudaGetLastError();
+                clusters = 0;
+            }
+            capacity[sp] = clusters;
         }
+        if (capacity[1] <= 0) return cudaErrorInvalidConfiguration;
         configured = true;
     }
-    while (S > max_splits) S = (S + 1) / 2;
+    const int units = P.B * P.Hkv;
+    int S = 1;
+    if (n >= 4)
+        for (int sp = n / 2 < kMaxSplits ? n / 2 : kMaxSplits; sp > 1; --sp)
+            if (capacity[sp] >= units) {
+                S = sp;
+                break;
+            }
     P.splits = S;
-    cfg.gridDim = dim3((unsigned)(P.B * P.Hkv * S));
+    cfg.gridDim = dim3((unsigned)(units * S));
     attr[1].val.clusterDim.x = (unsigned)S;
     return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, P);
 }
