@@ -50,6 +50,9 @@ def load():
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_float, i64, ctypes.c_int,
                            i64, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.fa_fwd_strided.restype = ctypes.c_int
+    lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64] + [i64] * 12 + [
+        ctypes.c_float, i64, ctypes.c_int, i64, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
     lib.fa_last_error.restype = ctypes.c_char_p
     lib.fa_last_error.argtypes = []
     lib.fa_version.restype = ctypes.c_int
@@ -95,11 +98,28 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, scale, q_offset, causal, wind
     return st
 
 
+def fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q_strides, k_strides, v_strides, o_strides, scale,
+                   q_offset, causal, window, sinks, mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream=None, *,
+                   check=True) -> int:
+    """Call the strided C entry point (each *_strides = (batch, head, row) in
+    elements, d contiguous); raises FaError on a non-OK status when ``check``."""
+    lib = load()
+    st = lib.fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(Tq),
+                            int(Tk), int(d), *[int(x) for x in (*q_strides, *k_strides, *v_strides, *o_strides)],
+                            float(scale), int(q_offset), int(bool(causal)), int(window), _ptr(sinks), _ptr(mask),
+                            int(mask_sb), int(mask_sh), int(mask_sq), int(mask_sk), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
 def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=None, mask=None,
               mask_strides=(0, 0, 0, 0), with_lse=True, out=None, lse_out=None, stream=None):
     """o [B,Hq,Tq,d] (q's dtype) and lse [B,Hq,Tq] (fp32) for CUDA tensors
-    q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (fp32 or bf16, contiguous).  ``mask`` is
-    an fp32 CUDA tensor addressed with ``mask_strides`` (elements)."""
+    q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (fp32 or bf16).  The tensors may be
+    strided views (a [B,T,H,d] buffer seen through .transpose(1, 2), say) as
+    long as d is contiguous; ``out`` may be strided the same way.  ``mask``
+    is an fp32 CUDA tensor addressed with ``mask_strides`` (elements)."""
     import torch
     B, Hq, Tq, d = q.shape
     Hkv, Tk = k.shape[1], k.shape[2]
@@ -109,14 +129,17 @@ def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=N
         dt = FA_DTYPE_BF16
     else:
         raise TypeError(f"unsupported dtype {q.dtype}")
-    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
-        raise ValueError("q, k and v must be contiguous")
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("out", out),) if out is not None else ()):
+        if t.dim() != 4 or (t.shape[3] > 1 and t.stride(3) != 1):
+            raise ValueError(f"{name} must be 4-D with its last dimension contiguous")
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k and v must share a dtype")
-    o = out if out is not None else torch.empty_like(q)
+    o = out if out is not None else torch.empty((B, Hq, Tq, d), dtype=q.dtype, device=q.device)
+    if lse_out is not None and not lse_out.is_contiguous():
+        raise ValueError("lse_out must be contiguous [B, Hq, Tq]")
     lse = lse_out if lse_out is not None else (
         torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if with_lse else None)
     sc = (1.0 / d ** 0.5) if scale is None else scale
-    fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, sc, q_offset, causal, window, sinks, mask, *mask_strides, dt,
-           stream)
+    fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q.stride()[:3], k.stride()[:3], v.stride()[:3],
+                   o.stride()[:3], sc, q_offset, causal, window, sinks, mask, *mask_strides, dt, stream)
     return o, lse

@@ -5,6 +5,7 @@
 // (section 4): every error is returned before any launch and before anything
 // is written.  There is no CPU fallback: a configuration the GPU kernels do
 // not cover is rejected with FA_EUNSUPPORTED.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -44,11 +45,45 @@ extern "C" const char *fa_last_error(void) { return g_last_error; }
 
 extern "C" int fa_version(void) { return 100; }
 
-extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
-                            int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, float scale,
-                            int64_t q_offset, int causal, int64_t window, const float *sinks, const float *mask,
-                            int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk, int dtype,
-                            void *stream) {
+namespace {
+
+// Row spans of a [B, H, T, d] view with strides (sb, sh, st), d contiguous:
+// false if a dimension of extent > 1 has a negative stride, or if two rows
+// share memory under the sufficient rule "each stride (in increasing order)
+// covers the span of the dimensions inside it".  `bytes_last` is the offset
+// of the last element + 1 (in elements).
+bool layout_ok(int64_t B, int64_t H, int64_t T, int64_t d, int64_t sb, int64_t sh, int64_t st, bool distinct,
+               int64_t &span) {
+    span = 0;
+    if (B == 0 || H == 0 || T == 0) return true;  // an empty tensor has no rows
+    struct Dim { int64_t n, s; } dims[3] = {{B, sb}, {H, sh}, {T, st}};
+    for (auto &x : dims)
+        if (x.n > 1 && x.s < 0) return false;
+    // sort by stride
+    for (int i = 0; i < 3; ++i)
+        for (int j = i + 1; j < 3; ++j)
+            if (dims[j].s < dims[i].s) std::swap(dims[i], dims[j]);
+    span = d;
+    for (auto &x : dims) {
+        if (x.n <= 1) continue;
+        if (distinct && x.s < span) return false;
+        int64_t ext = 0;
+        if (!mul_ok(x.s, x.n - 1, ext) || ext > std::numeric_limits<int64_t>::max() - span) return false;
+        span = distinct ? ext + span : std::max(span, ext + d);
+    }
+    return true;
+}
+
+// Every stride of a dimension with extent > 1 is a multiple of `m` elements.
+bool strides_multiple(int64_t B, int64_t H, int64_t T, int64_t sb, int64_t sh, int64_t st, int64_t m) {
+    return (B <= 1 || sb % m == 0) && (H <= 1 || sh % m == 0) && (T <= 1 || st % m == 0);
+}
+
+fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t Hq,
+                   int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, const int64_t *qs, const int64_t *ks,
+                   const int64_t *vs, const int64_t *os, float scale, int64_t q_offset, int causal, int64_t window,
+                   const float *sinks, const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq,
+                   int64_t mask_sk, int dtype, void *stream) {
     g_last_error[0] = '\0';
     if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return fail(FA_EINVAL, "unknown dtype %d", dtype);
     if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || Tk < 0 || d < 0)
@@ -67,6 +102,13 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
         !mul_ok(B, Hkv, kv_rows) || !mul_ok(kv_rows, Tk, kv_rows) || !mul_ok(kv_rows, d, kv_elems) ||
         q_elems > (std::numeric_limits<int64_t>::max() >> 3) || kv_elems > (std::numeric_limits<int64_t>::max() >> 3))
         return fail(FA_EINVAL, "element counts overflow");
+    int64_t span = 0;
+    if (!layout_ok(B, Hq, Tq, d, qs[0], qs[1], qs[2], false, span) ||
+        !layout_ok(B, Hkv, Tk, d, ks[0], ks[1], ks[2], false, span) ||
+        !layout_ok(B, Hkv, Tk, d, vs[0], vs[1], vs[2], false, span))
+        return fail(FA_EINVAL, "q, k or v strides are negative or their extents overflow");
+    if (!layout_ok(B, Hq, Tq, d, os[0], os[1], os[2], true, span))
+        return fail(FA_EINVAL, "o strides are negative or make two output rows overlap");
     if (rows == 0) return FA_OK;  // nothing to compute, nothing to write
 
     if (!q || !o) return fail(FA_EINVAL, "q or o is NULL");
@@ -82,6 +124,26 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
     if (B * Hq >= (int64_t(1) << 24)) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^24");
     if (!aligned16(q) || !aligned16(o) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
         return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
+    // bf16: tensor-map strides are 16-byte multiples below 2^40 bytes.
+    // fp32: rows start on 8-byte boundaries (16-byte copies when all do).
+    const int64_t m = dtype == FA_DTYPE_BF16 ? 8 : 2;
+    const bool kv = Tk > 0;
+    if (!strides_multiple(B, Hq, Tq, qs[0], qs[1], qs[2], m) || !strides_multiple(B, Hq, Tq, os[0], os[1], os[2], m) ||
+        (kv && (!strides_multiple(B, Hkv, Tk, ks[0], ks[1], ks[2], m) ||
+                !strides_multiple(B, Hkv, Tk, vs[0], vs[1], vs[2], m))))
+        return fail(FA_EUNSUPPORTED, "strides must be multiples of %lld elements for this dtype", (long long)m);
+    if (dtype == FA_DTYPE_BF16) {
+        const int64_t lim = (int64_t(1) << 39) - 1;  // elements: 2^40 bytes
+        const int64_t ext[4][3] = {{B, Hq, Tq}, {B, Hkv, Tk}, {B, Hkv, Tk}, {B, Hq, Tq}};
+        const int64_t *all[4] = {qs, ks, vs, os};
+        for (int t = 0; t < 4; ++t)
+            for (int i = 0; i < 3; ++i) {
+                if (all[t][i] > lim) return fail(FA_EUNSUPPORTED, "a stride reaches 2^40 bytes");
+                if (ext[t][i] > 1 && all[t][i] <= 0 && (t == 0 || t == 3 || kv))
+                    return fail(FA_EUNSUPPORTED, "bf16 strides must be positive (tensor maps)");
+            }
+        if (B > 0x7fffffff || Hq > 0x7fffffff) return fail(FA_EUNSUPPORTED, "B and H must fit 31 bits");
+    }
 
     fa::Params P;
     std::memset(&P, 0, sizeof P);
@@ -104,6 +166,13 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
     P.d = (int)d;
     P.group = (int)(Hq / Hkv);
     P.splits = 1;
+    P.q_sb = qs[0], P.q_sh = qs[1], P.q_st = qs[2];
+    P.k_sb = ks[0], P.k_sh = ks[1], P.k_st = ks[2];
+    P.v_sb = vs[0], P.v_sh = vs[1], P.v_st = vs[2];
+    P.o_sb = os[0], P.o_sh = os[1], P.o_st = os[2];
+    P.vec16 = (d % 4 == 0) && strides_multiple(B, Hq, Tq, qs[0], qs[1], qs[2], 4) &&
+              (!kv || (strides_multiple(B, Hkv, Tk, ks[0], ks[1], ks[2], 4) &&
+                       strides_multiple(B, Hkv, Tk, vs[0], vs[1], vs[2], 4)));
     P.q_offset = (int)q_offset;
     P.causal = causal ? 1 : 0;
     // A window wider than every possible distance is no window.
@@ -115,4 +184,35 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
     cudaError_t e = dtype == FA_DTYPE_F32 ? fa::launch_f32(P, s) : fa::launch_bf16(P, s);
     if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                                    int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, int64_t q_sb,
+                                    int64_t q_sh, int64_t q_st, int64_t k_sb, int64_t k_sh, int64_t k_st,
+                                    int64_t v_sb, int64_t v_sh, int64_t v_st, int64_t o_sb, int64_t o_sh,
+                                    int64_t o_st, float scale, int64_t q_offset, int causal, int64_t window,
+                                    const float *sinks, const float *mask, int64_t mask_sb, int64_t mask_sh,
+                                    int64_t mask_sq, int64_t mask_sk, int dtype, void *stream) {
+    const int64_t qs[3] = {q_sb, q_sh, q_st}, ks[3] = {k_sb, k_sh, k_st}, vs[3] = {v_sb, v_sh, v_st},
+                  os[3] = {o_sb, o_sh, o_st};
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, qs, ks, vs, os, scale, q_offset, causal, window, sinks,
+                    mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream);
+}
+
+extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                            int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, float scale,
+                            int64_t q_offset, int causal, int64_t window, const float *sinks, const float *mask,
+                            int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk, int dtype,
+                            void *stream) {
+    // Contiguous [B, H, T, d]; products are checked for overflow in fwd_impl
+    // through the element counts, so wrapped strides only reach it when those
+    // counts are rejected first.
+    const uint64_t uq = (uint64_t)(Tq < 0 ? 0 : Tq) * (uint64_t)(d < 0 ? 0 : d);
+    const uint64_t uk = (uint64_t)(Tk < 0 ? 0 : Tk) * (uint64_t)(d < 0 ? 0 : d);
+    const int64_t qs[3] = {(int64_t)(uq * (uint64_t)(Hq < 0 ? 0 : Hq)), (int64_t)uq, d},
+                  ks[3] = {(int64_t)(uk * (uint64_t)(Hkv < 0 ? 0 : Hkv)), (int64_t)uk, d};
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, qs, ks, ks, qs, scale, q_offset, causal, window, sinks,
+                    mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream);
 }

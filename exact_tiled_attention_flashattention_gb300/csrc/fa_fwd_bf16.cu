@@ -96,11 +96,11 @@ constexpr int kMaxStages = 6;
 // The two ways rows are mapped onto 128-row tiles.
 //   kPrefill  a unit is one 128-row query tile of one (batch, query head);
 //             persistent grid, heaviest units first.
-//   kDecode   all group * Tq query rows of a KV head (heads of a GQA group are
-//             contiguous in q and o) form one tile, so K and V are read once
-//             per KV head; the unit's key range is split over the CTAs of a
-//             cluster, which merge their partial (m, l, O) through
-//             distributed shared memory.
+//   kDecode   all group * Tq query rows of a KV head form one tile (row
+//             r = i * group + hl: query head g * group + hl, its row i), so K
+//             and V are read once per KV head; the unit's key range is split
+//             over the CTAs of a cluster, which merge their partial (m, l, O)
+//             through distributed shared memory.
 constexpr int kPrefill = 0, kDecode = 1;
 
 template <int D, int MODE>
@@ -144,9 +144,7 @@ struct Barriers {
 
 struct Unit {
     int b, h, g, bh;
-    int kv_head;  // K/V tensor-map head coordinate: b * Hkv + g
-    int q_head;   // Q/O tensor-map head coordinate
-    int r0;       // Q/O tensor-map row of the tile's first row
+    int r0;  // first query row of the tile (prefill)
     int t_begin, n_tiles;
 };
 
@@ -169,8 +167,6 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     }
     U.bh = U.b * P.Hq + U.h;
     U.g = U.h / P.group;
-    U.kv_head = U.b * P.Hkv + U.g;
-    U.q_head = U.bh;
     U.r0 = qt * kBM;
     int64_t lo_a, hi_a, lo_b, hi_b;
     visible_range(P, (int64_t)P.q_offset + U.r0, lo_a, hi_a);
@@ -197,8 +193,6 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
     U.g = cid % P.Hkv;
     U.h = U.g * P.group;
     U.bh = U.b * P.Hq + U.h;
-    U.kv_head = cid;
-    U.q_head = cid;
     U.r0 = 0;
     int64_t lo_a, hi_a, lo_b, hi_b;
     visible_range(P, (int64_t)P.q_offset, lo_a, hi_a);
@@ -321,7 +315,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         const Unit U = get_unit<MODE, PAIR>(P, u, rank);
         const int n = U.n_tiles;
         if (n == 0) continue;
-        const int kv_head = U.kv_head;
+
         // Tile t of the unit into the next stage of a ring; the stage is
         // refilled once every CTA reading it released its previous use.
         auto load_tile = [&](uint32_t ring, int stages, uint64_t *full, uint64_t *empty, int *issued, RingPos &pos,
@@ -334,10 +328,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             for (int c = 0; c < L::kBoxes; ++c) {
                 uint8_t *dst = smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes);
                 if (PAIR == 2)
-                    tma_load_3d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * 64,
-                                          key0 + rank * (kBN / 2), kv_head, (uint16_t)0x3);
+                    tma_load_4d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * 64,
+                                          key0 + rank * (kBN / 2), U.g, U.b, (uint16_t)0x3);
                 else
-                    tma_load_3d(dst, map, &full[st], c * 64, key0, kv_head);
+                    tma_load_4d(dst, map, &full[st], c * 64, key0, U.g, U.b);
             }
             ++issued[st];
             if (++pos.st == stages) {
@@ -356,10 +350,18 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         if (n > 1 && !(ok = load_k(1))) break;
         // Q of this unit, once the previous unit's S MMAs are done with the buffer.
         if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
-        mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
+        if constexpr (MODE == kDecode) {
+            // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
+            mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
-        for (int c = 0; c < L::kBoxes; ++c)
-            tma_load_3d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.q_head);
+            for (int c = 0; c < L::kBoxes; ++c)
+                tma_load_5d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, 0, 0, U.g, U.b);
+        } else {
+            mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
+#pragma unroll
+            for (int c = 0; c < L::kBoxes; ++c)
+                tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.h, U.b);
+        }
         ++q_issued;
         for (int j = 0; j < n && ok; ++j) {
             ok = load_v(j);
@@ -505,16 +507,17 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         const Unit U = get_unit<MODE, PAIR>(P, u, rank);
         const int n = U.n_tiles;
         // The row's query head h and its row i in that head.  Prefill: the
-        // unit's head, consecutive rows.  Packed rows: row = (h - g group) Tq + i,
-        // and rows from group * Tq on are padding that sees no key.
+        // unit's head, consecutive rows.  Packed rows: row = i * group + hl
+        // (h = g * group + hl), and rows from group * Tq on are padding that
+        // sees no key.
         int h = U.h, i = U.r0 + row;
         bool live;  // the row holds a query
         int64_t p_first = (int64_t)P.q_offset + U.r0, p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
         if constexpr (MODE == kDecode) {
             live = row < P.group * P.Tq;
-            const int hl = live ? row / P.Tq : 0;
+            const int hl = live ? row % P.group : 0;
             h = U.g * P.group + hl;
-            i = live ? row - hl * P.Tq : 0;
+            i = live ? row / P.group : 0;
             p_first = P.q_offset;
             p_last = (int64_t)P.q_offset + P.Tq - 1;
         } else {
@@ -735,7 +738,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 if (lane == 0) {
     #pragma unroll
                     for (int cb = 0; cb < L::kBoxes; ++cb)
-                        tma_store_3d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.bh);
+                        tma_store_4d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.h, U.b);
                     bulk_commit_group();
                 }
             }
@@ -763,10 +766,10 @@ __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
     const int S = P.splits, rank = (int)blockIdx.x % S, cid = (int)blockIdx.x / S;
     const int R = P.group * P.Tq;
     const uint32_t op0 = smem_u32(smem + L::kKRing), st0 = smem_u32(smem + L::kVRing);
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P.o) + (int64_t)cid * R * P.d;
-    float *lse_out = P.lse != nullptr ? P.lse + (int64_t)cid * R : nullptr;
+    const int b = cid / P.Hkv, g = cid % P.Hkv;
     for (int e = rank * kThreads + (int)threadIdx.x; e < R * P.d; e += S * kThreads) {
         const int row = e / P.d, col = e - row * P.d;
+        const int h = g * P.group + row % P.group, i = row / P.group;  // row = i * group + (h - g group)
         float M = -INFINITY;
         for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ld_cluster_f32(map_to_rank(st0 + row * 8, sp)));
         float lsum = 0.f, acc = 0.f;
@@ -778,8 +781,9 @@ __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
             acc = sp == 0 ? w * ov : fmaf(w, ov, acc);
         }
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        out[(int64_t)row * P.d + col] = __float2bfloat16_rn(acc * inv);
-        if (col == 0 && lse_out != nullptr) lse_out[row] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+        static_cast<__nv_bfloat16 *>(P.o)[b * P.o_sb + h * P.o_sh + i * P.o_st + col] = __float2bfloat16_rn(acc * inv);
+        if (col == 0 && P.lse != nullptr)
+            P.lse[((int64_t)b * P.Hq + h) * P.Tq + i] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
     }
 }
 
@@ -886,16 +890,57 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [heads, rows, d] bf16 viewed as a 3-D tensor; boxes of 64 columns x box_rows
-// rows with the 128-byte swizzle; rows past `rows` read as zero.
-bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int rows, int heads, int box_rows) {
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+// A bf16 tensor map over `rank` dimensions, dims[0] = d contiguous, the
+// others with element strides; boxes of 64 columns by box[1..] elements with
+// the 128-byte swizzle.  Coordinates outside the tensor read as zero (loads)
+// or are dropped (stores).  A dimension of extent 1 is never stepped, so it
+// gets a packed stride whatever the caller's.
+bool encode_bf16(EncodeTiledFn enc, CUtensorMap *map, const void *base, int rank, const int64_t *dims,
+                 const int64_t *strides, const uint32_t *box) {
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    uint64_t packed = (uint64_t)dims[0] * 2;
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = (cuuint64_t)dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i > 0) {
+            gs[i - 1] = dims[i] > 1 ? (cuuint64_t)strides[i] * 2 : (cuuint64_t)packed;
+            packed = (uint64_t)gs[i - 1] * (uint64_t)dims[i];
+        }
+    }
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bx, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [B, H, T, d] with element strides (sb, sh, st) as the 4-D map (d, T, H, B);
+// boxes of 64 columns x box_rows rows of one (batch, head).
+bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int T, int H, int B, int64_t st,
+              int64_t sh, int64_t sb, int box_rows) {
+    const int64_t dims[4] = {d, T, H, B}, strides[4] = {1, st, sh, sb};
+    const uint32_t box[4] = {64, (uint32_t)box_rows, 1, 1};
+    return encode_bf16(enc, map, base, 4, dims, strides, box);
+}
+
+// The query rows of one KV group as the 5-D map (d, group, Tq, Hkv, B): head
+// g * group + hl at row i is coordinate (., hl, i, g, b), and one box of 64
+// columns x group x Tq lands in shared memory as rows i * group + hl.
+bool make_packed_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, const Params &P, int64_t st, int64_t sh,
+                     int64_t sb) {
+    const int64_t dims[5] = {P.d, P.group, P.Tq, P.Hkv, P.B}, strides[5] = {1, sh, st, sh * P.group, sb};
+    const uint32_t box[5] = {64, (uint32_t)P.group, (uint32_t)P.Tq, 1, 1};
+    return encode_bf16(enc, map, base, 5, dims, strides, box);
+}
+
+// The K and V maps; with Tk == 0 no key tile is ever loaded and the maps only
+// need to be valid (they then describe q).
+bool make_kv_maps(EncodeTiledFn enc, CUtensorMap *tk, CUtensorMap *tv, const Params &P, int box_rows) {
+    if (P.Tk == 0)
+        return make_map(enc, tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, P.q_sb, box_rows) &&
+               make_map(enc, tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, P.q_sb, box_rows);
+    return make_map(enc, tk, P.k, P.d, P.Tk, P.Hkv, P.B, P.k_st, P.k_sh, P.k_sb, box_rows) &&
+           make_map(enc, tv, P.v, P.d, P.Tk, P.Hkv, P.B, P.v_st, P.v_sh, P.v_sb, box_rows);
 }
 
 // Streaming multiprocessors of the current device (cached per device).
@@ -916,17 +961,12 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     CUtensorMap tq, tk, tv, to;
-    // With Tk == 0 no key tile is ever loaded; the K/V maps only need to be valid.
-    const void *kb = P.Tk > 0 ? P.k : P.q;
-    const void *vb = P.Tk > 0 ? P.v : P.q;
-    const int krows = P.Tk > 0 ? P.Tk : 1;
-    const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
     // The maps carry the true head dimension d <= D: columns [d, D) of Q, K
     // and V load as zero (leaving S exact and O's extra columns zero), and the
     // O store drops them.
-    if (!make_map(enc, &tq, P.q, P.d, P.Tq, P.B * P.Hq, kBM) ||
-        !make_map(enc, &tk, kb, P.d, krows, kheads, kBN / PAIR) ||
-        !make_map(enc, &tv, vb, P.d, krows, kheads, kBN / PAIR) || !make_map(enc, &to, P.o, P.d, P.Tq, P.B * P.Hq, kBM))
+    if (!make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM) ||
+        !make_kv_maps(enc, &tk, &tv, P, kBN / PAIR) ||
+        !make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM))
         return cudaErrorInvalidValue;
     // The CTA takes all 512 tensor-memory columns; the shared-memory request
     // (the K/V ring fills it) keeps a second CTA off the SM.
@@ -987,13 +1027,10 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     const int n = packed_tiles(P);
     const int R = P.group * P.Tq;
     CUtensorMap tq, tk, tv, to;
-    const void *kb = P.Tk > 0 ? P.k : P.q;
-    const void *vb = P.Tk > 0 ? P.v : P.q;
-    const int krows = P.Tk > 0 ? P.Tk : 1;
-    const int kheads = P.Tk > 0 ? P.B * P.Hkv : 1;
-    // q and o viewed as [B * Hkv, group * Tq, d]: a KV group's heads are contiguous.
-    if (!make_map(enc, &tq, P.q, P.d, R, P.B * P.Hkv, kBM) || !make_map(enc, &tk, kb, P.d, krows, kheads, kBN) ||
-        !make_map(enc, &tv, vb, P.d, krows, kheads, kBN) || !make_map(enc, &to, P.o, P.d, R, P.B * P.Hkv, kBM))
+    (void)R;
+    // to is not used by the packed path (O leaves through the merge).
+    if (!make_packed_map(enc, &tq, P.q, P, P.q_st, P.q_sh, P.q_sb) || !make_kv_maps(enc, &tk, &tv, P, kBN) ||
+        !make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM))
         return cudaErrorInvalidValue;
     constexpr size_t kSmem = SmemLayout<D, kDecode>::kTotal + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");

@@ -59,19 +59,22 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// Stage rows [row0, row0 + 64) of a [T, d] fp32 matrix into dst[64][DT + 4],
-// zero-filling rows outside [0, T) and columns [d, DT).
+// Stage rows [row0, row0 + 64) of a [T, d] fp32 matrix with row stride `ld`
+// (elements) into dst[64][DT + 4], zero-filling rows outside [0, T) and
+// columns [d, DT).  vec16: every row starts on a 16-byte boundary and d is a
+// multiple of 4 (16-byte copies); otherwise rows start on 8-byte boundaries.
 template <int DT>
-__device__ __forceinline__ void stage_rows(float *dst, const float *src, int row0, int T, int d) {
+__device__ __forceinline__ void stage_rows(float *dst, const float *src, int row0, int T, int d, int64_t ld,
+                                           bool vec16) {
     constexpr int LD = DT + 4;
-    if ((d & 3) == 0) {
+    if (vec16) {
         constexpr int kChunks = DT / 4;
 #pragma unroll 4
         for (int c = threadIdx.x; c < kBr * kChunks; c += kThreads) {
             const int r = c / kChunks, col = (c % kChunks) * 4;
             const int row = row0 + r;
             const bool ok = row < T && col < d;
-            const float *g = ok ? src + (int64_t)row * d + col : src;
+            const float *g = ok ? src + (int64_t)row * ld + col : src;
             cp_async16(dst + r * LD + col, g, ok ? 16 : 0);
         }
     } else {
@@ -81,7 +84,7 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, int row
             const int r = c / kChunks, col = (c % kChunks) * 2;
             const int row = row0 + r;
             const bool ok = row < T && col < d;
-            const float *g = ok ? src + (int64_t)row * d + col : src;
+            const float *g = ok ? src + (int64_t)row * ld + col : src;
             cp_async8(dst + r * LD + col, g, ok ? 8 : 0);
         }
     }
@@ -107,9 +110,9 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
     const int g = h / P.group;
     const int r0 = qt * kBr;
 
-    const float *qh = static_cast<const float *>(P.q) + (int64_t)bh * P.Tq * P.d;
-    const float *kh = static_cast<const float *>(P.k) + (int64_t)(b * P.Hkv + g) * P.Tk * P.d;
-    const float *vh = static_cast<const float *>(P.v) + (int64_t)(b * P.Hkv + g) * P.Tk * P.d;
+    const float *qh = static_cast<const float *>(P.q) + b * P.q_sb + h * P.q_sh;
+    const float *kh = static_cast<const float *>(P.k) + b * P.k_sb + g * P.k_sh;
+    const float *vh = static_cast<const float *>(P.v) + b * P.v_sb + g * P.v_sh;
 
     // Key tiles any row of this query tile can see.
     const int64_t p_first = (int64_t)P.q_offset + r0;
@@ -133,14 +136,14 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
         for (int c = 0; c < NC; ++c) acc[a][c] = make_float2(0.f, 0.f);
     }
 
-    stage_rows<DT>(Qs, qh, r0, P.Tq, P.d);
-    if (t_begin < t_end) stage_rows<DT>(Ks, kh, t_begin * kBc, P.Tk, P.d);
+    stage_rows<DT>(Qs, qh, r0, P.Tq, P.d, P.q_st, P.vec16 != 0);
+    if (t_begin < t_end) stage_rows<DT>(Ks, kh, t_begin * kBc, P.Tk, P.d, P.k_st, P.vec16 != 0);
     cp_async_commit();
 
     for (int t = t_begin; t < t_end; ++t) {
         cp_async_wait<0>();
         __syncthreads();  // Q and K_t landed; every thread finished the previous P.V
-        stage_rows<DT>(Vs, vh, t * kBc, P.Tk, P.d);
+        stage_rows<DT>(Vs, vh, t * kBc, P.Tk, P.d, P.v_st, P.vec16 != 0);
         cp_async_commit();
 
         // S = Q K_t^T for rows 4ty+a, keys tx+16b.
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
 
         __syncthreads();  // Pt complete; every thread done with Ks
         if (t + 1 < t_end) {
-            stage_rows<DT>(Ks, kh, (t + 1) * kBc, P.Tk, P.d);
+            stage_rows<DT>(Ks, kh, (t + 1) * kBc, P.Tk, P.d, P.k_st, P.vec16 != 0);
             cp_async_commit();
             cp_async_wait<1>();  // V_t landed; K_{t+1} may still be in flight
         } else {
@@ -257,13 +260,13 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
     cp_async_wait<0>();
 
     // Epilogue: o = acc / l; lse = (m + log2 l) ln 2; empty rows give 0 and -inf.
-    float *oh = static_cast<float *>(P.o) + (int64_t)bh * P.Tq * P.d;
+    float *oh = static_cast<float *>(P.o) + b * P.o_sb + h * P.o_sh;
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
         const int i = r0 + 4 * ty + a;
         if (i >= P.Tq) continue;
         const float inv = l[a] > 0.f ? 1.f / l[a] : 0.f;
-        float *orow = oh + (int64_t)i * P.d;
+        float *orow = oh + (int64_t)i * P.o_st;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             const int col = 2 * tx + 32 * c;

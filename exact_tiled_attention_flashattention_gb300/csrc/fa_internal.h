@@ -23,6 +23,10 @@ struct Params {
     float scale;          // scale applied to q.k
     float scale_log2;     // scale * log2(e)
     int splits;           // bf16 packed-row path: CTAs that split a key range (set by its launcher)
+    // Element strides of q, k, v, o: batch, head, row (the d elements of a
+    // row are contiguous).
+    int64_t q_sb, q_sh, q_st, k_sb, k_sh, k_st, v_sb, v_sh, v_st, o_sb, o_sh, o_st;
+    int vec16;            // fp32: every q/k/v row starts on a 16-byte boundary
 };
 
 // Visible key range [lo, hi) of query position p (absolute), before the mask.

@@ -88,6 +88,34 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk,
                  int dtype, void *stream);
 
+/* The same computation on strided tensors (the layouts of engines that keep
+ * [B, T, H, d] or [T, H*d] buffers; "FlashAttention forward in C" works on
+ * [B, H, T, d] only).  Element (b, h, t, x) of q is at
+ * q[b*q_sb + h*q_sh + t*q_st + x], likewise k, v (with Hkv, Tk) and o; the d
+ * elements of a row are contiguous.  lse stays contiguous [B, Hq, Tq].
+ * fa_fwd(...) is this call with q_sb = Hq*Tq*d, q_sh = Tq*d, q_st = d (and so
+ * on).  Additional errors:
+ *   FA_EINVAL        a negative stride of a dimension of extent > 1, an
+ *                    extent overflowing int64, or o strides that make two
+ *                    output rows overlap (checked by the rule "every stride,
+ *                    in increasing order, covers the span of the smaller
+ *                    dimensions").
+ *   FA_EUNSUPPORTED  bf16: a stride (of a dimension of extent > 1) that is
+ *                    not a multiple of 8 elements (16 bytes, a TMA rule) or
+ *                    reaches 2^40 bytes; fp32: a stride that is odd.
+ * Reading k or v through overlapping rows (a stride of 0 over the batch, say)
+ * is allowed for fp32; the bf16 path needs positive strides. */
+fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d,
+                         int64_t q_sb, int64_t q_sh, int64_t q_st,
+                         int64_t k_sb, int64_t k_sh, int64_t k_st,
+                         int64_t v_sb, int64_t v_sh, int64_t v_st,
+                         int64_t o_sb, int64_t o_sh, int64_t o_st,
+                         float scale, int64_t q_offset, int causal, int64_t window,
+                         const float *sinks,
+                         const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk,
+                         int dtype, void *stream);
+
 /* Message for the last non-OK status on this thread ("" if none).  The
  * pointer stays valid until the next fa_* call on the same thread. */
 const char *fa_last_error(void);

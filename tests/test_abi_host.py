@@ -130,3 +130,42 @@ def test_binding_raises_on_error(lib):
         fa.fa_fwd(q, q, q, o, lse, 1, 6, 4, 4, 4, 8, 0.5, 0, 1, 0, None, None, 0, 0, 0, 0, fa.FA_DTYPE_F32, 0)
     assert ei.value.status == fa.FA_ESHAPE
     assert c.untouched()
+
+
+# ---------------------------------------------------------------- strided
+
+def _strided(fa_mod, **kw):
+    """fa_fwd_strided on fake (aligned, never dereferenced) pointers: every
+    case below is rejected before any launch."""
+    a = dict(B=2, Hq=4, Hkv=2, Tq=8, Tk=8, d=64, dtype=fa_mod.FA_DTYPE_BF16)
+    a.update(kw)
+    B, Hq, Hkv, Tq, Tk, d = a["B"], a["Hq"], a["Hkv"], a["Tq"], a["Tk"], a["d"]
+    qs = a.get("qs", (Hq * Tq * d, Tq * d, d))
+    ks = a.get("ks", (Hkv * Tk * d, Tk * d, d))
+    os_ = a.get("os", qs)
+    p = 1 << 20  # 16-byte aligned fake address
+    return fa_mod.fa_fwd_strided(p, p, p, p, None, B, Hq, Hkv, Tq, Tk, d, qs, ks, ks, os_, 0.125, 0, 1, 0, None,
+                                 None, 0, 0, 0, 0, a["dtype"], 0, check=False)
+
+
+@pytest.mark.parametrize("case,kw,want", [
+    ("negative row stride", dict(qs=(2048, 512, -64)), "FA_EINVAL"),
+    ("output rows overlap", dict(os=(2048, 512, 32)), "FA_EINVAL"),
+    ("output heads overlap", dict(os=(2048, 64, 64)), "FA_EINVAL"),
+    ("bf16 stride not a multiple of 8", dict(qs=(2048, 516, 64), os=(4096, 1024, 128)), "FA_EUNSUPPORTED"),
+    ("bf16 zero batch stride on k", dict(ks=(0, 512, 64)), "FA_EUNSUPPORTED"),
+    ("fp32 odd stride", dict(dtype=1 - 1, qs=(2048, 513, 64), os=(4096, 1024, 128)), "FA_EUNSUPPORTED"),
+])
+def test_strided_rejections(lib, case, kw, want):
+    import exact_tiled_attention_flashattention_gb300 as fa_mod
+    assert _strided(fa_mod, **kw) == getattr(fa_mod, want), case
+    assert fa_mod.fa_last_error() != ""
+
+
+def test_strided_bshd_layout_is_valid_up_to_launch(lib):
+    # A [B, T, H, d] layout passes validation; with B*Hq*Tq == 0 the call is
+    # a no-op (nothing is launched on this GPU-less host).
+    import exact_tiled_attention_flashattention_gb300 as fa_mod
+    B, T, H, d = 2, 8, 4, 64
+    st = _strided(fa_mod, Tq=0, qs=(T * H * d, d, H * d), ks=(T * 2 * d, d, 2 * d))
+    assert st == fa_mod.FA_OK
