@@ -53,6 +53,9 @@ def load():
     lib.fa_fwd_strided.restype = ctypes.c_int
     lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64] + [i64] * 12 + [
         ctypes.c_float, i64, ctypes.c_int, i64, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.fa_fwd_paged.restype = ctypes.c_int
+    lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, i64, vp, i64, i64, i64,
+                                 ctypes.c_float, ctypes.c_int, i64, vp, ctypes.c_int, vp]
     lib.fa_last_error.restype = ctypes.c_char_p
     lib.fa_last_error.argtypes = []
     lib.fa_version.restype = ctypes.c_int
@@ -142,4 +145,40 @@ def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=N
     sc = (1.0 / d ** 0.5) if scale is None else scale
     fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q.stride()[:3], k.stride()[:3], v.stride()[:3],
                    o.stride()[:3], sc, q_offset, causal, window, sinks, mask, *mask_strides, dt, stream)
+    return o, lse
+
+
+def fa_fwd_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tq, d, seq_lens, max_seq_len, block_table, max_blocks,
+                 page_size, num_pages, scale, causal, window, sinks, dtype, stream=None, *, check=True) -> int:
+    """Call the paged-cache C entry point; raises FaError on a non-OK status
+    when ``check``."""
+    lib = load()
+    st = lib.fa_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
+                          int(Tq), int(d), _ptr(seq_lens), int(max_seq_len), _ptr(block_table), int(max_blocks),
+                          int(page_size), int(num_pages), float(scale), int(bool(causal)), int(window), _ptr(sinks),
+                          int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+def paged_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, *, scale=None, causal=True, window=0,
+                    sinks=None, stream=None):
+    """Decode step on paged caches: q [B, Hq, Tq, d] bf16, k_cache/v_cache
+    [num_pages, page_size, Hkv, d] bf16, block_table [B, max_blocks] int32,
+    seq_lens [B] int32 (CUDA tensors).  Returns o [B, Hq, Tq, d], lse."""
+    import torch
+    B, Hq, Tq, d = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("block_table", block_table),
+                    ("seq_lens", seq_lens)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    sc = (1.0 / d ** 0.5) if scale is None else scale
+    fa_fwd_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tq, d, seq_lens, max_seq_len, block_table,
+                 block_table.shape[1], page_size, num_pages, sc, causal, window, sinks, FA_DTYPE_BF16, stream)
     return o, lse

@@ -216,3 +216,77 @@ extern "C" fa_status fa_fwd(const void *q, const void *k, const void *v, void *o
     return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, qs, ks, ks, qs, scale, q_offset, causal, window, sinks,
                     mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream);
 }
+
+extern "C" fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                  int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t d, const int32_t *seq_lens,
+                                  int64_t max_seq_len, const int32_t *block_table, int64_t max_blocks,
+                                  int64_t page_size, int64_t num_pages, float scale, int causal, int64_t window,
+                                  const float *sinks, int dtype, void *stream) {
+    g_last_error[0] = '\0';
+    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return fail(FA_EINVAL, "unknown dtype %d", dtype);
+    if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || d < 0 || max_seq_len < 0 || max_blocks < 0 || page_size < 0 ||
+        num_pages < 0)
+        return fail(FA_EINVAL, "negative size");
+    if (!std::isfinite(scale)) return fail(FA_EINVAL, "scale is not finite");
+    if (Hkv == 0 ? Hq > 0 : (Hkv > Hq || Hq % Hkv != 0))
+        return fail(FA_ESHAPE, "Hq=%lld is not a multiple of Hkv=%lld (or Hkv > Hq)", (long long)Hq,
+                    (long long)Hkv);
+    int64_t rows = 0, elems = 0, cache = 0;
+    if (!mul_ok(B, Hq, rows) || !mul_ok(rows, Tq, rows) || !mul_ok(rows, d, elems) || !mul_ok(num_pages, page_size, cache) ||
+        !mul_ok(cache, Hkv, cache) || !mul_ok(cache, d, cache) || elems > (std::numeric_limits<int64_t>::max() >> 3) ||
+        cache > (std::numeric_limits<int64_t>::max() >> 3))
+        return fail(FA_EINVAL, "element counts overflow");
+    if (rows == 0) return FA_OK;
+    if (!q || !o || !seq_lens) return fail(FA_EINVAL, "q, o or seq_lens is NULL");
+    if (max_seq_len > 0 && (!k_cache || !v_cache || !block_table))
+        return fail(FA_EINVAL, "k_cache, v_cache or block_table is NULL");
+    if (dtype != FA_DTYPE_BF16) return fail(FA_EUNSUPPORTED, "the paged path is bf16 only");
+    if (d % 8 != 0 || d == 0 || d > 128)
+        return fail(FA_EUNSUPPORTED, "bf16 path supports d a multiple of 8 up to 128 (got %lld)", (long long)d);
+    if (Hq / Hkv * Tq > 128)
+        return fail(FA_EUNSUPPORTED, "paged path: (Hq / Hkv) * Tq must be at most 128 (decode steps)");
+    if (max_seq_len > 0) {
+        if (page_size < 8 || (page_size <= 128 ? (128 % page_size != 0) : (page_size % 128 != 0)))
+            return fail(FA_EUNSUPPORTED, "page_size must divide 128 (and be >= 8) or be a multiple of 128");
+        if (max_blocks == 0 || max_seq_len > max_blocks * page_size)
+            return fail(FA_EINVAL, "max_seq_len exceeds max_blocks * page_size");
+        if (num_pages == 0 || num_pages > 0x7fffffff || max_blocks > 0x7fffffff)
+            return fail(FA_EUNSUPPORTED, "num_pages and max_blocks must be in [1, 2^31)");
+    }
+    if (max_seq_len >= kMaxLen || Tq >= kMaxLen) return fail(FA_EUNSUPPORTED, "lengths must be below 2^30");
+    if (B * Hq >= (int64_t(1) << 24)) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^24");
+    if (!aligned16(q) || !aligned16(o) || (max_seq_len > 0 && (!aligned16(k_cache) || !aligned16(v_cache))))
+        return fail(FA_EUNSUPPORTED, "q, o and the caches must be 16-byte aligned");
+
+    fa::Params P;
+    std::memset(&P, 0, sizeof P);
+    P.q = q;
+    P.k = k_cache;
+    P.v = v_cache;
+    P.o = o;
+    P.lse = lse;
+    P.sinks = sinks;
+    P.B = (int)B;
+    P.Hq = (int)Hq;
+    P.Hkv = (int)Hkv;
+    P.Tq = (int)Tq;
+    P.Tk = (int)max_seq_len;
+    P.d = (int)d;
+    P.group = (int)(Hq / Hkv);
+    P.splits = 1;
+    P.q_sb = Hq * Tq * d, P.q_sh = Tq * d, P.q_st = d;
+    P.o_sb = P.q_sb, P.o_sh = P.q_sh, P.o_st = P.q_st;
+    P.causal = causal ? 1 : 0;
+    P.window = window <= 0 ? 0 : (window >= 2 * kMaxLen ? 0 : (int)window);
+    P.scale = scale;
+    P.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    P.seq_lens = seq_lens;
+    P.block_table = block_table;
+    P.max_blocks = (int)max_blocks;
+    P.page_size = (int)(page_size > 0 ? page_size : 128);
+    P.num_pages = (int)(num_pages > 0 ? num_pages : 1);
+    P.max_seq_len = (int)max_seq_len;
+    cudaError_t e = fa::launch_bf16_paged(P, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
+    return FA_OK;
+}

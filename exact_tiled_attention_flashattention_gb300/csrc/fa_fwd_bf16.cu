@@ -101,7 +101,9 @@ constexpr int kMaxStages = 6;
 //             and V are read once per KV head; the unit's key range is split
 //             over the CTAs of a cluster, which merge their partial (m, l, O)
 //             through distributed shared memory.
-constexpr int kPrefill = 0, kDecode = 1;
+//   kPaged    kDecode on paged K/V caches with a key count per sequence:
+//             key tiles are gathered page by page through a block table.
+constexpr int kPrefill = 0, kDecode = 1, kPaged = 2;
 
 template <int D, int MODE>
 struct SmemLayout {
@@ -111,12 +113,12 @@ struct SmemLayout {
     static constexpr int kStages = D == 128 ? 3 : 6;      // K ring: 96 KB
     // V ring: one stage fewer in prefill, where the O tile is staged for its
     // TMA store; packed rows write O from registers and take the full ring.
-    static constexpr int kVStages = MODE == kDecode ? kStages : kStages - 1;
+    static constexpr int kVStages = MODE != kPrefill ? kStages : kStages - 1;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKRing = kQ + kQBytes;
     static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
     static constexpr uint32_t kOStage = kVRing + kVStages * kKVBytes;  // O tile, bf16, for the TMA store
-    static constexpr uint32_t kBar = kOStage + (MODE == kDecode ? 0u : kQBytes);
+    static constexpr uint32_t kBar = kOStage + (MODE != kPrefill ? 0u : kQBytes);
     // Packed-row split merge: O partials (fp32, padded rows) over the K ring,
     // (m, l) per row over the V ring.
     static constexpr int kOPartStride = D + 4;
@@ -146,6 +148,7 @@ struct Unit {
     int b, h, g, bh;
     int r0;  // first query row of the tile (prefill)
     int t_begin, n_tiles;
+    int Tk, q_offset;  // keys of the unit's sequence, position of its query row 0
 };
 
 // Units sorted heaviest first: unit u has query tile nqt-1-u/per_qt.  With
@@ -168,6 +171,8 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     U.bh = U.b * P.Hq + U.h;
     U.g = U.h / P.group;
     U.r0 = qt * kBM;
+    U.Tk = P.Tk;
+    U.q_offset = P.q_offset;
     int64_t lo_a, hi_a, lo_b, hi_b;
     visible_range(P, (int64_t)P.q_offset + U.r0, lo_a, hi_a);
     visible_range(P, (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1, lo_b, hi_b);
@@ -186,6 +191,7 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
 // tiles [t_begin, t_begin + n_tiles) = this CTA's share (cluster rank
 // blockIdx.x % splits) of the tiles the rows at positions q_offset ..
 // q_offset + Tq - 1 can see.
+template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const Params &P) {
     Unit U;
     const int cid = (int)blockIdx.x / P.splits, rank = (int)blockIdx.x % P.splits;
@@ -194,9 +200,17 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
     U.h = U.g * P.group;
     U.bh = U.b * P.Hq + U.h;
     U.r0 = 0;
+    if constexpr (MODE == kPaged) {
+        // the sequence's cache length; its Tq queries are its last positions
+        U.Tk = min(max(__ldg(P.seq_lens + U.b), 0), P.max_seq_len);
+        U.q_offset = U.Tk - P.Tq;  // rows at negative positions see no key
+    } else {
+        U.Tk = P.Tk;
+        U.q_offset = P.q_offset;
+    }
     int64_t lo_a, hi_a, lo_b, hi_b;
-    visible_range(P, (int64_t)P.q_offset, lo_a, hi_a);
-    visible_range(P, (int64_t)P.q_offset + P.Tq - 1, lo_b, hi_b);
+    visible_range_tk(P, U.Tk, (int64_t)U.q_offset, lo_a, hi_a);
+    visible_range_tk(P, U.Tk, (int64_t)U.q_offset + P.Tq - 1, lo_b, hi_b);
     const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
     U.t_begin = 0;
     U.n_tiles = 0;
@@ -214,8 +228,8 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
 
 template <int MODE, int PAIR>
 __device__ __forceinline__ Unit get_unit(const Params &P, int u, int rank) {
-    if constexpr (MODE == kDecode)
-        return decode_unit(P);
+    if constexpr (MODE != kPrefill)
+        return decode_unit<MODE>(P);
     else
         return make_unit<PAIR>(P, u, rank);
 }
@@ -232,7 +246,7 @@ struct Schedule {
 
 template <int MODE, int PAIR>
 __device__ __forceinline__ Schedule make_schedule(const Params &P) {
-    if constexpr (MODE == kDecode) return Schedule{1, 1, 0};  // one unit per CTA
+    if constexpr (MODE != kPrefill) return Schedule{1, 1, 0};  // one unit per CTA
     const int nqt = (P.Tq + kBM - 1) / kBM;
     const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
     return Schedule{nqt * per_qt, (int)(gridDim.x / PAIR), (int)(blockIdx.x / PAIR)};
@@ -324,6 +338,22 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             if (issued[st] > 0 && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
             mbar_arrive_expect_tx(&full[st], L::kKVBytes);  // halves from both CTAs
             const int key0 = (U.t_begin + t) * kBN;
+            if constexpr (MODE == kPaged) {
+                // Runs of min(page_size, 128) keys, each from its page; keys
+                // past the sequence (or past the table) read page -1: zeros.
+                const int run = P.page_size < kBN ? P.page_size : kBN;
+                for (int k0 = 0; k0 < kBN; k0 += run) {
+                    const int key = key0 + k0;
+                    const int blk = key / P.page_size;
+                    const int page = (key < U.Tk && blk < P.max_blocks)
+                                         ? __ldg(P.block_table + (int64_t)U.b * P.max_blocks + blk)
+                                         : -1;
+#pragma unroll
+                    for (int c = 0; c < L::kBoxes; ++c)
+                        tma_load_4d(smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes) + k0 * kSwRowBytes, map,
+                                    &full[st], c * 64, key % P.page_size, U.g, page);
+                }
+            } else {
 #pragma unroll
             for (int c = 0; c < L::kBoxes; ++c) {
                 uint8_t *dst = smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes);
@@ -332,6 +362,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
                                           key0 + rank * (kBN / 2), U.g, U.b, (uint16_t)0x3);
                 else
                     tma_load_4d(dst, map, &full[st], c * 64, key0, U.g, U.b);
+            }
             }
             ++issued[st];
             if (++pos.st == stages) {
@@ -350,7 +381,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         if (n > 1 && !(ok = load_k(1))) break;
         // Q of this unit, once the previous unit's S MMAs are done with the buffer.
         if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
-        if constexpr (MODE == kDecode) {
+        if constexpr (MODE != kPrefill) {
             // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
             mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
@@ -512,38 +543,44 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         // sees no key.
         int h = U.h, i = U.r0 + row;
         bool live;  // the row holds a query
-        int64_t p_first = (int64_t)P.q_offset + U.r0, p_last = (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1;
-        if constexpr (MODE == kDecode) {
+        // Keys and query position of the unit's sequence: the call's, or the
+        // sequence's own with paged K/V (kernel parameters stay in the
+        // constant bank otherwise).
+        const int uTk = MODE == kPaged ? U.Tk : P.Tk;
+        const int uq0 = MODE == kPaged ? U.q_offset : P.q_offset;
+        int64_t p_first = (int64_t)uq0 + U.r0, p_last = (int64_t)uq0 + min(U.r0 + kBM, P.Tq) - 1;
+        if constexpr (MODE != kPrefill) {
             live = row < P.group * P.Tq;
             const int hl = live ? row % P.group : 0;
             h = U.g * P.group + hl;
             i = live ? row / P.group : 0;
-            p_first = P.q_offset;
-            p_last = (int64_t)P.q_offset + P.Tq - 1;
+            p_first = uq0;
+            p_last = (int64_t)uq0 + P.Tq - 1;
         } else {
             live = i < P.Tq;
         }
-        const int64_t p = (int64_t)P.q_offset + i;
+        const int64_t p = (int64_t)uq0 + i;
         // Per-row visible key interval [vlo, vhi) before the additive mask.
         int vlo = 0, vhi = 0;  // within [0, Tk]
-        if (MODE != kDecode || live) {
+        if (MODE == kPrefill || live) {
             int64_t lo64, hi64;
-            visible_range(P, p, lo64, hi64);
+            visible_range_tk(P, uTk, p, lo64, hi64);
             vlo = (int)lo64;
             vhi = (int)hi64;
         }
         const bool has_sink = P.sinks != nullptr;
         // The sink joins the sum once: in the first CTA of a split key range.
-        const bool sink_here = has_sink && half == 0 && (MODE != kDecode || (int)blockIdx.x % P.splits == 0);
+        const bool sink_here = has_sink && half == 0 && (MODE == kPrefill || (int)blockIdx.x % P.splits == 0);
         float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;  // log2 units
         float l = sink_here ? 1.f : 0.f;                                // this thread's share of the sum
-        const float *mrow =
-            (P.mask != nullptr && live) ? P.mask + U.b * P.msb + h * P.msh + (int64_t)i * P.msq : nullptr;
+        const float *mrow = (MODE != kPaged && P.mask != nullptr && live)
+                                ? P.mask + U.b * P.msb + h * P.msh + (int64_t)i * P.msq
+                                : nullptr;
         // Tiles j in [ti_lo, ti_hi) are interior: every key visible to every
         // row of the unit, and no additive mask.
         int ti_lo = 0, ti_hi = 0;
         if (P.mask == nullptr && c > 0.f) {
-            int64_t hi_key = P.Tk;                                       // j0 + kBN <= Tk
+            int64_t hi_key = uTk;                                        // j0 + kBN <= Tk
             if (P.causal && p_first + 1 < hi_key) hi_key = p_first + 1;  // j0 + kBN - 1 <= p_first
             int64_t lo_key = 0;                                          // j0 > p_last - window
             if (P.window > 0 && p_last - P.window + 1 > 0) lo_key = p_last - P.window + 1;
@@ -572,7 +609,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                     // clamped (valid) address and are dropped by the interval.
 #pragma unroll
                     for (int e = 0; e < kHK; ++e) {
-                        const int jj = min(k0 + e, P.Tk - 1);
+                        const int jj = min(k0 + e, P.Tk - 1);  // (no mask with paged K/V)
                         const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
                         s[e] = visible(e) ? x : -INFINITY;
                     }
@@ -673,7 +710,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
         }
-        if constexpr (MODE == kDecode) {
+        if constexpr (MODE != kPrefill) {
             // This CTA's partial result over its share of the keys:
             // unnormalised O (fp32, rows of kOPartStride floats) and (m, l) per
             // row, in the K/V ring space (no copy or MMA is in flight any
@@ -855,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if constexpr (MODE == kDecode) {
+    if constexpr (MODE != kPrefill) {
         cluster_sync();  // every CTA's partial is written
         if (!bar.abort) merge_partials<D>(P, smem);
         cluster_sync();  // no CTA leaves while a peer reads its partial
@@ -1002,11 +1039,12 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR, kPrefill>, tq, tk, tv, to, P);
 }
 
-// Key tiles seen by the rows at positions q_offset .. q_offset + Tq - 1.
-int packed_tiles(const Params &P) {
+// Key tiles seen by the rows at positions q_offset .. q_offset + Tq - 1 among
+// Tk keys.
+int packed_tiles(const Params &P, int Tk, int q_offset) {
     int64_t lo_a, hi_a, lo_b, hi_b;
-    visible_range(P, (int64_t)P.q_offset, lo_a, hi_a);
-    visible_range(P, (int64_t)P.q_offset + P.Tq - 1, lo_b, hi_b);
+    visible_range_tk(P, Tk, (int64_t)q_offset, lo_a, hi_a);
+    visible_range_tk(P, Tk, (int64_t)q_offset + P.Tq - 1, lo_b, hi_b);
     const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
     if (khi <= klo) return 0;
     return (int)((khi + kBN - 1) / kBN - klo / kBN);
@@ -1019,22 +1057,31 @@ int packed_tiles(const Params &P) {
 // matches the prefill kernel bit for bit).  It depends on B * Hkv and on the
 // device's cluster capacity, so split rows are not batch-invariant: the
 // split trades invariance for parallelism.
-template <int D>
+template <int D, int MODE>
 cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     Params P = P0;
-    const int n = packed_tiles(P);
-    const int R = P.group * P.Tq;
+    // Paged: the longest sequence sizes the split (each cluster splits its own range).
+    const int n = MODE == kPaged ? packed_tiles(P, P.max_seq_len, P.max_seq_len > P.Tq ? P.max_seq_len - P.Tq : 0)
+                                 : packed_tiles(P, P.Tk, P.q_offset);
     CUtensorMap tq, tk, tv, to;
-    (void)R;
-    // to is not used by the packed path (O leaves through the merge).
-    if (!make_packed_map(enc, &tq, P.q, P, P.q_st, P.q_sh, P.q_sb) || !make_kv_maps(enc, &tk, &tv, P, kBN) ||
-        !make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM))
-        return cudaErrorInvalidValue;
-    constexpr size_t kSmem = SmemLayout<D, kDecode>::kTotal + 1024;
+    bool ok = make_packed_map(enc, &tq, P.q, P, P.q_st, P.q_sh, P.q_sb) &&
+              // to is not used by the packed path (O leaves through the merge).
+              make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM);
+    if (MODE == kPaged) {
+        // caches [num_pages, page_size, Hkv, d]: the map (d, page_size, Hkv, num_pages)
+        const int run = P.page_size < kBN ? P.page_size : kBN;
+        const int64_t st = (int64_t)P.Hkv * P.d, sp = (int64_t)P.page_size * st;
+        ok = ok && make_map(enc, &tk, P.k, P.d, P.page_size, P.Hkv, P.num_pages, st, P.d, sp, run) &&
+             make_map(enc, &tv, P.v, P.d, P.page_size, P.Hkv, P.num_pages, st, P.d, sp, run);
+    } else {
+        ok = ok && make_kv_maps(enc, &tk, &tv, P, kBN);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    constexpr size_t kSmem = SmemLayout<D, MODE>::kTotal + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    auto kernel = fa_fwd_bf16_kernel<D, 1, kDecode>;
+    auto kernel = fa_fwd_bf16_kernel<D, 1, MODE>;
     constexpr int kMaxSplits = 16;
     static bool configured = false;
     static int capacity[kMaxSplits + 1] = {};  // clusters of s CTAs resident at once
@@ -1083,12 +1130,17 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream) {
+    return P.d <= 64 ? launch_packed<64, kPaged>(P, stream) : launch_packed<128, kPaged>(P, stream);
+}
+
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
     // Pairs of query heads share a KV head when the group size is even.
     const bool pair = (P.group % 2) == 0;
     // d is a multiple of 8 up to 128: the 64- or 128-column kernel, padded.
     // All query rows of a KV group in one tile: the packed-row kernel.
-    if ((int64_t)P.group * P.Tq <= kBM) return P.d <= 64 ? launch_packed<64>(P, stream) : launch_packed<128>(P, stream);
+    if ((int64_t)P.group * P.Tq <= kBM)
+        return P.d <= 64 ? launch_packed<64, kDecode>(P, stream) : launch_packed<128, kDecode>(P, stream);
     if (P.d <= 64) return pair ? launch_d<64, 2>(P, stream) : launch_d<64, 1>(P, stream);
     return pair ? launch_d<128, 2>(P, stream) : launch_d<128, 1>(P, stream);
 }

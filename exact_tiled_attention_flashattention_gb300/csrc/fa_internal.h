@@ -27,16 +27,29 @@ struct Params {
     // row are contiguous).
     int64_t q_sb, q_sh, q_st, k_sb, k_sh, k_st, v_sb, v_sh, v_st, o_sb, o_sh, o_st;
     int vec16;            // fp32: every q/k/v row starts on a 16-byte boundary
+    // Paged K/V (bf16 packed rows): k and v are caches [num_pages, page_size,
+    // Hkv, d]; key j of sequence b is row j % page_size of page
+    // block_table[b * max_blocks + j / page_size]; sequence b has seq_lens[b]
+    // keys (at most max_seq_len) and its Tq queries are its last positions.
+    const int *seq_lens;
+    const int *block_table;
+    int max_blocks, page_size, num_pages, max_seq_len;
 };
 
-// Visible key range [lo, hi) of query position p (absolute), before the mask.
-__host__ __device__ inline void visible_range(const Params &P, int64_t p, int64_t &lo, int64_t &hi) {
-    hi = P.causal ? (p + 1 < (int64_t)P.Tk ? p + 1 : (int64_t)P.Tk) : (int64_t)P.Tk;
+// Visible key range [lo, hi) of query position p (absolute) among Tk keys,
+// before the mask.
+__host__ __device__ inline void visible_range_tk(const Params &P, int64_t Tk, int64_t p, int64_t &lo, int64_t &hi) {
+    hi = P.causal ? (p + 1 < Tk ? p + 1 : Tk) : Tk;
     lo = P.window > 0 ? (p - P.window + 1 > 0 ? p - P.window + 1 : 0) : 0;
     if (hi < lo) hi = lo;
 }
 
+__host__ __device__ inline void visible_range(const Params &P, int64_t p, int64_t &lo, int64_t &hi) {
+    visible_range_tk(P, (int64_t)P.Tk, p, lo, hi);
+}
+
 cudaError_t launch_f32(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream);
+cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream);
 
 }  // namespace fa

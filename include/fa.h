@@ -116,6 +116,34 @@ fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, f
                          const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk,
                          int dtype, void *stream);
 
+/* Decode steps against paged K/V caches (the consumer named on "FlashAttention
+ * forward in C", section 5: paged attention performs the same tile update on
+ * blocks and is held to this kernel bit for bit).  Sequence b holds
+ * seq_lens[b] keys (device int32 [B], at most max_seq_len); its Tq queries
+ * q[b, :, 0..Tq) are its last Tq positions (q_offset_b = seq_lens[b] - Tq,
+ * the rows below 0 seeing no key).  Key j of sequence b and KV head g is
+ * k_cache[page, j % page_size, g, :] with page = block_table[b * max_blocks +
+ * j / page_size] (device int32); the caches are contiguous
+ * [num_pages, page_size, Hkv, d], q and o contiguous [B, Hq, Tq, d], lse
+ * [B, Hq, Tq].  Page indices outside [0, num_pages) read as zero keys; table
+ * entries past a sequence's keys are never read.  The flags are those of
+ * fa_fwd (no additive mask).  Errors as fa_fwd, plus:
+ *   FA_EINVAL        max_seq_len > max_blocks * page_size; NULL seq_lens, or
+ *                    NULL caches / block_table with max_seq_len > 0.
+ *   FA_EUNSUPPORTED  dtype other than bf16; (Hq / Hkv) * Tq > 128;
+ *                    page_size neither a divisor of 128 (>= 8) nor a multiple
+ *                    of 128; num_pages or max_blocks >= 2^31.
+ * A sequence's result equals that of fa_fwd on its keys laid out
+ * contiguously, bit for bit, when both calls split the key range the same
+ * way (same B, Hkv and longest length). */
+fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                       int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t d,
+                       const int32_t *seq_lens, int64_t max_seq_len,
+                       const int32_t *block_table, int64_t max_blocks,
+                       int64_t page_size, int64_t num_pages,
+                       float scale, int causal, int64_t window, const float *sinks,
+                       int dtype, void *stream);
+
 /* Message for the last non-OK status on this thread ("" if none).  The
  * pointer stays valid until the next fa_* call on the same thread. */
 const char *fa_last_error(void);

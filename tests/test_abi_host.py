@@ -169,3 +169,27 @@ def test_strided_bshd_layout_is_valid_up_to_launch(lib):
     B, T, H, d = 2, 8, 4, 64
     st = _strided(fa_mod, Tq=0, qs=(T * H * d, d, H * d), ks=(T * 2 * d, d, 2 * d))
     assert st == fa_mod.FA_OK
+
+
+# ---------------------------------------------------------------- paged
+
+@pytest.mark.parametrize("case,kw,want", [
+    ("fp32 is not paged", dict(dtype=0), "FA_EUNSUPPORTED"),
+    ("group * Tq > 128", dict(Tq=65), "FA_EUNSUPPORTED"),
+    ("page size 48", dict(page_size=48), "FA_EUNSUPPORTED"),
+    ("page size 4", dict(page_size=4), "FA_EUNSUPPORTED"),
+    ("table too short", dict(max_blocks=2), "FA_EINVAL"),
+    ("null seq_lens", dict(seq_lens=None), "FA_EINVAL"),
+    ("negative pages", dict(num_pages=-1), "FA_EINVAL"),
+    ("Hq % Hkv", dict(Hq=6, Hkv=4), "FA_ESHAPE"),
+])
+def test_paged_rejections(lib, case, kw, want):
+    import exact_tiled_attention_flashattention_gb300 as fa_mod
+    a = dict(B=2, Hq=4, Hkv=2, Tq=1, d=64, seq_lens=1 << 20, max_seq_len=1000, max_blocks=16, page_size=64,
+             num_pages=40, dtype=fa_mod.FA_DTYPE_BF16)
+    a.update(kw)
+    p = 1 << 20
+    st = fa_mod.fa_fwd_paged(p, p, p, p, None, a["B"], a["Hq"], a["Hkv"], a["Tq"], a["d"], a["seq_lens"],
+                             a["max_seq_len"], p, a["max_blocks"], a["page_size"], a["num_pages"], 0.125, 1, 0, None,
+                             a["dtype"], 0, check=False)
+    assert st == getattr(fa_mod, want), case
