@@ -233,6 +233,46 @@ def measure_decode(fa, dev, flush, local_rank):
                     "algorithmic_bytes": alg, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
                     "hbm_peak_kind": peak_kind, "clocks": sampler.summary()})
         del sets
+    # Paged caches: the keys of each sequence scattered over shuffled pages.
+    for name, w in workloads.PAGED.items():
+        B, Hq, Hkv, d, ps = w["B"], w["Hq"], w["Hkv"], w["d"], w["page_size"]
+        lens = workloads.paged_lengths(w["seed"], B, w["lo"], w["hi"])
+        max_len = max(lens)
+        blocks = [-(-L // ps) for L in lens]
+        kv_bytes = 2 * sum(lens) * Hkv * d * 2
+        alg = kv_bytes + 2 * B * Hq * d * 2 + 4 * B * Hq
+        n_seq = max(2, min(16, -(-2 * L2_FLUSH_BYTES // kv_bytes)))
+        g = torch.Generator().manual_seed(w["seed"])
+        sets = []
+        for i in range(n_seq):
+            npages = sum(blocks)
+            kc = torch.randn((npages, ps, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+            vc = torch.randn((npages, ps, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+            perm = torch.randperm(npages, generator=g)
+            table = torch.full((B, max(blocks)), -1, dtype=torch.int32)
+            k0 = 0
+            for b in range(B):
+                table[b, :blocks[b]] = perm[k0:k0 + blocks[b]].to(torch.int32)
+                k0 += blocks[b]
+            q = torch.randn((B, Hq, 1, d), generator=g).to(torch.bfloat16).to(dev)
+            sets.append((q, kc, vc, table.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev),
+                         torch.empty_like(q), torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)))
+
+        def seq():
+            for q, kc, vc, table, sl, o, lse in sets:
+                fa.fa_fwd_paged(q, kc, vc, o, lse, B, Hq, Hkv, 1, d, sl, max_len, table, table.shape[1], ps,
+                                kc.shape[0], d ** -0.5, 1, 0, None, fa.FA_DTYPE_BF16, None)
+
+        sampler = ClockSampler(local_rank)
+        med, _ = time_graph(seq, 10, flush)
+        sampler.stop()
+        per_call = med / n_seq
+        gbs = alg / (per_call / 1e3) / 1e9
+        out.append({"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Tk": f"{min(lens)}..{max_len}", "d": d,
+                    "page_size": ps, "us_per_call": round(per_call * 1e3, 2), "calls_in_sequence": n_seq,
+                    "algorithmic_bytes": alg, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
+                    "hbm_peak_kind": peak_kind, "clocks": sampler.summary()})
+        del sets
     return out
 
 

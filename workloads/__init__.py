@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Problem", "qkv", "sinks", "strided_mask", "CONFIGS", "DECODE", "chunk_ranges"]
+__all__ = ["Problem", "qkv", "sinks", "strided_mask", "CONFIGS", "DECODE", "PAGED", "paged_lengths", "chunk_ranges"]
 
 
 @dataclass(frozen=True)
@@ -151,4 +151,19 @@ DECODE = {
         "decode_b8_gqa16x8_d128_k8192", Problem(8, 16, 8, 1, 8192, 128, q_offset=8191), ("bf16",), seeds=(203,)),
     "decode_gqa9x3_d64_k328": Workload(
         "decode_gqa9x3_d64_k328", Problem(1, 9, 3, 1, 328, 64, q_offset=327), ("bf16",), seeds=(204,)),
+}
+
+
+def paged_lengths(seed: int, B: int, lo: int, hi: int) -> list:
+    """Per-sequence cache lengths, uniform in [lo, hi] (seeded)."""
+    g = _gen(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (B,), generator=g)]
+
+
+# Paged decode steps (one new token per sequence over a paged cache): 8 and 32
+# sequences of the 16q/8kv d=128 model with lengths drawn in [4096, 8192],
+# 64-token pages.
+PAGED = {
+    "paged_b8_gqa16x8_d128_k4k-8k_p64": dict(B=8, Hq=16, Hkv=8, d=128, lo=4096, hi=8192, page_size=64, seed=210),
+    "paged_b32_gqa16x8_d128_k4k-8k_p64": dict(B=32, Hq=16, Hkv=8, d=128, lo=4096, hi=8192, page_size=64, seed=211),
 }
