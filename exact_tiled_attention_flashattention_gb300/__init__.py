@@ -56,6 +56,9 @@ def load():
     lib.fa_fwd_paged.restype = ctypes.c_int
     lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, i64, vp, i64, i64, i64,
                                  ctypes.c_float, ctypes.c_int, i64, vp, ctypes.c_int, vp]
+    lib.fa_fwd_varlen.restype = ctypes.c_int
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64, i64, i64, i64] + [i64] * 8 + [
+        ctypes.c_float, ctypes.c_int, i64, vp, ctypes.c_int, vp]
     lib.fa_last_error.restype = ctypes.c_char_p
     lib.fa_last_error.argtypes = []
     lib.fa_version.restype = ctypes.c_int
@@ -181,4 +184,42 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, *, 
     sc = (1.0 / d ** 0.5) if scale is None else scale
     fa_fwd_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tq, d, seq_lens, max_seq_len, block_table,
                  block_table.shape[1], page_size, num_pages, sc, causal, window, sinks, FA_DTYPE_BF16, stream)
+    return o, lse
+
+
+def fa_fwd_varlen(q, k, v, o, lse, B, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q,
+                  max_seqlen_k, q_strides, k_strides, v_strides, o_strides, scale, causal, window, sinks, dtype,
+                  stream=None, *, check=True) -> int:
+    """Call the variable-length C entry point (each *_strides = (head, row)
+    in elements); raises FaError on a non-OK status when ``check``."""
+    lib = load()
+    st = lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(d),
+                           _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(total_q), int(total_k), int(max_seqlen_q),
+                           int(max_seqlen_k), *[int(x) for x in (*q_strides, *k_strides, *v_strides, *o_strides)],
+                           float(scale), int(bool(causal)), int(window), _ptr(sinks), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, scale=None, causal=True,
+                     window=0, sinks=None, stream=None):
+    """Packed sequences: q [total_q, Hq, d], k/v [total_k, Hkv, d] (fp32 or
+    bf16, d contiguous), cu_seqlens_* int32 [B+1] CUDA tensors.  Returns o
+    [total_q, Hq, d] and lse [Hq, total_q]."""
+    import torch
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    dt = FA_DTYPE_F32 if q.dtype == torch.float32 else FA_DTYPE_BF16
+    if q.dtype not in (torch.float32, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share a dtype, fp32 or bf16")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    o = torch.empty((total_q, Hq, d), dtype=q.dtype, device=q.device)
+    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    sc = (1.0 / d ** 0.5) if scale is None else scale
+    fa_fwd_varlen(q, k, v, o, lse, B, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q,
+                  max_seqlen_k, (q.stride(1), q.stride(0)), (k.stride(1), k.stride(0)), (v.stride(1), v.stride(0)),
+                  (o.stride(1), o.stride(0)), sc, causal, window, sinks, dt, stream)
     return o, lse

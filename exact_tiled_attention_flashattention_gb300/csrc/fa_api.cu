@@ -290,3 +290,88 @@ extern "C" fa_status fa_fwd_paged(const void *q, const void *k_cache, const void
     if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
     return FA_OK;
 }
+
+extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                                   int64_t Hq, int64_t Hkv, int64_t d, const int32_t *cu_seqlens_q,
+                                   const int32_t *cu_seqlens_k, int64_t total_q, int64_t total_k,
+                                   int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t q_sh, int64_t q_st,
+                                   int64_t k_sh, int64_t k_st, int64_t v_sh, int64_t v_st, int64_t o_sh,
+                                   int64_t o_st, float scale, int causal, int64_t window, const float *sinks,
+                                   int dtype, void *stream) {
+    g_last_error[0] = '\0';
+    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return fail(FA_EINVAL, "unknown dtype %d", dtype);
+    if (B < 0 || Hq < 0 || Hkv < 0 || d < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+        return fail(FA_EINVAL, "negative size");
+    if (!std::isfinite(scale)) return fail(FA_EINVAL, "scale is not finite");
+    if (Hkv == 0 ? Hq > 0 : (Hkv > Hq || Hq % Hkv != 0))
+        return fail(FA_ESHAPE, "Hq=%lld is not a multiple of Hkv=%lld (or Hkv > Hq)", (long long)Hq,
+                    (long long)Hkv);
+    int64_t span = 0;
+    if (!layout_ok(1, Hq, total_q, d, 0, q_sh, q_st, false, span) ||
+        !layout_ok(1, Hkv, total_k, d, 0, k_sh, k_st, false, span) ||
+        !layout_ok(1, Hkv, total_k, d, 0, v_sh, v_st, false, span))
+        return fail(FA_EINVAL, "q, k or v strides are negative or their extents overflow");
+    if (!layout_ok(1, Hq, total_q, d, 0, o_sh, o_st, true, span))
+        return fail(FA_EINVAL, "o strides are negative or make two output rows overlap");
+    if (B == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query row
+    if (!q || !o || !cu_seqlens_q || !cu_seqlens_k) return fail(FA_EINVAL, "q, o or a cu_seqlens table is NULL");
+    if (total_k > 0 && (!k || !v)) return fail(FA_EINVAL, "k or v is NULL with total_k > 0");
+    if (d == 0 || (d & 1)) return fail(FA_EUNSUPPORTED, "d=%lld: d must be even and positive", (long long)d);
+    if (dtype == FA_DTYPE_F32 && d > 256)
+        return fail(FA_EUNSUPPORTED, "fp32 path supports d <= 256 (got %lld)", (long long)d);
+    if (dtype == FA_DTYPE_BF16 && (d % 8 != 0 || d > 128))
+        return fail(FA_EUNSUPPORTED, "bf16 path supports d a multiple of 8 up to 128 (got %lld)", (long long)d);
+    if (total_q >= kMaxLen || total_k >= kMaxLen || max_seqlen_q > total_q)
+        return fail(FA_EUNSUPPORTED, "totals must be below 2^30 and max_seqlen_q <= total_q");
+    if (B >= (int64_t(1) << 24) || B * Hq >= (int64_t(1) << 31)) return fail(FA_EUNSUPPORTED, "too many sequences");
+    if (!aligned16(q) || !aligned16(o) || (total_k > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
+    const int64_t m = dtype == FA_DTYPE_BF16 ? 8 : 2;
+    const bool kv = total_k > 0;
+    if (!strides_multiple(1, Hq, total_q, 0, q_sh, q_st, m) || !strides_multiple(1, Hq, total_q, 0, o_sh, o_st, m) ||
+        (kv && (!strides_multiple(1, Hkv, total_k, 0, k_sh, k_st, m) ||
+                !strides_multiple(1, Hkv, total_k, 0, v_sh, v_st, m))))
+        return fail(FA_EUNSUPPORTED, "strides must be multiples of %lld elements for this dtype", (long long)m);
+    if (dtype == FA_DTYPE_BF16) {
+        const int64_t st[8] = {q_sh, q_st, k_sh, k_st, v_sh, v_st, o_sh, o_st};
+        const int64_t ext[8] = {Hq, total_q, Hkv, total_k, Hkv, total_k, Hq, total_q};
+        for (int i = 0; i < 8; ++i) {
+            if (st[i] > (int64_t(1) << 39) - 1) return fail(FA_EUNSUPPORTED, "a stride reaches 2^40 bytes");
+            if (ext[i] > 1 && st[i] <= 0) return fail(FA_EUNSUPPORTED, "bf16 strides must be positive (tensor maps)");
+        }
+    }
+
+    fa::Params P;
+    std::memset(&P, 0, sizeof P);
+    P.q = q;
+    P.k = k;
+    P.v = v;
+    P.o = o;
+    P.lse = lse;
+    P.sinks = sinks;
+    P.B = (int)B;
+    P.Hq = (int)Hq;
+    P.Hkv = (int)Hkv;
+    P.Tq = (int)max_seqlen_q;
+    P.Tk = (int)(max_seqlen_k < kMaxLen ? max_seqlen_k : kMaxLen - 1);
+    P.d = (int)d;
+    P.group = (int)(Hq / Hkv);
+    P.splits = 1;
+    P.q_sh = q_sh, P.q_st = q_st, P.k_sh = k_sh, P.k_st = k_st;
+    P.v_sh = v_sh, P.v_st = v_st, P.o_sh = o_sh, P.o_st = o_st;
+    P.vec16 = (d % 4 == 0) && strides_multiple(1, Hq, total_q, 0, q_sh, q_st, 4) &&
+              (!kv || (strides_multiple(1, Hkv, total_k, 0, k_sh, k_st, 4) &&
+                       strides_multiple(1, Hkv, total_k, 0, v_sh, v_st, 4)));
+    P.causal = causal ? 1 : 0;
+    P.window = window <= 0 ? 0 : (window >= 2 * kMaxLen ? 0 : (int)window);
+    P.scale = scale;
+    P.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    P.cu_q = cu_seqlens_q;
+    P.cu_k = cu_seqlens_k;
+    P.total_q = (int)total_q;
+    P.total_k = (int)total_k;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dtype == FA_DTYPE_F32 ? fa::launch_f32_varlen(P, s) : fa::launch_bf16_varlen(P, s);
+    if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
+    return FA_OK;
+}

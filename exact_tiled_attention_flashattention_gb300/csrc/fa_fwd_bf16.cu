@@ -103,7 +103,10 @@ constexpr int kMaxStages = 6;
 //             through distributed shared memory.
 //   kPaged    kDecode on paged K/V caches with a key count per sequence:
 //             key tiles are gathered page by page through a block table.
-constexpr int kPrefill = 0, kDecode = 1, kPaged = 2;
+//   kVarlen   kPrefill over a batch of sequences packed along the rows
+//             ([total, H, d] tensors, cu_seqlens offsets), each with its own
+//             row and key counts; O is written with predicated stores.
+constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3;
 
 template <int D, int MODE>
 struct SmemLayout {
@@ -113,12 +116,13 @@ struct SmemLayout {
     static constexpr int kStages = D == 128 ? 3 : 6;      // K ring: 96 KB
     // V ring: one stage fewer in prefill, where the O tile is staged for its
     // TMA store; packed rows write O from registers and take the full ring.
-    static constexpr int kVStages = MODE != kPrefill ? kStages : kStages - 1;
+    static constexpr bool kStaging = MODE == kPrefill;  // O leaves through a TMA store
+    static constexpr int kVStages = kStaging ? kStages - 1 : kStages;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKRing = kQ + kQBytes;
     static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
     static constexpr uint32_t kOStage = kVRing + kVStages * kKVBytes;  // O tile, bf16, for the TMA store
-    static constexpr uint32_t kBar = kOStage + (MODE != kPrefill ? 0u : kQBytes);
+    static constexpr uint32_t kBar = kOStage + (kStaging ? kQBytes : 0u);
     // Packed-row split merge: O partials (fp32, padded rows) over the K ring,
     // (m, l) per row over the V ring.
     static constexpr int kOPartStride = D + 4;
@@ -149,12 +153,14 @@ struct Unit {
     int r0;  // first query row of the tile (prefill)
     int t_begin, n_tiles;
     int Tk, q_offset;  // keys of the unit's sequence, position of its query row 0
+    int Tq;            // query rows of the unit's sequence
+    int qrow, krow;    // tensor rows where the sequence's queries / keys start
 };
 
 // Units sorted heaviest first: unit u has query tile nqt-1-u/per_qt.  With
 // PAIR == 2 a unit covers query heads 2h' (cluster rank 0) and 2h'+1 (rank 1)
 // of one KV group; `rank` picks this CTA's head.
-template <int PAIR>
+template <int PAIR, int MODE>
 __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     Unit U;
     const int nqt = (P.Tq + kBM - 1) / kBM;
@@ -171,11 +177,30 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     U.bh = U.b * P.Hq + U.h;
     U.g = U.h / P.group;
     U.r0 = qt * kBM;
-    U.Tk = P.Tk;
-    U.q_offset = P.q_offset;
+    if constexpr (MODE == kVarlen) {
+        // offsets clamped into the tensors: a malformed table cannot reach outside them
+        const int q0 = min(max(__ldg(P.cu_q + U.b), 0), P.total_q);
+        const int q1 = min(max(__ldg(P.cu_q + U.b + 1), q0), P.total_q);
+        const int k0 = min(max(__ldg(P.cu_k + U.b), 0), P.total_k);
+        const int k1 = min(max(__ldg(P.cu_k + U.b + 1), k0), P.total_k);
+        U.Tq = q1 - q0;
+        U.Tk = k1 - k0;
+        U.qrow = q0;
+        U.krow = k0;
+        U.q_offset = U.Tk - U.Tq;  // the sequence's queries are its last positions
+    } else {
+        U.Tq = P.Tq;
+        U.Tk = P.Tk;
+        U.qrow = 0;
+        U.krow = 0;
+        U.q_offset = P.q_offset;
+    }
+    U.t_begin = 0;
+    U.n_tiles = 0;
+    if (U.r0 >= U.Tq) return U;  // a tile past the sequence's rows: nothing to do
     int64_t lo_a, hi_a, lo_b, hi_b;
-    visible_range(P, (int64_t)P.q_offset + U.r0, lo_a, hi_a);
-    visible_range(P, (int64_t)P.q_offset + min(U.r0 + kBM, P.Tq) - 1, lo_b, hi_b);
+    visible_range_tk(P, U.Tk, (int64_t)U.q_offset + U.r0, lo_a, hi_a);
+    visible_range_tk(P, U.Tk, (int64_t)U.q_offset + min(U.r0 + kBM, U.Tq) - 1, lo_b, hi_b);
     const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
     if (khi > klo) {
         U.t_begin = (int)(klo / kBN);
@@ -200,6 +225,9 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
     U.h = U.g * P.group;
     U.bh = U.b * P.Hq + U.h;
     U.r0 = 0;
+    U.Tq = P.Tq;
+    U.qrow = 0;
+    U.krow = 0;
     if constexpr (MODE == kPaged) {
         // the sequence's cache length; its Tq queries are its last positions
         U.Tk = min(max(__ldg(P.seq_lens + U.b), 0), P.max_seq_len);
@@ -228,10 +256,10 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
 
 template <int MODE, int PAIR>
 __device__ __forceinline__ Unit get_unit(const Params &P, int u, int rank) {
-    if constexpr (MODE != kPrefill)
+    if constexpr (MODE == kDecode || MODE == kPaged)
         return decode_unit<MODE>(P);
     else
-        return make_unit<PAIR>(P, u, rank);
+        return make_unit<PAIR, MODE>(P, u, rank);
 }
 
 // Snake order over groups: round r gives group g unit r*G + g (r even) or
@@ -246,7 +274,7 @@ struct Schedule {
 
 template <int MODE, int PAIR>
 __device__ __forceinline__ Schedule make_schedule(const Params &P) {
-    if constexpr (MODE != kPrefill) return Schedule{1, 1, 0};  // one unit per CTA
+    if constexpr (MODE == kDecode || MODE == kPaged) return Schedule{1, 1, 0};  // one unit per CTA
     const int nqt = (P.Tq + kBM - 1) / kBM;
     const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
     return Schedule{nqt * per_qt, (int)(gridDim.x / PAIR), (int)(blockIdx.x / PAIR)};
@@ -338,6 +366,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             if (issued[st] > 0 && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
             mbar_arrive_expect_tx(&full[st], L::kKVBytes);  // halves from both CTAs
             const int key0 = (U.t_begin + t) * kBN;
+            const int kvb = MODE == kVarlen ? 0 : U.b;  // varlen tensors have one batch
             if constexpr (MODE == kPaged) {
                 // Runs of min(page_size, 128) keys, each from its page; keys
                 // past the sequence (or past the table) read page -1: zeros.
@@ -359,9 +388,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
                 uint8_t *dst = smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes);
                 if (PAIR == 2)
                     tma_load_4d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * 64,
-                                          key0 + rank * (kBN / 2), U.g, U.b, (uint16_t)0x3);
+                                          U.krow + key0 + rank * (kBN / 2), U.g, kvb, (uint16_t)0x3);
                 else
-                    tma_load_4d(dst, map, &full[st], c * 64, key0, U.g, U.b);
+                    tma_load_4d(dst, map, &full[st], c * 64, U.krow + key0, U.g, kvb);
             }
             }
             ++issued[st];
@@ -381,7 +410,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         if (n > 1 && !(ok = load_k(1))) break;
         // Q of this unit, once the previous unit's S MMAs are done with the buffer.
         if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
-        if constexpr (MODE != kPrefill) {
+        if constexpr (MODE == kDecode || MODE == kPaged) {
             // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
             mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
@@ -391,7 +420,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kBoxes; ++c)
-                tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.r0, U.h, U.b);
+                tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.qrow + U.r0, U.h,
+                            MODE == kVarlen ? 0 : U.b);
         }
         ++q_issued;
         for (int j = 0; j < n && ok; ++j) {
@@ -546,10 +576,13 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         // Keys and query position of the unit's sequence: the call's, or the
         // sequence's own with paged K/V (kernel parameters stay in the
         // constant bank otherwise).
-        const int uTk = MODE == kPaged ? U.Tk : P.Tk;
-        const int uq0 = MODE == kPaged ? U.q_offset : P.q_offset;
-        int64_t p_first = (int64_t)uq0 + U.r0, p_last = (int64_t)uq0 + min(U.r0 + kBM, P.Tq) - 1;
-        if constexpr (MODE != kPrefill) {
+        constexpr bool kSeq = MODE == kPaged || MODE == kVarlen;  // per-sequence lengths
+        const int uTk = kSeq ? U.Tk : P.Tk;
+        const int uq0 = kSeq ? U.q_offset : P.q_offset;
+        const int uTq = MODE == kVarlen ? U.Tq : P.Tq;
+        if (MODE == kVarlen && U.r0 >= uTq) continue;  // a tile past the sequence's rows
+        int64_t p_first = (int64_t)uq0 + U.r0, p_last = (int64_t)uq0 + min(U.r0 + kBM, uTq) - 1;
+        if constexpr (MODE == kDecode || MODE == kPaged) {
             live = row < P.group * P.Tq;
             const int hl = live ? row % P.group : 0;
             h = U.g * P.group + hl;
@@ -557,7 +590,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             p_first = uq0;
             p_last = (int64_t)uq0 + P.Tq - 1;
         } else {
-            live = i < P.Tq;
+            live = i < uTq;
         }
         const int64_t p = (int64_t)uq0 + i;
         // Per-row visible key interval [vlo, vhi) before the additive mask.
@@ -570,10 +603,11 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         }
         const bool has_sink = P.sinks != nullptr;
         // The sink joins the sum once: in the first CTA of a split key range.
-        const bool sink_here = has_sink && half == 0 && (MODE == kPrefill || (int)blockIdx.x % P.splits == 0);
+        const bool sink_here =
+            has_sink && half == 0 && (MODE == kPrefill || MODE == kVarlen || (int)blockIdx.x % P.splits == 0);
         float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;  // log2 units
         float l = sink_here ? 1.f : 0.f;                                // this thread's share of the sum
-        const float *mrow = (MODE != kPaged && P.mask != nullptr && live)
+        const float *mrow = (!kSeq && P.mask != nullptr && live)
                                 ? P.mask + U.b * P.msb + h * P.msh + (int64_t)i * P.msq
                                 : nullptr;
         // Tiles j in [ti_lo, ti_hi) are interior: every key visible to every
@@ -710,7 +744,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
         }
-        if constexpr (MODE != kPrefill) {
+        if constexpr (MODE == kDecode || MODE == kPaged) {
             // This CTA's partial result over its share of the keys:
             // unnormalised O (fp32, rows of kOPartStride floats) and (m, l) per
             // row, in the K/V ring space (no copy or MMA is in flight any
@@ -736,6 +770,36 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             }
             if (n > 0) tc_fence_before();
             if (live && half == 0) stats[row] = make_float2(m, lt);
+        } else if constexpr (MODE == kVarlen) {
+            // The sequence's rows only (a 128-row store would reach into the
+            // next sequence): this thread's half of the row, 16-byte stores.
+#pragma unroll
+            for (int cc = 0; cc < kHD; cc += 32) {
+                uint32_t ov[32];
+                if (n > 0) {
+                    tmem_load_pair32<kHD>(o_addr + cc, ov);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                }
+                if (live) {
+                    const int col0 = half * kHD + cc;  // columns [d, D) are padding: not written
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(P.o) + (int64_t)U.h * P.o_sh +
+                                                           (int64_t)(U.qrow + i) * P.o_st + col0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
+                                              __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
+                        if (col0 + 8 * e < P.d) dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            if (n > 0) tc_fence_before();
+            if (live && P.lse != nullptr && half == 0)
+                P.lse[(int64_t)U.h * P.total_q + U.qrow + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         } else {
             if (threadIdx.x == 0) {
                 bulk_wait_read_all();
@@ -872,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // the peer's barriers exist before any multicast reaches them
     else
         __syncthreads();
-    static_assert(MODE == kPrefill || PAIR == 1, "packed rows run without K/V multicast");
+    static_assert(MODE == kPrefill || MODE == kVarlen || PAIR == 1, "packed rows run without K/V multicast");
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
     // Inputs may come from the previous kernel in the stream, and outputs may
@@ -892,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if constexpr (MODE != kPrefill) {
+    if constexpr (MODE == kDecode || MODE == kPaged) {
         cluster_sync();  // every CTA's partial is written
         if (!bar.abort) merge_partials<D>(P, smem);
         cluster_sync();  // no CTA leaves while a peer reads its partial
@@ -993,25 +1057,38 @@ int sm_count() {
     return cached[dev];
 }
 
-template <int D, int PAIR>
+template <int D, int PAIR, int MODE>
 cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     CUtensorMap tq, tk, tv, to;
     // The maps carry the true head dimension d <= D: columns [d, D) of Q, K
     // and V load as zero (leaving S exact and O's extra columns zero), and the
-    // O store drops them.
-    if (!make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM) ||
-        !make_kv_maps(enc, &tk, &tv, P, kBN / PAIR) ||
-        !make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM))
-        return cudaErrorInvalidValue;
+    // O store drops them.  A variable-length batch is one [total, H, d]
+    // tensor (a batch of one) with the sequences along the rows.
+    bool ok;
+    if (MODE == kVarlen) {
+        ok = make_map(enc, &tq, P.q, P.d, P.total_q, P.Hq, 1, P.q_st, P.q_sh, 0, kBM) &&
+             make_map(enc, &to, P.o, P.d, P.total_q, P.Hq, 1, P.o_st, P.o_sh, 0, kBM);
+        if (P.total_k > 0)
+            ok = ok && make_map(enc, &tk, P.k, P.d, P.total_k, P.Hkv, 1, P.k_st, P.k_sh, 0, kBN / PAIR) &&
+                 make_map(enc, &tv, P.v, P.d, P.total_k, P.Hkv, 1, P.v_st, P.v_sh, 0, kBN / PAIR);
+        else
+            ok = ok && make_map(enc, &tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR) &&
+                 make_map(enc, &tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR);
+    } else {
+        ok = make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM) &&
+             make_kv_maps(enc, &tk, &tv, P, kBN / PAIR) &&
+             make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM);
+    }
+    if (!ok) return cudaErrorInvalidValue;
     // The CTA takes all 512 tensor-memory columns; the shared-memory request
     // (the K/V ring fills it) keeps a second CTA off the SM.
-    constexpr size_t kSmem = SmemLayout<D, kPrefill>::kTotal + 1024;
+    constexpr size_t kSmem = SmemLayout<D, MODE>::kTotal + 1024;
     static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "shared memory budget");
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, PAIR, kPrefill>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, PAIR, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -1036,7 +1113,7 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR, kPrefill>, tq, tk, tv, to, P);
+    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR, MODE>, tq, tk, tv, to, P);
 }
 
 // Key tiles seen by the rows at positions q_offset .. q_offset + Tq - 1 among
@@ -1134,6 +1211,12 @@ cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream) {
     return P.d <= 64 ? launch_packed<64, kPaged>(P, stream) : launch_packed<128, kPaged>(P, stream);
 }
 
+cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream) {
+    const bool pair = (P.group % 2) == 0;
+    if (P.d <= 64) return pair ? launch_d<64, 2, kVarlen>(P, stream) : launch_d<64, 1, kVarlen>(P, stream);
+    return pair ? launch_d<128, 2, kVarlen>(P, stream) : launch_d<128, 1, kVarlen>(P, stream);
+}
+
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
     // Pairs of query heads share a KV head when the group size is even.
     const bool pair = (P.group % 2) == 0;
@@ -1141,8 +1224,8 @@ cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
     // All query rows of a KV group in one tile: the packed-row kernel.
     if ((int64_t)P.group * P.Tq <= kBM)
         return P.d <= 64 ? launch_packed<64, kDecode>(P, stream) : launch_packed<128, kDecode>(P, stream);
-    if (P.d <= 64) return pair ? launch_d<64, 2>(P, stream) : launch_d<64, 1>(P, stream);
-    return pair ? launch_d<128, 2>(P, stream) : launch_d<128, 1>(P, stream);
+    if (P.d <= 64) return pair ? launch_d<64, 2, kPrefill>(P, stream) : launch_d<64, 1, kPrefill>(P, stream);
+    return pair ? launch_d<128, 2, kPrefill>(P, stream) : launch_d<128, 1, kPrefill>(P, stream);
 }
 
 }  // namespace fa

@@ -90,7 +90,7 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, int row
     }
 }
 
-template <int DT>
+template <int DT, bool VARLEN>
 __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
     constexpr int LD = DT + 4;
     constexpr int NC = DT / 32;  // float2 column pairs per thread
@@ -110,16 +110,31 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
     const int g = h / P.group;
     const int r0 = qt * kBr;
 
-    const float *qh = static_cast<const float *>(P.q) + b * P.q_sb + h * P.q_sh;
-    const float *kh = static_cast<const float *>(P.k) + b * P.k_sb + g * P.k_sh;
-    const float *vh = static_cast<const float *>(P.v) + b * P.v_sb + g * P.v_sh;
+    // The sequence's rows, keys and the position of its row 0: the call's,
+    // or (variable-length batch) sequence b's, whose queries are its last
+    // positions, with its rows and keys starting at tensor rows qrow / krow.
+    int Tq = P.Tq, Tk = P.Tk, qoff = P.q_offset;
+    int64_t qrow = 0, krow = 0;
+    if constexpr (VARLEN) {
+        // offsets clamped into the tensors: a malformed table cannot reach outside them
+        const int q0 = min(max(__ldg(P.cu_q + b), 0), P.total_q), k0 = min(max(__ldg(P.cu_k + b), 0), P.total_k);
+        Tq = min(max(__ldg(P.cu_q + b + 1), q0), P.total_q) - q0;
+        Tk = min(max(__ldg(P.cu_k + b + 1), k0), P.total_k) - k0;
+        qoff = Tk - Tq;
+        qrow = q0;
+        krow = k0;
+        if (r0 >= Tq) return;  // a tile past the sequence's rows (the whole block leaves)
+    }
+    const float *qh = static_cast<const float *>(P.q) + (VARLEN ? 0 : b * P.q_sb) + h * P.q_sh + qrow * P.q_st;
+    const float *kh = static_cast<const float *>(P.k) + (VARLEN ? 0 : b * P.k_sb) + g * P.k_sh + krow * P.k_st;
+    const float *vh = static_cast<const float *>(P.v) + (VARLEN ? 0 : b * P.v_sb) + g * P.v_sh + krow * P.v_st;
 
     // Key tiles any row of this query tile can see.
-    const int64_t p_first = (int64_t)P.q_offset + r0;
-    const int64_t p_last = (int64_t)P.q_offset + min(r0 + kBr, P.Tq) - 1;
+    const int64_t p_first = (int64_t)qoff + r0;
+    const int64_t p_last = (int64_t)qoff + min(r0 + kBr, Tq) - 1;
     int64_t lo_a, hi_a, lo_b, hi_b;
-    visible_range(P, p_first, lo_a, hi_a);
-    visible_range(P, p_last, lo_b, hi_b);
+    visible_range_tk(P, Tk, p_first, lo_a, hi_a);
+    visible_range_tk(P, Tk, p_last, lo_b, hi_b);
     const int64_t klo = lo_a, khi = hi_b > hi_a ? hi_b : hi_a;
     const int t_begin = (int)(klo / kBc);
     const int t_end = khi > klo ? (int)((khi + kBc - 1) / kBc) : t_begin;
@@ -136,14 +151,14 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
         for (int c = 0; c < NC; ++c) acc[a][c] = make_float2(0.f, 0.f);
     }
 
-    stage_rows<DT>(Qs, qh, r0, P.Tq, P.d, P.q_st, P.vec16 != 0);
-    if (t_begin < t_end) stage_rows<DT>(Ks, kh, t_begin * kBc, P.Tk, P.d, P.k_st, P.vec16 != 0);
+    stage_rows<DT>(Qs, qh, r0, Tq, P.d, P.q_st, P.vec16 != 0);
+    if (t_begin < t_end) stage_rows<DT>(Ks, kh, t_begin * kBc, Tk, P.d, P.k_st, P.vec16 != 0);
     cp_async_commit();
 
     for (int t = t_begin; t < t_end; ++t) {
         cp_async_wait<0>();
         __syncthreads();  // Q and K_t landed; every thread finished the previous P.V
-        stage_rows<DT>(Vs, vh, t * kBc, P.Tk, P.d, P.v_st, P.vec16 != 0);
+        stage_rows<DT>(Vs, vh, t * kBc, Tk, P.d, P.v_st, P.vec16 != 0);
         cp_async_commit();
 
         // S = Q K_t^T for rows 4ty+a, keys tx+16b.
@@ -175,21 +190,21 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
         // Scale, additive mask, visibility.  Interior tiles (every key visible
         // to every row of the tile) skip the per-element rule.
         const int j0 = t * kBc;
-        const bool full = (j0 + kBc <= P.Tk) && (!P.causal || (int64_t)(j0 + kBc - 1) <= p_first) &&
+        const bool full = (j0 + kBc <= Tk) && (!P.causal || (int64_t)(j0 + kBc - 1) <= p_first) &&
                           (P.window <= 0 || (int64_t)j0 > p_last - P.window);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int i = r0 + 4 * ty + a;
-            const int64_t p = (int64_t)P.q_offset + i;
+            const int64_t p = (int64_t)qoff + i;
 #pragma unroll
             for (int bb = 0; bb < 4; ++bb) {
                 const int j = j0 + tx + 16 * bb;
                 float v = s[a][bb] * P.scale_log2;
-                if (P.mask != nullptr && i < P.Tq && j < P.Tk)
+                if (!VARLEN && P.mask != nullptr && i < Tq && j < Tk)
                     v = fmaf(__ldg(P.mask + b * P.msb + h * P.msh + (int64_t)i * P.msq + (int64_t)j * P.msk),
                              kLog2e, v);
                 if (!full) {
-                    const bool vis = j < P.Tk && (!P.causal || (int64_t)j <= p) &&
+                    const bool vis = j < Tk && (!P.causal || (int64_t)j <= p) &&
                                      (P.window <= 0 || (int64_t)j > p - P.window);
                     if (!vis) v = -INFINITY;
                 }
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
 
         __syncthreads();  // Pt complete; every thread done with Ks
         if (t + 1 < t_end) {
-            stage_rows<DT>(Ks, kh, (t + 1) * kBc, P.Tk, P.d, P.k_st, P.vec16 != 0);
+            stage_rows<DT>(Ks, kh, (t + 1) * kBc, Tk, P.d, P.k_st, P.vec16 != 0);
             cp_async_commit();
             cp_async_wait<1>();  // V_t landed; K_{t+1} may still be in flight
         } else {
@@ -260,11 +275,11 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
     cp_async_wait<0>();
 
     // Epilogue: o = acc / l; lse = (m + log2 l) ln 2; empty rows give 0 and -inf.
-    float *oh = static_cast<float *>(P.o) + b * P.o_sb + h * P.o_sh;
+    float *oh = static_cast<float *>(P.o) + (VARLEN ? 0 : b * P.o_sb) + h * P.o_sh + qrow * P.o_st;
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
         const int i = r0 + 4 * ty + a;
-        if (i >= P.Tq) continue;
+        if (i >= Tq) continue;
         const float inv = l[a] > 0.f ? 1.f / l[a] : 0.f;
         float *orow = oh + (int64_t)i * P.o_st;
 #pragma unroll
@@ -273,34 +288,40 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
             if (col < P.d) *reinterpret_cast<float2 *>(orow + col) = make_float2(acc[a][c].x * inv, acc[a][c].y * inv);
         }
         if (tx == 0 && P.lse != nullptr)
-            P.lse[(int64_t)bh * P.Tq + i] = l[a] > 0.f ? (m[a] + log2f(l[a])) * kLn2 : -INFINITY;
+            P.lse[VARLEN ? (int64_t)h * P.total_q + qrow + i : (int64_t)bh * P.Tq + i] =
+                l[a] > 0.f ? (m[a] + log2f(l[a])) * kLn2 : -INFINITY;
     }
 }
 
-template <int DT>
+template <int DT, bool VARLEN>
 cudaError_t launch_dt(const Params &P, cudaStream_t stream) {
     constexpr int LD = DT + 4;
     const size_t smem = (size_t)(kBr * LD + 2 * kBc * LD + kBc * kPLd) * sizeof(float);
     static bool configured = false;  // one attribute call per instantiation
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_f32_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_f32_kernel<DT, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int nqt = (P.Tq + kBr - 1) / kBr;
     const unsigned grid = (unsigned)nqt * (unsigned)(P.B * P.Hq);
-    fa_fwd_f32_kernel<DT><<<grid, kThreads, smem, stream>>>(P);
+    fa_fwd_f32_kernel<DT, VARLEN><<<grid, kThreads, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_f32(const Params &P, cudaStream_t stream) {
-    if (P.d <= 64) return launch_dt<64>(P, stream);
-    if (P.d <= 96) return launch_dt<96>(P, stream);
-    if (P.d <= 128) return launch_dt<128>(P, stream);
-    return launch_dt<256>(P, stream);
+template <bool VARLEN>
+cudaError_t launch_f32_v(const Params &P, cudaStream_t stream) {
+    if (P.d <= 64) return launch_dt<64, VARLEN>(P, stream);
+    if (P.d <= 96) return launch_dt<96, VARLEN>(P, stream);
+    if (P.d <= 128) return launch_dt<128, VARLEN>(P, stream);
+    return launch_dt<256, VARLEN>(P, stream);
 }
+
+cudaError_t launch_f32(const Params &P, cudaStream_t stream) { return launch_f32_v<false>(P, stream); }
+
+cudaError_t launch_f32_varlen(const Params &P, cudaStream_t stream) { return launch_f32_v<true>(P, stream); }
 
 }  // namespace fa

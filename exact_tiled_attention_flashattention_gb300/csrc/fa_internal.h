@@ -34,6 +34,11 @@ struct Params {
     const int *seq_lens;
     const int *block_table;
     int max_blocks, page_size, num_pages, max_seq_len;
+    // Variable-length batch: sequence b has rows [cu_q[b], cu_q[b+1]) of q
+    // and o (tensors [total_q, H, d]) and rows [cu_k[b], cu_k[b+1]) of k and
+    // v; its queries are its last positions.  Tq / Tk hold the maxima.
+    const int *cu_q, *cu_k;
+    int total_q, total_k;
 };
 
 // Visible key range [lo, hi) of query position p (absolute) among Tk keys,
@@ -51,5 +56,7 @@ __host__ __device__ inline void visible_range(const Params &P, int64_t p, int64_
 cudaError_t launch_f32(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream);
+cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream);
+cudaError_t launch_f32_varlen(const Params &P, cudaStream_t stream);
 
 }  // namespace fa

@@ -144,6 +144,28 @@ fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, 
                        float scale, int causal, int64_t window, const float *sinks,
                        int dtype, void *stream);
 
+/* A variable-length batch: B sequences packed along the rows of q, o
+ * ([total_q, Hq, d]) and k, v ([total_k, Hkv, d]), element (t, h, x) of q at
+ * q[h*q_sh + t*q_st + x] (likewise k, v, o), d contiguous.  Sequence b has the
+ * rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q and o and [cu_seqlens_k[b],
+ * cu_seqlens_k[b+1]) of k and v (device int32 [B+1], non-decreasing); its
+ * queries are its last positions (q_offset_b = its keys - its queries), which
+ * makes Tq = Tk a causal prefill and fewer queries a chunk or a decode step.
+ * lse is contiguous [Hq, total_q].  max_seqlen_q bounds every sequence's
+ * query count (it sizes the grid; rows past it are not computed);
+ * max_seqlen_k is the analogous bound on keys.  Offsets are clamped into
+ * [0, total], so a malformed table cannot make the kernels reach outside the
+ * tensors.  No additive mask.  Errors as fa_fwd_strided, plus FA_EINVAL for a
+ * NULL cu_seqlens table and FA_EUNSUPPORTED when max_seqlen_q > total_q. */
+fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int64_t B, int64_t Hq, int64_t Hkv, int64_t d,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                        int64_t total_q, int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
+                        int64_t q_sh, int64_t q_st, int64_t k_sh, int64_t k_st,
+                        int64_t v_sh, int64_t v_st, int64_t o_sh, int64_t o_st,
+                        float scale, int causal, int64_t window, const float *sinks,
+                        int dtype, void *stream);
+
 /* Message for the last non-OK status on this thread ("" if none).  The
  * pointer stays valid until the next fa_* call on the same thread. */
 const char *fa_last_error(void);

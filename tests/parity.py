@@ -38,7 +38,7 @@ def gpu_attention(q, k, v, *, scale, q_offset=0, causal=True, window=0, sinks=No
 
 def oracle_attention(q, k, v, *, scale, q_offset=0, causal=True, window=0, sinks=None, mask=None,
                      mask_strides=(0, 0, 0, 0), rows=None):
-    f = lambda t: None if t is None else t.float().numpy()  # exact widening of fp32 / bf16
+    f = lambda t: None if t is None else t.detach().cpu().float().numpy()  # exact widening of fp32 / bf16
     return oracle.attention(f(q), f(k), f(v), scale, q_offset=q_offset, causal=causal, window=window,
                             sinks=f(sinks), mask=None if mask is None else f(mask).reshape(-1),
                             mask_strides=mask_strides, rows=rows)

@@ -193,3 +193,27 @@ def test_paged_rejections(lib, case, kw, want):
                              a["max_seq_len"], p, a["max_blocks"], a["page_size"], a["num_pages"], 0.125, 1, 0, None,
                              a["dtype"], 0, check=False)
     assert st == getattr(fa_mod, want), case
+
+
+# ---------------------------------------------------------------- varlen
+
+@pytest.mark.parametrize("case,kw,want", [
+    ("null cu_seqlens_q", dict(cuq=None), "FA_EINVAL"),
+    ("max_seqlen_q > total_q", dict(max_q=300), "FA_EUNSUPPORTED"),
+    ("overlapping output rows", dict(o_st=32), "FA_EINVAL"),
+    ("Hq % Hkv", dict(Hq=6, Hkv=4), "FA_ESHAPE"),
+    ("bf16 d = 100", dict(d=100), "FA_EUNSUPPORTED"),
+])
+def test_varlen_rejections(lib, case, kw, want):
+    import exact_tiled_attention_flashattention_gb300 as fa_mod
+    a = dict(B=3, Hq=4, Hkv=2, d=64, cuq=1 << 20, total_q=200, total_k=200, max_q=100, max_k=100, o_st=None,
+             dtype=fa_mod.FA_DTYPE_BF16)
+    a.update(kw)
+    p = 1 << 20
+    H, d = a["Hq"], a["d"]
+    qs, ks = (d, H * d), (d, a["Hkv"] * d)
+    os_ = (d, a["o_st"]) if a["o_st"] is not None else qs
+    st = fa_mod.fa_fwd_varlen(p, p, p, p, None, a["B"], a["Hq"], a["Hkv"], d, a["cuq"], p, a["total_q"],
+                              a["total_k"], a["max_q"], a["max_k"], qs, ks, ks, os_, 0.125, 1, 0, None, a["dtype"], 0,
+                              check=False)
+    assert st == getattr(fa_mod, want), case
