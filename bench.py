@@ -324,6 +324,30 @@ def measure_other_paths(fa, dev, flush):
 
     entry("mask_b4h8_t1024_d96", "f32", masked, p.flops())
 
+    # variable-length causal prefill batches, bf16 and fp32
+    for name, w in workloads.VARLEN.items():
+        B, Hq, Hkv, d = w["B"], w["Hq"], w["Hkv"], w["d"]
+        lens = workloads.paged_lengths(w["seed"], B, w["lo"], w["hi"])
+        total = sum(lens)
+        cu = torch.tensor([0] + list(__import__("itertools").accumulate(lens)), dtype=torch.int32, device=dev)
+        flops = sum(workloads.Problem(1, Hq, Hkv, L, L, d).flops() for L in lens)
+        for dt, code in (("bf16", fa.FA_DTYPE_BF16), ("f32", fa.FA_DTYPE_F32)):
+            tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+            g = torch.Generator().manual_seed(w["seed"])
+            qv = torch.randn((total, Hq, d), generator=g).to(tdt).to(dev)
+            kv = torch.randn((total, Hkv, d), generator=g).to(tdt).to(dev)
+            vv = torch.randn((total, Hkv, d), generator=g).to(tdt).to(dev)
+            ov = torch.empty_like(qv)
+            lv = torch.empty((Hq, total), dtype=torch.float32, device=dev)
+
+            def varlen():
+                fa.fa_fwd_varlen(qv, kv, vv, ov, lv, B, Hq, Hkv, d, cu, cu, total, total, max(lens), max(lens),
+                                 (d, Hq * d), (d, Hkv * d), (d, Hkv * d), (d, Hq * d), d ** -0.5, 1, 0, None, code,
+                                 None)
+
+            entry(name, dt, varlen, flops)
+            del qv, kv, vv, ov, lv
+
     # windowed GQA with sinks, 4096 tokens as chunks of 1000 (keys so far per chunk)
     w = workloads.CONFIGS["window128_sinks_gqa32x4_d64_chunked"]
     p = w.problem

@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Problem", "qkv", "sinks", "strided_mask", "CONFIGS", "DECODE", "PAGED", "paged_lengths", "chunk_ranges"]
+__all__ = ["Problem", "qkv", "sinks", "strided_mask", "CONFIGS", "DECODE", "PAGED", "VARLEN", "paged_lengths", "chunk_ranges"]
 
 
 @dataclass(frozen=True)
@@ -166,4 +166,11 @@ def paged_lengths(seed: int, B: int, lo: int, hi: int) -> list:
 PAGED = {
     "paged_b8_gqa16x8_d128_k4k-8k_p64": dict(B=8, Hq=16, Hkv=8, d=128, lo=4096, hi=8192, page_size=64, seed=210),
     "paged_b32_gqa16x8_d128_k4k-8k_p64": dict(B=32, Hq=16, Hkv=8, d=128, lo=4096, hi=8192, page_size=64, seed=211),
+}
+
+
+# A variable-length prefill batch: 8 prompts of the 16q/8kv d=128 model with
+# lengths drawn in [256, 4096] (causal, each its own sequence).
+VARLEN = {
+    "varlen_b8_gqa16x8_d128_256-4096": dict(B=8, Hq=16, Hkv=8, d=128, lo=256, hi=4096, seed=220),
 }
