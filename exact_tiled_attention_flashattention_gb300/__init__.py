@@ -16,10 +16,11 @@ import ctypes
 from pathlib import Path
 
 __all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_DTYPE_F32", "FA_DTYPE_BF16",
+           "FA_DTYPE_F32_TC",
            "FaError", "fa_fwd", "fa_last_error", "fa_version", "attention", "library_path", "load"]
 
 FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA = 0, 1, 2, 3, 4
-FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
+FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F32_TC = 0, 1, 2
 _STATUS = {0: "FA_OK", 1: "FA_EINVAL", 2: "FA_ESHAPE", 3: "FA_EUNSUPPORTED", 4: "FA_ECUDA"}
 
 _LIB_PATH = Path(__file__).resolve().parent / "libfa.so"
@@ -120,17 +121,20 @@ def fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q_strides, k_strides,
 
 
 def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=None, mask=None,
-              mask_strides=(0, 0, 0, 0), with_lse=True, out=None, lse_out=None, stream=None):
+              mask_strides=(0, 0, 0, 0), with_lse=True, out=None, lse_out=None, stream=None, fp32_tc=False):
     """o [B,Hq,Tq,d] (q's dtype) and lse [B,Hq,Tq] (fp32) for CUDA tensors
     q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (fp32 or bf16).  The tensors may be
     strided views (a [B,T,H,d] buffer seen through .transpose(1, 2), say) as
     long as d is contiguous; ``out`` may be strided the same way.  ``mask``
-    is an fp32 CUDA tensor addressed with ``mask_strides`` (elements)."""
+    is an fp32 CUDA tensor addressed with ``mask_strides`` (elements).
+    ``fp32_tc`` selects, for fp32 tensors, the tensor-core path with three
+    TF32 products per matrix product (FA_DTYPE_F32_TC) instead of the SIMT
+    one (FA_DTYPE_F32)."""
     import torch
     B, Hq, Tq, d = q.shape
     Hkv, Tk = k.shape[1], k.shape[2]
     if q.dtype == torch.float32:
-        dt = FA_DTYPE_F32
+        dt = FA_DTYPE_F32_TC if fp32_tc else FA_DTYPE_F32
     elif q.dtype == torch.bfloat16:
         dt = FA_DTYPE_BF16
     else:

@@ -18,7 +18,7 @@ INCLUDE = PKG.parent / "include"
 LIB = PKG / "libfa.so"
 OBJ_DIR = PKG / "_build"
 
-SOURCES = ["fa_api.cu", "fa_fwd_f32.cu", "fa_fwd_bf16.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_f32.cu", "fa_fwd_bf16.cu", "fa_fwd_f32tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -74,6 +74,8 @@ bool layout_ok(int64_t B, int64_t H, int64_t T, int64_t d, int64_t sb, int64_t s
     return true;
 }
 
+bool known_dtype(int dtype) { return dtype == FA_DTYPE_F32 || dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F32_TC; }
+
 // Every stride of a dimension with extent > 1 is a multiple of `m` elements.
 bool strides_multiple(int64_t B, int64_t H, int64_t T, int64_t sb, int64_t sh, int64_t st, int64_t m) {
     return (B <= 1 || sb % m == 0) && (H <= 1 || sh % m == 0) && (T <= 1 || st % m == 0);
@@ -85,7 +87,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
                    const float *sinks, const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq,
                    int64_t mask_sk, int dtype, void *stream) {
     g_last_error[0] = '\0';
-    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return fail(FA_EINVAL, "unknown dtype %d", dtype);
+    if (!known_dtype(dtype)) return fail(FA_EINVAL, "unknown dtype %d", dtype);
     if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || Tk < 0 || d < 0)
         return fail(FA_EINVAL, "negative size (B=%lld Hq=%lld Hkv=%lld Tq=%lld Tk=%lld d=%lld)", (long long)B,
                     (long long)Hq, (long long)Hkv, (long long)Tq, (long long)Tk, (long long)d);
@@ -119,31 +121,39 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
         return fail(FA_EUNSUPPORTED, "fp32 path supports d <= 256 (got %lld)", (long long)d);
     if (dtype == FA_DTYPE_BF16 && (d % 8 != 0 || d > 128))
         return fail(FA_EUNSUPPORTED, "bf16 path supports d a multiple of 8 up to 128 (got %lld)", (long long)d);
+    if (dtype == FA_DTYPE_F32_TC && (d % 4 != 0 || d > 128))
+        return fail(FA_EUNSUPPORTED, "tensor-core fp32 path supports d a multiple of 4 up to 128 (got %lld)",
+                    (long long)d);
     if (Tq >= kMaxLen || Tk >= kMaxLen || q_offset >= kMaxLen)
         return fail(FA_EUNSUPPORTED, "Tq, Tk and q_offset must be below 2^30");
     if (B * Hq >= (int64_t(1) << 24)) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^24");
     if (!aligned16(q) || !aligned16(o) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
         return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
-    // bf16: tensor-map strides are 16-byte multiples below 2^40 bytes.
-    // fp32: rows start on 8-byte boundaries (16-byte copies when all do).
-    const int64_t m = dtype == FA_DTYPE_BF16 ? 8 : 2;
+    // bf16 and fp32 on the tensor cores: tensor-map strides are 16-byte
+    // multiples below 2^40 bytes.  fp32 on the SIMT cores: rows start on
+    // 8-byte boundaries (16-byte copies when all do).
+    const bool tma = dtype != FA_DTYPE_F32;
+    const int64_t m = dtype == FA_DTYPE_BF16 ? 8 : (dtype == FA_DTYPE_F32_TC ? 4 : 2);
     const bool kv = Tk > 0;
     if (!strides_multiple(B, Hq, Tq, qs[0], qs[1], qs[2], m) || !strides_multiple(B, Hq, Tq, os[0], os[1], os[2], m) ||
         (kv && (!strides_multiple(B, Hkv, Tk, ks[0], ks[1], ks[2], m) ||
                 !strides_multiple(B, Hkv, Tk, vs[0], vs[1], vs[2], m))))
         return fail(FA_EUNSUPPORTED, "strides must be multiples of %lld elements for this dtype", (long long)m);
-    if (dtype == FA_DTYPE_BF16) {
-        const int64_t lim = (int64_t(1) << 39) - 1;  // elements: 2^40 bytes
+    if (tma) {
+        const int64_t lim = ((int64_t(1) << 40) / (dtype == FA_DTYPE_BF16 ? 2 : 4)) - 1;  // elements
         const int64_t ext[4][3] = {{B, Hq, Tq}, {B, Hkv, Tk}, {B, Hkv, Tk}, {B, Hq, Tq}};
         const int64_t *all[4] = {qs, ks, vs, os};
         for (int t = 0; t < 4; ++t)
             for (int i = 0; i < 3; ++i) {
                 if (all[t][i] > lim) return fail(FA_EUNSUPPORTED, "a stride reaches 2^40 bytes");
                 if (ext[t][i] > 1 && all[t][i] <= 0 && (t == 0 || t == 3 || kv))
-                    return fail(FA_EUNSUPPORTED, "bf16 strides must be positive (tensor maps)");
+                    return fail(FA_EUNSUPPORTED, "strides must be positive for this dtype (tensor maps)");
             }
         if (B > 0x7fffffff || Hq > 0x7fffffff) return fail(FA_EUNSUPPORTED, "B and H must fit 31 bits");
     }
+    // One CTA per 128-row query tile of each (batch, head).
+    if (dtype == FA_DTYPE_F32_TC && ((Tq + 127) / 128) * B * Hq > 0x7fffffff)
+        return fail(FA_EUNSUPPORTED, "tensor-core fp32 path: B*Hq*ceil(Tq/128) must be below 2^31");
 
     fa::Params P;
     std::memset(&P, 0, sizeof P);
@@ -181,7 +191,9 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     P.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dtype == FA_DTYPE_F32 ? fa::launch_f32(P, s) : fa::launch_bf16(P, s);
+    cudaError_t e = dtype == FA_DTYPE_F32 ? fa::launch_f32(P, s)
+                    : dtype == FA_DTYPE_BF16 ? fa::launch_bf16(P, s)
+                                             : fa::launch_f32_tc(P, s);
     if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
     return FA_OK;
 }
@@ -223,7 +235,7 @@ extern "C" fa_status fa_fwd_paged(const void *q, const void *k_cache, const void
                                   int64_t page_size, int64_t num_pages, float scale, int causal, int64_t window,
                                   const float *sinks, int dtype, void *stream) {
     g_last_error[0] = '\0';
-    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return fail(FA_EINVAL, "unknown dtype %d", dtype);
+    if (!known_dtype(dtype)) return fail(FA_EINVAL, "unknown dtype %d", dtype);
     if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || d < 0 || max_seq_len < 0 || max_blocks < 0 || page_size < 0 ||
         num_pages < 0)
         return fail(FA_EINVAL, "negative size");
@@ -299,7 +311,7 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
                                    int64_t o_st, float scale, int causal, int64_t window, const float *sinks,
                                    int dtype, void *stream) {
     g_last_error[0] = '\0';
-    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return fail(FA_EINVAL, "unknown dtype %d", dtype);
+    if (!known_dtype(dtype)) return fail(FA_EINVAL, "unknown dtype %d", dtype);
     if (B < 0 || Hq < 0 || Hkv < 0 || d < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
         return fail(FA_EINVAL, "negative size");
     if (!std::isfinite(scale)) return fail(FA_EINVAL, "scale is not finite");
@@ -316,6 +328,7 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
     if (B == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query row
     if (!q || !o || !cu_seqlens_q || !cu_seqlens_k) return fail(FA_EINVAL, "q, o or a cu_seqlens table is NULL");
     if (total_k > 0 && (!k || !v)) return fail(FA_EINVAL, "k or v is NULL with total_k > 0");
+    if (dtype == FA_DTYPE_F32_TC) return fail(FA_EUNSUPPORTED, "the varlen path is fp32 (SIMT) or bf16 only");
     if (d == 0 || (d & 1)) return fail(FA_EUNSUPPORTED, "d=%lld: d must be even and positive", (long long)d);
     if (dtype == FA_DTYPE_F32 && d > 256)
         return fail(FA_EUNSUPPORTED, "fp32 path supports d <= 256 (got %lld)", (long long)d);

@@ -54,6 +54,8 @@ __host__ __device__ inline void visible_range(const Params &P, int64_t p, int64_
 }
 
 cudaError_t launch_f32(const Params &P, cudaStream_t stream);
+// fp32 with three TF32 tensor-core products per matrix product.
+cudaError_t launch_f32_tc(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream);

@@ -35,7 +35,13 @@
  * writes fp32 o.  FA_DTYPE_BF16 reads bf16 q/k/v, forms S = Q K^T and O = P V
  * on the tcgen05 tensor cores with fp32 accumulators in tensor memory, keeps
  * the softmax statistics in fp32, rounds P to bf16 for the P.V product, and
- * writes bf16 o (round to nearest even).  lse is fp32 in both.
+ * writes bf16 o (round to nearest even).  FA_DTYPE_F32_TC reads and writes
+ * fp32 like FA_DTYPE_F32 but forms both products on the tcgen05 tensor cores
+ * in TF32 mode, three products per matrix product: each operand x is split
+ * into x_hi (x with its low 13 mantissa bits cleared, the part TF32 keeps)
+ * and x_lo = x - x_hi, and a.b is taken as a_hi b_hi + a_hi b_lo + a_lo b_hi
+ * (the dropped a_lo b_lo term is ~2^-20 relative); fp32 accumulation.  lse is
+ * fp32 in all three.
  *
  * Execution: asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  * stream); results are valid once the stream has synchronised.
@@ -50,7 +56,9 @@
  *   FA_EUNSUPPORTED  d odd or 0 ("Fused attention and softmax": d must be
  *                    even), d > 256 for fp32, bf16 d not a multiple of 8
  *                    or above 128 (rows must be 16-byte multiples for TMA),
- *                    Tq or Tk >= 2^30, pointers not 16-byte aligned.
+ *                    FA_DTYPE_F32_TC d not a multiple of 4 or above 128, or
+ *                    B*Hq*ceil(Tq/128) >= 2^31, Tq or Tk >= 2^30, pointers
+ *                    not 16-byte aligned.
  *   FA_ECUDA         a CUDA error while configuring or launching.
  * B*Hq*Tq == 0 is a no-op returning FA_OK.  Tk == 0 writes o = 0 and
  * lse = -inf (or the sink).  fa_last_error() describes the last non-OK
@@ -75,7 +83,8 @@ typedef enum {
 
 typedef enum {
     FA_DTYPE_F32 = 0,
-    FA_DTYPE_BF16 = 1
+    FA_DTYPE_BF16 = 1,
+    FA_DTYPE_F32_TC = 2
 } fa_dtype;
 
 /* The attention forward described above.  `dtype` is an fa_dtype value;
@@ -102,9 +111,10 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *                    dimensions").
  *   FA_EUNSUPPORTED  bf16: a stride (of a dimension of extent > 1) that is
  *                    not a multiple of 8 elements (16 bytes, a TMA rule) or
- *                    reaches 2^40 bytes; fp32: a stride that is odd.
+ *                    reaches 2^40 bytes; FA_DTYPE_F32_TC: likewise with 4
+ *                    elements; fp32: a stride that is odd.
  * Reading k or v through overlapping rows (a stride of 0 over the batch, say)
- * is allowed for fp32; the bf16 path needs positive strides. */
+ * is allowed for FA_DTYPE_F32; the tensor-core paths need positive strides. */
 fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse,
                          int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d,
                          int64_t q_sb, int64_t q_sh, int64_t q_st,
@@ -156,7 +166,8 @@ fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, 
  * max_seqlen_k is the analogous bound on keys.  Offsets are clamped into
  * [0, total], so a malformed table cannot make the kernels reach outside the
  * tensors.  No additive mask.  Errors as fa_fwd_strided, plus FA_EINVAL for a
- * NULL cu_seqlens table and FA_EUNSUPPORTED when max_seqlen_q > total_q. */
+ * NULL cu_seqlens table and FA_EUNSUPPORTED when max_seqlen_q > total_q or
+ * dtype is FA_DTYPE_F32_TC (fp32 batches run on FA_DTYPE_F32 here). */
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                         int64_t B, int64_t Hq, int64_t Hkv, int64_t d,
                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

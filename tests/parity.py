@@ -24,14 +24,15 @@ TOL = {
 
 
 def gpu_attention(q, k, v, *, scale, q_offset=0, causal=True, window=0, sinks=None, mask=None,
-                  mask_strides=(0, 0, 0, 0)):
-    """CUDA path through fa_fwd; CPU tensors in, CPU tensors out."""
+                  mask_strides=(0, 0, 0, 0), fp32_tc=False):
+    """CUDA path through fa_fwd; CPU tensors in, CPU tensors out.  ``fp32_tc``
+    selects the three-TF32 tensor-core path for fp32 inputs."""
     dev = torch.device("cuda", 0)
     qd, kd, vd = q.to(dev).contiguous(), k.to(dev).contiguous(), v.to(dev).contiguous()
     sd = sinks.to(dev).float().contiguous() if sinks is not None else None
     md = mask.to(dev).float().contiguous() if mask is not None else None
     o, lse = fa.attention(qd, kd, vd, scale=scale, q_offset=q_offset, causal=causal, window=window, sinks=sd,
-                          mask=md, mask_strides=mask_strides)
+                          mask=md, mask_strides=mask_strides, fp32_tc=fp32_tc)
     torch.cuda.synchronize()
     return o.cpu(), lse.cpu()
 

@@ -93,6 +93,9 @@ CASES = [
     ("fp32 d > 256", dict(d=258), fa.FA_EUNSUPPORTED),
     ("bf16 d = 100 (not a multiple of 8)", dict(d=100, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
     ("bf16 d = 136 (> 128)", dict(d=136, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
+    ("fp32 tc d = 30 (not a multiple of 4)", dict(d=30, dtype=fa.FA_DTYPE_F32_TC), fa.FA_EUNSUPPORTED),
+    ("fp32 tc d = 132 (> 128)", dict(d=132, dtype=fa.FA_DTYPE_F32_TC), fa.FA_EUNSUPPORTED),
+    ("unknown dtype 3", dict(dtype=3), fa.FA_EINVAL),
     ("Tk >= 2^30", dict(Tk=1 << 30), fa.FA_EUNSUPPORTED),
     ("Tq >= 2^30", dict(Tq=1 << 30, B=1, Hq=1, Hkv=1, d=2), fa.FA_EUNSUPPORTED),
 ]
@@ -155,6 +158,9 @@ def _strided(fa_mod, **kw):
     ("bf16 stride not a multiple of 8", dict(qs=(2048, 516, 64), os=(4096, 1024, 128)), "FA_EUNSUPPORTED"),
     ("bf16 zero batch stride on k", dict(ks=(0, 512, 64)), "FA_EUNSUPPORTED"),
     ("fp32 odd stride", dict(dtype=1 - 1, qs=(2048, 513, 64), os=(4096, 1024, 128)), "FA_EUNSUPPORTED"),
+    ("fp32 tc stride not a multiple of 4", dict(dtype=2, qs=(2048, 514, 64), os=(4096, 1024, 128)),
+     "FA_EUNSUPPORTED"),
+    ("fp32 tc zero batch stride on k", dict(dtype=2, ks=(0, 512, 64)), "FA_EUNSUPPORTED"),
 ])
 def test_strided_rejections(lib, case, kw, want):
     import exact_tiled_attention_flashattention_gb300 as fa_mod
@@ -175,6 +181,7 @@ def test_strided_bshd_layout_is_valid_up_to_launch(lib):
 
 @pytest.mark.parametrize("case,kw,want", [
     ("fp32 is not paged", dict(dtype=0), "FA_EUNSUPPORTED"),
+    ("fp32 tc is not paged", dict(dtype=2), "FA_EUNSUPPORTED"),
     ("group * Tq > 128", dict(Tq=65), "FA_EUNSUPPORTED"),
     ("page size 48", dict(page_size=48), "FA_EUNSUPPORTED"),
     ("page size 4", dict(page_size=4), "FA_EUNSUPPORTED"),
@@ -203,6 +210,7 @@ def test_paged_rejections(lib, case, kw, want):
     ("overlapping output rows", dict(o_st=32), "FA_EINVAL"),
     ("Hq % Hkv", dict(Hq=6, Hkv=4), "FA_ESHAPE"),
     ("bf16 d = 100", dict(d=100), "FA_EUNSUPPORTED"),
+    ("fp32 tc is not varlen", dict(dtype=2), "FA_EUNSUPPORTED"),
 ])
 def test_varlen_rejections(lib, case, kw, want):
     import exact_tiled_attention_flashattention_gb300 as fa_mod
