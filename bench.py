@@ -278,13 +278,21 @@ def measure_decode(fa, dev, flush, local_rank):
 
 # FP32 SIMT peak of the GB300: 152 SMs x 128 FFMA lanes x 2 FLOP x 2.07 GHz.
 FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# Dense TF32 against dense bf16 on the tensor cores (nominal 1.1 / 2.25 PF/s).
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
-def measure_other_paths(fa, dev, flush):
-    """fp32 28-layer prefill, fp32 masked batch, windowed-sink chunked prompt
-    (bf16 and fp32): device time per configuration from CUDA graphs."""
+def measure_other_paths(fa, dev, flush, peak_bf16):
+    """fp32 28-layer prefill, fp32 long-context prefill, fp32 masked batch,
+    variable-length batches, windowed-sink chunked prompt: device time per
+    configuration from CUDA graphs.  fp32 runs on both fp32 paths: "f32" (SIMT
+    FFMA) and "f32tc" (three TF32 tensor-core products per matrix product;
+    its tensor work is 3x the algorithmic FLOPs, set against the dense TF32
+    peak taken as the measured bf16 peak x 1.1 / 2.25)."""
     import torch
     out = []
+    codes = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC}
+    tf32_peak = peak_bf16 * TF32_OVER_BF16
 
     def entry(name, dtype, fn, flops, reps=10):
         med, _ = time_graph(fn, reps, flush)
@@ -292,6 +300,9 @@ def measure_other_paths(fa, dev, flush):
         e = {"workload": name, "dtype": dtype, "ms": round(med, 4), "tflops": round(tf, 2)}
         if dtype == "f32":
             e["frac_of_fp32_simt_peak"] = round(tf / FP32_SIMT_PEAK_TFLOPS, 4)
+        elif dtype == "f32tc":
+            e["tf32_tensor_tflops"] = round(3 * tf, 2)
+            e["frac_of_tf32_tensor_peak"] = round(3 * tf / tf32_peak, 4)
         out.append(e)
 
     # 28 x 511-token layers in fp32
@@ -301,14 +312,29 @@ def measure_other_paths(fa, dev, flush):
         q, k, v = workloads.qkv(layer, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float32)
         layers.append((q.to(dev), k.to(dev), v.to(dev), torch.empty((p.B, p.Hq, p.Tq, p.d), device=dev),
                        torch.empty((p.B, p.Hq, p.Tq), device=dev)))
+    for dt in ("f32", "f32tc"):
+        def prefill_f32():
+            for q, k, v, o, lse in layers:
+                fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0,
+                          0, 0, codes[dt], None)
 
-    def prefill_f32():
-        for q, k, v, o, lse in layers:
-            fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0, 0,
-                      0, fa.FA_DTYPE_F32, None)
-
-    entry("prefill511_gqa16x8_d128_x28", "f32", prefill_f32, 28 * p.flops(), reps=5)
+        entry("prefill511_gqa16x8_d128_x28", dt, prefill_f32, 28 * p.flops(), reps=5)
     del layers
+
+    # long-context causal prefill in fp32, one call
+    for name in ("longctx2044_gqa16x8_d128", "longctx8192_gqa16x8_d128"):
+        w = workloads.CONFIGS[name]
+        p = w.problem
+        q, k, v = [t.to(dev) for t in workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float32)]
+        o = torch.empty_like(q)
+        lse = torch.empty((p.B, p.Hq, p.Tq), device=dev)
+        for dt in ("f32", "f32tc"):
+            def longctx():
+                fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0,
+                          0, 0, codes[dt], None)
+
+            entry(name, dt, longctx, p.flops(), reps=5)
+        del q, k, v, o, lse
 
     # additive-mask batch, fp32
     w = workloads.CONFIGS["mask_b4h8_t1024_d96"]
@@ -317,12 +343,12 @@ def measure_other_paths(fa, dev, flush):
     m = workloads.strided_mask(w.extra["mask_seed"], p.Tq, p.Tk).to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((p.B, p.Hq, p.Tq), device=dev)
+    for dt in ("f32", "f32tc"):
+        def masked():
+            fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 0, 0, None, m, 0, 0, p.Tk,
+                      1, codes[dt], None)
 
-    def masked():
-        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 0, 0, None, m, 0, 0, p.Tk, 1,
-                  fa.FA_DTYPE_F32, None)
-
-    entry("mask_b4h8_t1024_d96", "f32", masked, p.flops())
+        entry("mask_b4h8_t1024_d96", dt, masked, p.flops())
 
     # variable-length causal prefill batches, bf16 and fp32
     for name, w in workloads.VARLEN.items():
@@ -352,7 +378,8 @@ def measure_other_paths(fa, dev, flush):
     w = workloads.CONFIGS["window128_sinks_gqa32x4_d64_chunked"]
     p = w.problem
     z = workloads.sinks(w.extra["sink_seed"], p.Hq).to(dev)
-    for dt, code in (("bf16", fa.FA_DTYPE_BF16), ("f32", fa.FA_DTYPE_F32)):
+    for dt in ("bf16", "f32", "f32tc"):
+        code = codes[dt]
         tdt = torch.bfloat16 if dt == "bf16" else torch.float32
         q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, tdt)
         chunks, flops = [], 0
@@ -559,7 +586,7 @@ def run_fa(args, rank, world, local_rank):
     others = []
     decode = []
     if not args.skip_long and rank == 0:
-        others = measure_other_paths(fa, dev, flush)
+        others = measure_other_paths(fa, dev, flush, peak_burst)
         decode = measure_decode(fa, dev, flush, local_rank)
 
     cpu = None
@@ -626,13 +653,14 @@ def run_only(args, local_rank):
     w = {**workloads.CONFIGS, **workloads.DECODE}[args.only]
     p = w.problem
     dt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
+    code = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC}[args.dtype]
     q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, dt)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)
     def one_call():
         fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, int(p.causal), p.window,
-                  None, None, 0, 0, 0, 0, fa.FA_DTYPE_BF16 if args.dtype == "bf16" else fa.FA_DTYPE_F32, None)
+                  None, None, 0, 0, 0, 0, code, None)
 
     if args.calls <= 3:
         # few launches (profiling): plain calls, no graph
@@ -663,7 +691,8 @@ def main():
     ap.add_argument("--only", choices=sorted({**workloads.CONFIGS, **workloads.DECODE}),
                     help="profiling driver: one workload only")
     ap.add_argument("--calls", type=int, default=3)
-    ap.add_argument("--dtype", choices=["bf16", "f32"], default="bf16")
+    ap.add_argument("--dtype", choices=["bf16", "f32", "f32tc"], default="bf16",
+                    help="--only: bf16, fp32 on the SIMT cores, or fp32 as three TF32 tensor-core products")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

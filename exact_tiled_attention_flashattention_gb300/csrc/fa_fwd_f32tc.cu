@@ -1,34 +1,42 @@
-// fa_fwd_f32tc.cu -- fp32 exact tiled attention on the tcgen05 tensor cores
-// with three TF32 products per matrix product.
+// fa_fwd_f32tc.cu -- fp32 exact tiled attention on the tcgen05 tensor cores,
+// three products per matrix product.
 //
-// The tensor core's TF32 mode keeps the top 19 bits of each fp32 operand (the
-// low 13 mantissa bits are dropped, not rounded).  With x = x_hi + x_lo,
-// x_hi = x with those bits cleared and x_lo = x - x_hi (exact in fp32),
+// Same method as "FlashAttention forward in C" (sections 2.2-2.4): the online
+// softmax over absolute key tiles, in base 2 with a lazy maximum.  Per key
+// tile t of 128 keys:
 //
-//   a . b  ~  a_hi b_hi + a_hi b_lo + a_lo b_hi        (the a_lo b_lo term,
-//                                                      ~2^-20 relative, dropped)
+//   S_t = Q K_t^T  as three TF32 products.  TF32 keeps the top 19 bits of an
+//                  fp32 operand (the low 13 mantissa bits are dropped); with
+//                  x_hi = x with those bits cleared and x_lo = x - x_hi
+//                  (exact), Q K^T ~ Q_hi K_hi + Q_hi K_lo + Q_lo K_hi, the
+//                  dropped Q_lo K_lo being ~2^-20 relative.  The tensor core
+//                  truncates raw fp32 to x_hi itself, so raw Q and K serve as
+//                  Q_hi and K_hi.  A logit's error stays ~2^-20 of the sum of
+//                  |q_i k_i|, which keeps sharp softmaxes (large logits)
+//                  within the fp32 bound.
+//   P_t = 2^(S_t c - m)  (softmax warps), then split P = P_0 + P_1 with
+//                  P_0 = bf16(P), P_1 = bf16(P - P_0).
+//   O  += P_t V_t  as three bf16 products P_0 V_0 + P_0 V_1 + P_1 V_0 with
+//                  V = V_0 + V_1 split the same way (each product exact in
+//                  fp32, the representation error ~2^-18 of |p v|; P is
+//                  bounded, so this error does not grow with the logits).
 //
-// where the tensor core itself truncates raw fp32 to x_hi, so only the lo
-// parts are materialised.  Same method as "FlashAttention forward in C"
-// (sections 2.2-2.4): the online softmax over absolute key tiles, in base 2
-// with a lazy maximum; per key tile t of 32 keys:
-//
-//   S_t = Q K_t^T       3 x (d / 8) MMAs 128 x 32 x 8, A = Q_hi / Q_lo from
-//                       tensor memory, B = raw K_t / K_t,lo from shared memory
-//   P_t = 2^(S_t c - m) softmax warps; P_t and P_t,lo written to tensor memory
-//   O  += P_t V_t       3 x 4 MMAs 128 x d x 8, A = P_t / P_t,lo (tensor
-//                       memory), B = V_t^T hi / lo (shared memory, K-major)
-//
-// Work unit: one 128-row query tile of one (batch, head); one unit per CTA.
-// Warp roles (448 threads):
+// Work unit: one 128-row query tile of one (batch, head); one unit per CTA,
+// heaviest first.  Warp roles (448 threads):
 //   warps 0-7   softmax, Q split into tensor memory, epilogue: two threads per
-//               row (paired-lane TMEM access), each half of the keys and of O
-//   warps 8-11  splitters: K_lo next to the raw K tile; V transposed into
-//               V^T hi / lo (every B operand is K-major)
-//   warp 12     TMA producer (one lane): raw K and V tiles
+//               row (paired-lane TMEM access), each half of the keys / of O
+//   warps 8-11  splitters: K_lo next to each raw K chunk; V_0 / V_1 in place
+//               of each raw V chunk
+//   warp 12     TMA producer (one lane)
 //   warp 13     MMA issuer (one lane) and tensor-memory owner
-// Tensor memory (512 columns): Q_hi [0,128) Q_lo [128,256) O [256,384)
-// S_b / P_b [384 + 64b, +32) P_b,lo [416 + 64b, +32), b = 0, 1.
+// Tensor memory (512 columns): Q_hi [0, D), Q_lo [D, 2D), O [2D, 3D),
+// S [3D, 3D + 128); P_0 (bf16 pairs) over S's first 64 columns, P_1 over
+// the next 64.  One S buffer: S_{t+1} is issued after P_t V_t.
+// Shared memory: a ring of six 32 KB slots holding, in the order the MMAs
+// consume them, per tile D/32 K chunks (128 keys x 32 columns: raw fp32 in
+// the first 16 KB, K_lo in the second) and 128 / (8192 / D) V chunks
+// (8192 / D keys x D columns: raw fp32 landed by TMA, rewritten in place as
+// the bf16 planes V_0 | V_1).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the device watchdog word, the roles leave their loops and drain
@@ -50,40 +58,34 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;  // query rows per unit
-constexpr int kBN = 32;   // keys per tile
+constexpr int kBN = 128;  // keys per tile
 constexpr int kThreads = 448;
 constexpr int kSoftmaxWarps = 8, kSplitWarps = 4;
 constexpr int kWarpSplit = 8, kWarpTma = 12, kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQh = 0, kColQl = 128, kColO = 256;
-__host__ __device__ constexpr uint32_t col_s(int b) { return 384u + 64u * b; }
-__host__ __device__ constexpr uint32_t col_plo(int b) { return 416u + 64u * b; }
+constexpr int kSlots = 6;
+constexpr uint32_t kSlotBytes = 32768;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kKStages = 3, kVRawStages = 2, kVTStages = 3;
 
 template <int D>
-struct Layout {
-    static constexpr int kBoxes = D / 32;                        // 32-column (128-byte) boxes per K/V tile
-    static constexpr uint32_t kTileBytes = kBN * D * 4;          // raw K or V tile, K_lo tile
-    static constexpr uint32_t kVTBytes = D * kBN * 4;            // V^T tile: D rows x 32 keys
-    static constexpr uint32_t kKRaw = 0;
-    static constexpr uint32_t kKLo = kKRaw + kKStages * kTileBytes;
-    static constexpr uint32_t kVRaw = kKLo + kKStages * kTileBytes;
-    static constexpr uint32_t kVHiT = kVRaw + kVRawStages * kTileBytes;
-    static constexpr uint32_t kVLoT = kVHiT + kVTStages * kVTBytes;
-    static constexpr uint32_t kBar = kVLoT + kVTStages * kVTBytes;
-    static constexpr uint32_t kTotal = kBar + 512;
+struct Cfg {
+    static constexpr int kKChunks = D / 32;     // K chunks per tile (32 columns each)
+    static constexpr int kVK = 8192 / D;        // keys per V chunk (32 KB of fp32)
+    static constexpr int kVChunks = kBN / kVK;  // V chunks per tile
+    static constexpr uint32_t kColQh = 0, kColQl = D, kColO = 2 * D, kColS = 3 * D;
+    static constexpr uint32_t kBar = kSlots * kSlotBytes;
+    static constexpr uint32_t kSmem = kBar + 512;
+    static_assert(kColS + kBN <= kTmemCols, "tensor memory budget");
+    static_assert(kVChunks * kVK == kBN, "V chunks tile the key tile");
 };
 
 struct Barriers {
-    uint64_t k_full[kKStages], k_empty[kKStages], ks_full[kKStages];  // raw K landed / free; K_lo written
-    uint64_t vr_full[kVRawStages], vr_empty[kVRawStages];             // raw V landed / read by the splitters
-    uint64_t vt_full[kVTStages], vt_empty[kVTStages];                 // V^T hi/lo written / free
-    uint64_t q_ready;                                                  // Q_hi / Q_lo in tensor memory
-    uint64_t s_full[2], p_full[2];
-    uint64_t o_done, o_final, drain;
+    uint64_t full[kSlots];   // TMA landed
+    uint64_t ready[kSlots];  // split done (four splitter warps)
+    uint64_t empty[kSlots];  // MMAs done reading
+    uint64_t q_ready, s_full, p_full, o_final, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -91,9 +93,8 @@ struct Barriers {
 struct Pos {
     int st = 0;
     uint32_t ph = 0;
-    template <int N>
     __device__ __forceinline__ void advance() {
-        if (++st == N) {
+        if (++st == kSlots) {
             st = 0;
             ph ^= 1u;
         }
@@ -102,12 +103,15 @@ struct Pos {
 
 // Drop the 13 mantissa bits the TF32 mode ignores.
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
+// The two bf16 halves of a packed pair as fp32 (exact).
+__device__ __forceinline__ float bf16_lo_f(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 
 struct Unit {
     int b, h, g, r0, t_begin, n_tiles;
 };
 
-// Unit = blockIdx.x: heaviest query tiles first.
+// Unit = blockIdx.x: the query tiles with the most keys first.
 __device__ __forceinline__ Unit make_unit(const Params &P) {
     Unit U;
     const int BH = P.B * P.Hq;
@@ -127,168 +131,166 @@ __device__ __forceinline__ Unit make_unit(const Params &P) {
     return U;
 }
 
-// TMA producer: raw K_j and V_j in turn.
+// TMA producer: the raw chunks into the ring in consumption order.
 template <int D>
-__device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUtensorMap &tmV, const Params &P,
-                                              const Unit &U, uint8_t *smem, Barriers &bar) {
-    using L = Layout<D>;
+__device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUtensorMap &tmV, const Unit &U,
+                                              uint8_t *smem, Barriers &bar) {
+    using C = Cfg<D>;
     volatile int *abort = &bar.abort;
-    int k_issued[kKStages] = {}, v_issued[kVRawStages] = {};
-    Pos kp, vp;
+    int uses[kSlots] = {};
+    Pos p;
     bool ok = true;
     for (int j = 0; j < U.n_tiles && ok; ++j) {
         const int key0 = (U.t_begin + j) * kBN;
-        if (k_issued[kp.st] > 0 && !(ok = mbar_wait(&bar.k_empty[kp.st], kp.ph ^ 1u, abort))) break;
-        mbar_arrive_expect_tx(&bar.k_full[kp.st], L::kTileBytes);
+        for (int c = 0; c < C::kKChunks + C::kVChunks && ok; ++c) {
+            if (uses[p.st] > 0 && !(ok = mbar_wait(&bar.empty[p.st], p.ph ^ 1u, abort))) break;
+            uint8_t *slot = smem + p.st * kSlotBytes;
+            if (c < C::kKChunks) {
+                mbar_arrive_expect_tx(&bar.full[p.st], kBN * 128);
+                tma_load_4d(slot, &tmK, &bar.full[p.st], c * 32, key0, U.g, U.b);
+            } else {
+                const int v0 = key0 + (c - C::kKChunks) * C::kVK;
+                mbar_arrive_expect_tx(&bar.full[p.st], kSlotBytes);
 #pragma unroll
-        for (int c = 0; c < L::kBoxes; ++c)
-            tma_load_4d(smem + L::kKRaw + kp.st * L::kTileBytes + c * (kBN * 128), &tmK, &bar.k_full[kp.st], c * 32,
-                        key0, U.g, U.b);
-        ++k_issued[kp.st];
-        kp.template advance<kKStages>();
-        if (v_issued[vp.st] > 0 && !(ok = mbar_wait(&bar.vr_empty[vp.st], vp.ph ^ 1u, abort))) break;
-        mbar_arrive_expect_tx(&bar.vr_full[vp.st], L::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < L::kBoxes; ++c)
-            tma_load_4d(smem + L::kVRaw + vp.st * L::kTileBytes + c * (kBN * 128), &tmV, &bar.vr_full[vp.st], c * 32,
-                        key0, U.g, U.b);
-        ++v_issued[vp.st];
-        vp.template advance<kVRawStages>();
+                for (int bx = 0; bx < D / 32; ++bx)
+                    tma_load_4d(slot + bx * (C::kVK * 128), &tmV, &bar.full[p.st], bx * 32, v0, U.g, U.b);
+            }
+            ++uses[p.st];
+            p.advance();
+        }
     }
     // Every copy issued lands before shared memory goes away.
     int never = 0;
-    for (int s = 0; s < kKStages; ++s)
-        if (k_issued[s] > 0) mbar_wait(&bar.k_full[s], (k_issued[s] - 1) & 1, &never, 200000000ull);
-    for (int s = 0; s < kVRawStages; ++s)
-        if (v_issued[s] > 0) mbar_wait(&bar.vr_full[s], (v_issued[s] - 1) & 1, &never, 200000000ull);
+    for (int s = 0; s < kSlots; ++s)
+        if (uses[s] > 0) mbar_wait(&bar.full[s], (uses[s] - 1) & 1, &never, 200000000ull);
 }
 
-// Splitters (128 threads).  Raw tiles are [D/32 boxes][32 rows][128 bytes]
-// with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)).
-//   K_lo: the same layout, element-wise lo part.
-//   V^T hi / lo: [D rows (columns of V)][32 keys = 128 bytes], swizzled the
-//   same way, so that P V reads V^T as a K-major operand.
+// Splitters (128 threads, t = 0..127).  Raw tiles use the 128-byte swizzle:
+// 16-byte chunk k of a 128-byte row r sits at chunk k ^ (r % 8).
+//   K chunk: raw [128 keys][32 fp32] in bytes [0, 16K); K_lo (same layout)
+//            into [16K, 32K).
+//   V chunk: raw [D/32 boxes][kVK keys][32 fp32] rewritten as V_0 [16K]
+//            then V_1 [16K], each [D/64 boxes][kVK keys][64 bf16].  Box q of
+//            plane p covers the bytes of raw box 2p + q (D = 128) or p
+//            (D = 64), row for row, so row r of the planes only overwrites
+//            raw row r; each warp converts whole rows, loading all of its
+//            rows before storing any.
 template <int D>
-__device__ __forceinline__ void split_role(const Params &P, const Unit &U, uint8_t *smem, Barriers &bar, int t,
-                                           int lane) {
-    using L = Layout<D>;
+__device__ __forceinline__ void split_role(const Unit &U, uint8_t *smem, Barriers &bar, int t, int lane) {
+    using C = Cfg<D>;
+    constexpr int kUnitsPerRow = D / 4;                           // 16-byte units of a raw V row
+    constexpr int kUnitsPerThread = C::kVK * kUnitsPerRow / 128;  // 16
+    constexpr int kBatch = 8;
+    static_assert(kUnitsPerThread % kBatch == 0, "whole batches");
+    static_assert(32 % kUnitsPerRow == 0 || kUnitsPerRow % 32 == 0, "a warp instruction covers whole rows");
     volatile int *abort = &bar.abort;
-    Pos kp, vrp, vtp;
+    const int sw = t >> 5;
+    Pos p;
     bool ok = true;
     for (int j = 0; j < U.n_tiles && ok; ++j) {
-        // K_lo
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.k_full[kp.st], kp.ph, abort)))) break;
-        {
-            const float4 *src = reinterpret_cast<const float4 *>(smem + L::kKRaw + kp.st * L::kTileBytes);
-            float4 *dst = reinterpret_cast<float4 *>(smem + L::kKLo + kp.st * L::kTileBytes);
+        for (int c = 0; c < C::kKChunks + C::kVChunks; ++c) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[p.st], p.ph, abort)))) break;
+            uint8_t *slot = smem + p.st * kSlotBytes;
+            if (c < C::kKChunks) {
+                const float4 *src = reinterpret_cast<const float4 *>(slot);
+                float4 *dst = reinterpret_cast<float4 *>(slot + kBN * 128);
 #pragma unroll
-            for (int e = t; e < (int)(L::kTileBytes / 16); e += kSplitWarps * 32) {
-                const float4 x = src[e];
-                dst[e] = make_float4(x.x - tf32_hi(x.x), x.y - tf32_hi(x.y), x.z - tf32_hi(x.z), x.w - tf32_hi(x.w));
+                for (int e = 0; e < kBN * 128 / 16 / 128; ++e) {
+                    const float4 x = src[t + 128 * e];
+                    dst[t + 128 * e] =
+                        make_float4(x.x - tf32_hi(x.x), x.y - tf32_hi(x.y), x.z - tf32_hi(x.z), x.w - tf32_hi(x.w));
+                }
+            } else {
+                // Batches of kBatch warp instructions, each a set of whole
+                // rows: read, __syncwarp, rewrite.
+#pragma unroll
+                for (int i0 = 0; i0 < kUnitsPerThread; i0 += kBatch) {
+                    float4 x[kBatch];
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int u = ((i0 + i) * kSplitWarps + sw) * 32 + lane;
+                        const int r = u / kUnitsPerRow, c4 = u % kUnitsPerRow;
+                        x[i] = *reinterpret_cast<const float4 *>(slot + (c4 >> 3) * (C::kVK * 128) + r * 128 +
+                                                                 (((c4 & 7) ^ (r & 7)) << 4));
+                    }
+                    __syncwarp();  // the batch's rows read before any is rewritten
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int u = ((i0 + i) * kSplitWarps + sw) * 32 + lane;
+                        const int r = u / kUnitsPerRow, c4 = u % kUnitsPerRow;
+                        const uint32_t h0 = cvt_bf16x2(x[i].x, x[i].y), h1 = cvt_bf16x2(x[i].z, x[i].w);
+                        const uint32_t l0 = cvt_bf16x2(x[i].x - bf16_lo_f(h0), x[i].y - bf16_hi_f(h0));
+                        const uint32_t l1 = cvt_bf16x2(x[i].z - bf16_lo_f(h1), x[i].w - bf16_hi_f(h1));
+                        // bf16 column 4 c4: box c4 / 16, byte 8 (c4 % 16) of the box's 128-byte row
+                        const uint32_t off = (c4 >> 4) * (C::kVK * 128) + r * 128 +
+                                             ((((c4 & 15) >> 1) ^ (r & 7)) << 4) + ((c4 & 1) << 3);
+                        *reinterpret_cast<uint2 *>(slot + off) = make_uint2(h0, h1);
+                        *reinterpret_cast<uint2 *>(slot + 16384 + off) = make_uint2(l0, l1);
+                    }
+                    __syncwarp();
+                }
             }
+            fence_proxy_async_smem();  // the MMAs read the split parts through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.ready[p.st]);
+            p.advance();
         }
-        fence_proxy_async_smem();  // the MMAs read K_lo through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.ks_full[kp.st]);
-        kp.template advance<kKStages>();
-
-        // V^T hi / lo: thread t owns column x = t of V (row x of V^T)
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.vr_full[vrp.st], vrp.ph, abort)))) break;
-        if (j >= kVTStages && !(ok = __all_sync(0xffffffffu, mbar_wait(&bar.vt_empty[vtp.st], vtp.ph ^ 1u, abort))))
-            break;
-        if (t < D) {
-            const int x = t;
-            const uint8_t *raw = smem + L::kVRaw + vrp.st * L::kTileBytes + (x / 32) * (kBN * 128);
-            const int cx = (x % 32) / 4, wx = (x % 4) * 4;
-            float v[kBN];
-#pragma unroll
-            for (int r = 0; r < kBN; ++r) v[r] = *reinterpret_cast<const float *>(raw + r * 128 + ((cx ^ (r & 7)) * 16) + wx);
-            uint8_t *hi = smem + L::kVHiT + vtp.st * L::kVTBytes + x * 128;
-            uint8_t *lo = smem + L::kVLoT + vtp.st * L::kVTBytes + x * 128;
-#pragma unroll
-            for (int c = 0; c < kBN / 4; ++c) {
-                const float4 a = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                const float4 ah = make_float4(tf32_hi(a.x), tf32_hi(a.y), tf32_hi(a.z), tf32_hi(a.w));
-                *reinterpret_cast<float4 *>(hi + ((c ^ (x & 7)) * 16)) = ah;
-                *reinterpret_cast<float4 *>(lo + ((c ^ (x & 7)) * 16)) =
-                    make_float4(a.x - ah.x, a.y - ah.y, a.z - ah.z, a.w - ah.w);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.vr_empty[vrp.st]);  // raw V read
-        vrp.template advance<kVRawStages>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.vt_full[vtp.st]);
-        vtp.template advance<kVTStages>();
     }
 }
 
-// Shared-memory descriptor (128-byte swizzle, K-major, 8-row atoms of 1 KB).
-__device__ __forceinline__ uint64_t desc(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
+// K-major operand descriptor, 128-byte swizzle, 8-row atoms of 1 KB.
+__device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
 
-// S_b = Q K^T: per 8-column step of d, Q_hi K + Q_hi K_lo + Q_lo K.
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tbase, int b, uint32_t kraw, uint32_t klo) {
-    constexpr uint32_t id = idesc_tf32_f32(kBM, kBN);
-#pragma unroll
-    for (int kk = 0; kk < D / 8; ++kk) {
-        const uint32_t off = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;  // box, then 32 bytes per 8 fp32
-        const uint64_t dk = desc(kraw + off), dl = desc(klo + off);
-        mma_ts_tf32(tbase + col_s(b), tbase + kColQh + kk * 8, (uint32_t)dk, (uint32_t)(dk >> 32), id, kk > 0);
-        mma_ts_tf32(tbase + col_s(b), tbase + kColQh + kk * 8, (uint32_t)dl, (uint32_t)(dl >> 32), id, 1u);
-        mma_ts_tf32(tbase + col_s(b), tbase + kColQl + kk * 8, (uint32_t)dk, (uint32_t)(dk >> 32), id, 1u);
-    }
-}
-
-// O += P_b V: per 8 keys, P V_hi^T + P V_lo^T + P_lo V_hi^T.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tbase, int b, uint32_t vhi, uint32_t vlo, uint32_t accumulate) {
-    constexpr uint32_t id = idesc_tf32_f32(kBM, D);
-#pragma unroll
-    for (int kk = 0; kk < kBN / 8; ++kk) {
-        const uint64_t dh = desc(vhi + kk * 32), dl = desc(vlo + kk * 32);
-        mma_ts_tf32(tbase + kColO, tbase + col_s(b) + kk * 8, (uint32_t)dh, (uint32_t)(dh >> 32), id,
-                    (kk > 0 || accumulate) ? 1u : 0u);
-        mma_ts_tf32(tbase + kColO, tbase + col_s(b) + kk * 8, (uint32_t)dl, (uint32_t)(dl >> 32), id, 1u);
-        mma_ts_tf32(tbase + kColO, tbase + col_plo(b) + kk * 8, (uint32_t)dh, (uint32_t)(dh >> 32), id, 1u);
-    }
-}
-
-// MMA issuer: S_0, S_1 up front; per tile j: wait P_j, O += P_j V_j, then
-// S_{j+2} into the buffer P_j came from (tcgen05 MMAs of one thread execute
-// in order).
+// MMA issuer: per tile, S = Q K^T chunk by chunk, then (once P is written)
+// O += P V chunk by chunk; each chunk's slot is released by a commit.
 template <int D>
 __device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers &bar, uint32_t tbase) {
-    using L = Layout<D>;
+    using C = Cfg<D>;
+    constexpr uint32_t idQK = idesc_tf32_f32(kBM, kBN);
+    constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, 0, 1);
     volatile int *abort = &bar.abort;
     const int n = U.n_tiles;
     bool ok = true;
-    Pos kp, vtp;
-    auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(&bar.ks_full[kp.st], kp.ph, abort)) return false;  // raw K and K_lo
-        tc_fence_after();
-        issue_qk<D>(tbase, j & 1, smem_u32(smem + L::kKRaw + kp.st * L::kTileBytes),
-                    smem_u32(smem + L::kKLo + kp.st * L::kTileBytes));
-        mma_commit(&bar.s_full[j & 1]);
-        mma_commit(&bar.k_empty[kp.st]);
-        kp.template advance<kKStages>();
-        return true;
-    };
+    Pos p;
     if (n > 0) {
         ok = mbar_wait(&bar.q_ready, 0, abort);
-        if (ok) ok = issue_s(0);
-        if (ok && n > 1) ok = issue_s(1);
         for (int j = 0; j < n && ok; ++j) {
-            if (!(ok = mbar_wait(&bar.p_full[j & 1], (j >> 1) & 1, abort))) break;
-            if (!(ok = mbar_wait(&bar.vt_full[vtp.st], vtp.ph, abort))) break;
+            for (int c = 0; c < C::kKChunks; ++c) {
+                if (!(ok = mbar_wait(&bar.ready[p.st], p.ph, abort))) break;
+                tc_fence_after();
+                const uint32_t s = smem_u32(smem + p.st * kSlotBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t dr = desc_k(s + kk * 32), dl = desc_k(s + kBN * 128 + kk * 32);
+                    const uint32_t aq = tbase + C::kColQh + c * 32 + kk * 8;
+                    const uint32_t al = tbase + C::kColQl + c * 32 + kk * 8;
+                    mma_ts_tf32(tbase + C::kColS, aq, (uint32_t)dr, (uint32_t)(dr >> 32), idQK, (c | kk) != 0);
+                    mma_ts_tf32(tbase + C::kColS, aq, (uint32_t)dl, (uint32_t)(dl >> 32), idQK, 1u);
+                    mma_ts_tf32(tbase + C::kColS, al, (uint32_t)dr, (uint32_t)(dr >> 32), idQK, 1u);
+                }
+                mma_commit(&bar.empty[p.st]);
+                p.advance();
+            }
+            if (!ok) break;
+            mma_commit(&bar.s_full);
+            if (!(ok = mbar_wait(&bar.p_full, j & 1, abort))) break;
             tc_fence_after();
-            issue_pv<D>(tbase, j & 1, smem_u32(smem + L::kVHiT + vtp.st * L::kVTBytes),
-                        smem_u32(smem + L::kVLoT + vtp.st * L::kVTBytes), j > 0 ? 1u : 0u);
-            mma_commit(&bar.o_done);
-            mma_commit(&bar.vt_empty[vtp.st]);
-            vtp.template advance<kVTStages>();
-            if (j + 2 < n && !(ok = issue_s(j + 2))) break;
+            for (int c = 0; c < C::kVChunks; ++c) {
+                if (!(ok = mbar_wait(&bar.ready[p.st], p.ph, abort))) break;
+                tc_fence_after();
+                const uint32_t s = smem_u32(smem + p.st * kSlotBytes);
+#pragma unroll
+                for (int kk = 0; kk < C::kVK / 16; ++kk) {
+                    const uint64_t d0 = smem_desc_sw128(s + kk * 2048, C::kVK * 128, 1024);
+                    const uint64_t d1 = smem_desc_sw128(s + 16384 + kk * 2048, C::kVK * 128, 1024);
+                    const uint32_t a0 = tbase + C::kColS + (c * (C::kVK / 16) + kk) * 8;  // P_0: 16 keys
+                    mma_ts(tbase + C::kColO, a0, d0, idPV, (j | c | kk) != 0);
+                    mma_ts(tbase + C::kColO, a0, d1, idPV, 1u);
+                    mma_ts(tbase + C::kColO, a0 + 64, d0, idPV, 1u);  // P_1
+                }
+                mma_commit(&bar.empty[p.st]);
+                p.advance();
+            }
         }
         mma_commit(&bar.o_final);
     }
@@ -297,13 +299,13 @@ __device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers 
     mbar_wait(&bar.drain, 0, &never, 200000000ull);
 }
 
-// Softmax warps 0-7: Q split into tensor memory, the online softmax, the
-// epilogue.  Warp w covers TMEM lanes 32 (w % 4) + 16 (w / 4) .. +16; lanes
-// l and l + 16 share a row (keys [0, 16) and [16, 32) of a tile; columns
-// [0, D/2) and [D/2, D) of Q and O).
+// Softmax warps 0-7.  Warp w covers TMEM lanes 32 (w % 4) + 16 (w / 4) .. +16;
+// lanes l and l + 16 share a row: keys [0, 64) / [64, 128) of a tile,
+// columns [0, D/2) / [D/2, D) of Q and O.
 template <int D>
 __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Barriers &bar, uint32_t tbase, int warp,
                                              int lane) {
+    using C = Cfg<D>;
     constexpr int kHK = kBN / 2;  // keys per thread
     constexpr int kHD = D / 2;    // columns of Q / O per thread
     volatile int *abort = &bar.abort;
@@ -324,18 +326,20 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
         for (int cc = 0; cc < kHD; cc += 32) {
             uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
+            for (int e = 0; e < 32; e += 4) {
                 const int col = half * kHD + cc + e;
-                float2 x = make_float2(0.f, 0.f);
-                if (live && col < P.d) x = *reinterpret_cast<const float2 *>(qrow + col);
-                const float hx = tf32_hi(x.x), hy = tf32_hi(x.y);
-                hi[e] = __float_as_uint(hx);
-                hi[e + 1] = __float_as_uint(hy);
-                lo[e] = __float_as_uint(x.x - hx);
-                lo[e + 1] = __float_as_uint(x.y - hy);
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (live && col < P.d) x = __ldg(reinterpret_cast<const float4 *>(qrow + col));
+                const float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float hv = tf32_hi(v[k]);
+                    hi[e + k] = __float_as_uint(hv);
+                    lo[e + k] = __float_as_uint(v[k] - hv);
+                }
             }
-            tmem_store_pair32<kHD>(tbase + lane_off + kColQh + cc, hi);
-            tmem_store_pair32<kHD>(tbase + lane_off + kColQl + cc, lo);
+            tmem_store_pair32<kHD>(tbase + lane_off + C::kColQh + cc, hi);
+            tmem_store_pair32<kHD>(tbase + lane_off + C::kColQl + cc, lo);
         }
         tc_fence_before();
         __syncwarp();
@@ -366,13 +370,14 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
         ti_lo = (int)((lo_key + kBN - 1) / kBN - U.t_begin);
         ti_hi = (int)(hi_key / kBN - U.t_begin);
     }
+    const uint32_t s_addr = tbase + lane_off + C::kColS;
+    const uint32_t o_addr = tbase + lane_off + C::kColO;
 
     for (int j = 0; j < n; ++j) {
-        const int b = j & 1;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], (j >> 1) & 1, abort)))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1, abort)))) break;
         tc_fence_after();
         uint32_t sr[kHK];
-        tmem_load_pair16<kHK>(tbase + lane_off + col_s(b), sr);
+        tmem_load_pair64<kHK>(s_addr, sr);
         float *s = reinterpret_cast<float *>(sr);
         float cs = c;
         if (j < ti_lo || j >= ti_hi) {
@@ -395,46 +400,60 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
                 for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
             }
         }
-        float bm = s[0];
+        float bm;
+        {
+            float mx[8];
 #pragma unroll
-        for (int e = 1; e < kHK; ++e) bm = fmaxf(bm, s[e]);
-        bm *= cs;
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+            for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);
+#pragma unroll
+            for (int e = 24; e < 56; e += 16)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[56 + c8]);
+            bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        }
         float alpha = 1.f;
         if (bm > m + kRescaleThreshold) {
             alpha = ex2_approx(m - bm);
             m = bm;
         }
         const float shift = (m == -INFINITY) ? 0.f : m;
+        // S_j was issued after P_{j-1} V_{j-1}, so O is complete here.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-            // O must hold P_{j-1} V_{j-1} before it is rescaled.
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_done, (uint32_t)((j - 1) & 1), abort)))) break;
-            tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < kHD; cc += 32) {
-                uint32_t orr[32];
-                tmem_load_pair32<kHD>(tbase + lane_off + kColO + cc, orr);
+            for (int cc = 0; cc < kHD; cc += 16) {
+                uint32_t orr[16];
+                tmem_load_pair16<kHD>(o_addr + cc, orr);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                tmem_store_pair32<kHD>(tbase + lane_off + kColO + cc, orr);
+                for (int e = 0; e < 16; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_store_pair16<kHD>(o_addr + cc, orr);
             }
         }
-        // p in fp32: P = p (the tensor core drops its low bits), P_lo = p - P_hi.
-        uint32_t ph[kHK], pl[kHK];
-        float sum = 0.f;
+        // p = 2^(s cs - shift) in fp32; P_0 = bf16(p), P_1 = bf16(p - P_0),
+        // 32 keys at a time (every S value of the row is already loaded).
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < kHK; ++e) {
-            const float pe = ex2_approx(fmaf(s[e], cs, -shift));
-            sum += pe;
-            ph[e] = __float_as_uint(pe);
-            pl[e] = __float_as_uint(pe - tf32_hi(pe));
+        for (int hc = 0; hc < kHK; hc += 32) {
+            uint32_t p0[16], p1[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                const float pa = ex2_approx(fmaf(s[hc + e], cs, -shift));
+                const float pb = ex2_approx(fmaf(s[hc + e + 1], cs, -shift));
+                acc0 += pa;
+                acc1 += pb;
+                const uint32_t h = cvt_bf16x2(pa, pb);
+                p0[e / 2] = h;
+                p1[e / 2] = cvt_bf16x2(pa - bf16_lo_f(h), pb - bf16_hi_f(h));
+            }
+            tmem_store_pair16<kHK / 2>(s_addr + hc / 2, p0);
+            tmem_store_pair16<kHK / 2>(s_addr + 64 + hc / 2, p1);
         }
-        tmem_store_pair16<kHK>(tbase + lane_off + col_s(b), ph);
-        tmem_store_pair16<kHK>(tbase + lane_off + col_plo(b), pl);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.p_full[b]);
-        l = fmaf(alpha, l, sum);
+        if (lane == 0) mbar_arrive(&bar.p_full);
+        l = fmaf(alpha, l, acc0 + acc1);
     }
     if (!ok) return;
 
@@ -450,18 +469,19 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
     for (int cc = 0; cc < kHD; cc += 32) {
         uint32_t ov[32];
         if (n > 0) {
-            tmem_load_pair32<kHD>(tbase + lane_off + kColO + cc, ov);
+            tmem_load_pair32<kHD>(o_addr + cc, ov);
         } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = 0u;
         }
         if (live) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
+            for (int e = 0; e < 32; e += 4) {
                 const int col = half * kHD + cc + e;
                 if (col < P.d)
-                    *reinterpret_cast<float2 *>(orow + col) =
-                        make_float2(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv);
+                    *reinterpret_cast<float4 *>(orow + col) =
+                        make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                    __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
             }
         }
     }
@@ -474,31 +494,20 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_f32tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const Params P) {
-    using L = Layout<D>;
+    using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Barriers &bar = *reinterpret_cast<Barriers *>(smem + L::kBar);
+    Barriers &bar = *reinterpret_cast<Barriers *>(smem + C::kBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&bar.k_full[s], 1);
-            mbar_init(&bar.k_empty[s], 1);
-            mbar_init(&bar.ks_full[s], kSplitWarps);
-        }
-        for (int s = 0; s < kVRawStages; ++s) {
-            mbar_init(&bar.vr_full[s], 1);
-            mbar_init(&bar.vr_empty[s], kSplitWarps);
-        }
-        for (int s = 0; s < kVTStages; ++s) {
-            mbar_init(&bar.vt_full[s], kSplitWarps);
-            mbar_init(&bar.vt_empty[s], 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&bar.full[s], 1);
+            mbar_init(&bar.ready[s], kSplitWarps);
+            mbar_init(&bar.empty[s], 1);
         }
         mbar_init(&bar.q_ready, kSoftmaxWarps);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar.s_full[s], 1);
-            mbar_init(&bar.p_full[s], kSoftmaxWarps);
-        }
-        mbar_init(&bar.o_done, 1);
+        mbar_init(&bar.s_full, 1);
+        mbar_init(&bar.p_full, kSoftmaxWarps);
         mbar_init(&bar.o_final, 1);
         mbar_init(&bar.drain, 1);
         bar.abort = 0;
@@ -521,11 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Unit U = make_unit(P);
 
     if (warp == kWarpTma) {
-        if (lane == 0) producer_role<D>(tmK, tmV, P, U, smem, bar);
+        if (lane == 0) producer_role<D>(tmK, tmV, U, smem, bar);
     } else if (warp == kWarpMma) {
         if (lane == 0) mma_role<D>(U, smem, bar, tbase);
     } else if (warp >= kWarpSplit) {
-        split_role<D>(P, U, smem, bar, threadIdx.x - kWarpSplit * 32, lane);
+        split_role<D>(U, smem, bar, threadIdx.x - kWarpSplit * 32, lane);
     } else {
         softmax_role<D>(P, U, bar, tbase, warp, lane);
     }
@@ -560,13 +569,13 @@ EncodeTiledFn encode_fn32() {
 }
 
 // [B, H, T, d] fp32 with element strides as the 4-D map (d, T, H, B); boxes of
-// 32 columns (128 bytes) x 32 rows, 128-byte swizzle; rows and columns past
-// the tensor read as zero.  Extent-1 dimensions get a packed stride.
+// 32 columns (128 bytes) x `rows` rows, 128-byte swizzle; rows and columns
+// past the tensor read as zero.  Extent-1 dimensions get a packed stride.
 bool make_map32(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int T, int H, int B, int64_t st,
-                int64_t sh, int64_t sb) {
+                int64_t sh, int64_t sb, int rows) {
     const int64_t dims[4] = {d, T, H, B}, strides[4] = {1, st, sh, sb};
     cuuint64_t gd[4], gs[3];
-    cuuint32_t bx[4] = {32, (cuuint32_t)kBN, 1, 1}, es[4] = {1, 1, 1, 1};
+    cuuint32_t bx[4] = {32, (cuuint32_t)rows, 1, 1}, es[4] = {1, 1, 1, 1};
     uint64_t packed = (uint64_t)d * 4;
     for (int i = 0; i < 4; ++i) {
         gd[i] = (cuuint64_t)dims[i];
@@ -582,16 +591,17 @@ bool make_map32(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, in
 
 template <int D>
 cudaError_t launch_tc(const Params &P, cudaStream_t stream) {
+    using C = Cfg<D>;
     EncodeTiledFn enc = encode_fn32();
     if (enc == nullptr) return cudaErrorNotSupported;
     CUtensorMap tk, tv;
     const bool kv = P.Tk > 0;
     if (!make_map32(enc, &tk, kv ? P.k : P.q, P.d, kv ? P.Tk : 1, kv ? P.Hkv : 1, kv ? P.B : 1, kv ? P.k_st : P.q_st,
-                    kv ? P.k_sh : P.q_sh, kv ? P.k_sb : P.q_sb) ||
+                    kv ? P.k_sh : P.q_sh, kv ? P.k_sb : P.q_sb, kBN) ||
         !make_map32(enc, &tv, kv ? P.v : P.q, P.d, kv ? P.Tk : 1, kv ? P.Hkv : 1, kv ? P.B : 1, kv ? P.v_st : P.q_st,
-                    kv ? P.v_sh : P.q_sh, kv ? P.v_sb : P.q_sb))
+                    kv ? P.v_sh : P.q_sh, kv ? P.v_sb : P.q_sb, C::kVK))
         return cudaErrorInvalidValue;
-    constexpr size_t kSmem = Layout<D>::kTotal + 1024;
+    constexpr size_t kSmem = C::kSmem + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static bool configured = false;
     if (!configured) {

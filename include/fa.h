@@ -36,12 +36,13 @@
  * on the tcgen05 tensor cores with fp32 accumulators in tensor memory, keeps
  * the softmax statistics in fp32, rounds P to bf16 for the P.V product, and
  * writes bf16 o (round to nearest even).  FA_DTYPE_F32_TC reads and writes
- * fp32 like FA_DTYPE_F32 but forms both products on the tcgen05 tensor cores
- * in TF32 mode, three products per matrix product: each operand x is split
- * into x_hi (x with its low 13 mantissa bits cleared, the part TF32 keeps)
- * and x_lo = x - x_hi, and a.b is taken as a_hi b_hi + a_hi b_lo + a_lo b_hi
- * (the dropped a_lo b_lo term is ~2^-20 relative); fp32 accumulation.  lse is
- * fp32 in all three.
+ * fp32 like FA_DTYPE_F32 but forms both products on the tcgen05 tensor cores,
+ * three products per matrix product with fp32 accumulation: S = Q K^T in TF32
+ * mode as Q_hi K_hi + Q_hi K_lo + Q_lo K_hi, where x_hi is x with its low 13
+ * mantissa bits cleared (the part TF32 keeps) and x_lo = x - x_hi (a logit's
+ * error ~2^-20 of sum |q_i k_i|); O = P V in bf16 as P_0 V_0 + P_0 V_1 +
+ * P_1 V_0 with x_0 = bf16(x), x_1 = bf16(x - x_0) (~2^-17 of sum |p_j v_j|).
+ * lse is fp32 in all three.
  *
  * Execution: asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  * stream); results are valid once the stream has synchronised.
