@@ -23,20 +23,24 @@
 //
 // Work unit: one 128-row query tile of one (batch, head); one unit per CTA,
 // heaviest first.  Warp roles (448 threads):
-//   warps 0-7   softmax, Q split into tensor memory, epilogue: two threads per
-//               row (paired-lane TMEM access), each half of the keys / of O
+//   warps 0-7   softmax, Q split (Q_hi into tensor memory, Q_lo into shared
+//               memory), epilogue: two threads per row (paired-lane TMEM
+//               access), each half of the keys / of O
 //   warps 8-11  splitters: K_lo next to each raw K chunk; V_0 / V_1 in place
 //               of each raw V chunk
 //   warp 12     TMA producer (one lane)
 //   warp 13     MMA issuer (one lane) and tensor-memory owner
-// Tensor memory (512 columns): Q_hi [0, D), Q_lo [D, 2D), O [2D, 3D),
-// S [3D, 3D + 128); P_0 (bf16 pairs) over S's first 64 columns, P_1 over
-// the next 64.  One S buffer: S_{t+1} is issued after P_t V_t.
-// Shared memory: a ring of six 32 KB slots holding, in the order the MMAs
-// consume them, per tile D/32 K chunks (128 keys x 32 columns: raw fp32 in
-// the first 16 KB, K_lo in the second) and 128 / (8192 / D) V chunks
+// Tensor memory (512 columns): Q_hi [0, D), O [D, 2D), two S buffers of 128
+// columns from 2D; P_0 (bf16 pairs) over a buffer's first 64 columns, P_1
+// over the next 64.  With two buffers the softmax of tile t runs while the
+// tensor core forms S_{t+1}.
+// Shared memory: Q_lo ([D/32 boxes][128 rows][32 fp32], the A operand of the
+// Q_lo K_hi product), then a ring of 32 KB slots holding, in the order the
+// MMAs consume them, per tile D/32 K chunks (128 keys x 32 columns: raw fp32
+// in the first 16 KB, K_lo in the second) and 128 / (8192 / D) V chunks
 // (8192 / D keys x D columns: raw fp32 landed by TMA, rewritten in place as
-// the bf16 planes V_0 | V_1).
+// the bf16 planes V_0 | V_1).  The MMAs consume K_0, K_1, then V_t, K_{t+2}
+// for t = 0, 1, ...
 //
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the device watchdog word, the roles leave their loops and drain
@@ -63,7 +67,7 @@ constexpr int kThreads = 448;
 constexpr int kSoftmaxWarps = 8, kSplitWarps = 4;
 constexpr int kWarpSplit = 8, kWarpTma = 12, kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSlots = 6;
+constexpr int kMaxSlots = 6;
 constexpr uint32_t kSlotBytes = 32768;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -74,32 +78,60 @@ struct Cfg {
     static constexpr int kKChunks = D / 32;     // K chunks per tile (32 columns each)
     static constexpr int kVK = 8192 / D;        // keys per V chunk (32 KB of fp32)
     static constexpr int kVChunks = kBN / kVK;  // V chunks per tile
-    static constexpr uint32_t kColQh = 0, kColQl = D, kColO = 2 * D, kColS = 3 * D;
-    static constexpr uint32_t kBar = kSlots * kSlotBytes;
+    static constexpr int kSlots = D == 128 ? 4 : 6;
+    static constexpr uint32_t kColQh = 0, kColO = D, kColS0 = 2 * D;
+    static constexpr uint32_t kQlo = 0;                    // Q_lo: 128 rows x D fp32
+    static constexpr uint32_t kRing = kBM * D * 4;         // ring slots
+    static constexpr uint32_t kBar = kRing + kSlots * kSlotBytes;
     static constexpr uint32_t kSmem = kBar + 512;
-    static_assert(kColS + kBN <= kTmemCols, "tensor memory budget");
+    static_assert(kColS0 + 2 * kBN <= kTmemCols, "tensor memory budget");
     static_assert(kVChunks * kVK == kBN, "V chunks tile the key tile");
+    static_assert(kSlots <= kMaxSlots, "barrier arrays");
+    static_assert(kRing > 0, "a ring slot's shared address is never 0");
 };
+__host__ __device__ constexpr uint32_t col_s(uint32_t s0, int b) { return s0 + 128u * b; }
 
 struct Barriers {
-    uint64_t full[kSlots];   // TMA landed
-    uint64_t ready[kSlots];  // split done (four splitter warps)
-    uint64_t empty[kSlots];  // MMAs done reading
-    uint64_t q_ready, s_full, p_full, o_final, drain;
+    uint64_t full[kMaxSlots];   // TMA landed
+    uint64_t ready[kMaxSlots];  // split done (four splitter warps)
+    uint64_t empty[kMaxSlots];  // MMAs done reading
+    uint64_t s_full[2], p_full[2];
+    uint64_t q_ready, o_done, o_final, drain;
     uint32_t tmem_base;
     int abort;
 };
 
+template <int N>
 struct Pos {
     int st = 0;
     uint32_t ph = 0;
     __device__ __forceinline__ void advance() {
-        if (++st == kSlots) {
+        if (++st == N) {
             st = 0;
             ph ^= 1u;
         }
     }
 };
+
+// The chunk order of the ring: K_0, K_1, then V_t, K_{t+2} for t = 0..n-1.
+// f(is_v, tile, chunk) returns false to stop.
+template <int D, typename F>
+__device__ __forceinline__ bool for_each_chunk(int n, F &&f) {
+    using C = Cfg<D>;
+    auto k_tile = [&](int t) {
+        for (int c = 0; c < C::kKChunks; ++c)
+            if (!f(false, t, c)) return false;
+        return true;
+    };
+    if (n > 0 && !k_tile(0)) return false;
+    if (n > 1 && !k_tile(1)) return false;
+    for (int t = 0; t < n; ++t) {
+        for (int c = 0; c < C::kVChunks; ++c)
+            if (!f(true, t, c)) return false;
+        if (t + 2 < n && !k_tile(t + 2)) return false;
+    }
+    return true;
+}
 
 // Drop the 13 mantissa bits the TF32 mode ignores.
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
@@ -137,31 +169,28 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUte
                                               uint8_t *smem, Barriers &bar) {
     using C = Cfg<D>;
     volatile int *abort = &bar.abort;
-    int uses[kSlots] = {};
-    Pos p;
-    bool ok = true;
-    for (int j = 0; j < U.n_tiles && ok; ++j) {
-        const int key0 = (U.t_begin + j) * kBN;
-        for (int c = 0; c < C::kKChunks + C::kVChunks && ok; ++c) {
-            if (uses[p.st] > 0 && !(ok = mbar_wait(&bar.empty[p.st], p.ph ^ 1u, abort))) break;
-            uint8_t *slot = smem + p.st * kSlotBytes;
-            if (c < C::kKChunks) {
-                mbar_arrive_expect_tx(&bar.full[p.st], kBN * 128);
-                tma_load_4d(slot, &tmK, &bar.full[p.st], c * 32, key0, U.g, U.b);
-            } else {
-                const int v0 = key0 + (c - C::kKChunks) * C::kVK;
-                mbar_arrive_expect_tx(&bar.full[p.st], kSlotBytes);
+    int uses[C::kSlots] = {};
+    Pos<C::kSlots> p;
+    for_each_chunk<D>(U.n_tiles, [&](bool is_v, int t, int c) {
+        if (uses[p.st] > 0 && !mbar_wait(&bar.empty[p.st], p.ph ^ 1u, abort)) return false;
+        uint8_t *slot = smem + C::kRing + p.st * kSlotBytes;
+        const int key0 = (U.t_begin + t) * kBN;
+        if (!is_v) {
+            mbar_arrive_expect_tx(&bar.full[p.st], kBN * 128);
+            tma_load_4d(slot, &tmK, &bar.full[p.st], c * 32, key0, U.g, U.b);
+        } else {
+            mbar_arrive_expect_tx(&bar.full[p.st], kSlotBytes);
 #pragma unroll
-                for (int bx = 0; bx < D / 32; ++bx)
-                    tma_load_4d(slot + bx * (C::kVK * 128), &tmV, &bar.full[p.st], bx * 32, v0, U.g, U.b);
-            }
-            ++uses[p.st];
-            p.advance();
+            for (int bx = 0; bx < D / 32; ++bx)
+                tma_load_4d(slot + bx * (C::kVK * 128), &tmV, &bar.full[p.st], bx * 32, key0 + c * C::kVK, U.g, U.b);
         }
-    }
+        ++uses[p.st];
+        p.advance();
+        return true;
+    });
     // Every copy issued lands before shared memory goes away.
     int never = 0;
-    for (int s = 0; s < kSlots; ++s)
+    for (int s = 0; s < C::kSlots; ++s)
         if (uses[s] > 0) mbar_wait(&bar.full[s], (uses[s] - 1) & 1, &never, 200000000ull);
 }
 
@@ -185,114 +214,153 @@ __device__ __forceinline__ void split_role(const Unit &U, uint8_t *smem, Barrier
     static_assert(32 % kUnitsPerRow == 0 || kUnitsPerRow % 32 == 0, "a warp instruction covers whole rows");
     volatile int *abort = &bar.abort;
     const int sw = t >> 5;
-    Pos p;
-    bool ok = true;
-    for (int j = 0; j < U.n_tiles && ok; ++j) {
-        for (int c = 0; c < C::kKChunks + C::kVChunks; ++c) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.full[p.st], p.ph, abort)))) break;
-            uint8_t *slot = smem + p.st * kSlotBytes;
-            if (c < C::kKChunks) {
-                const float4 *src = reinterpret_cast<const float4 *>(slot);
-                float4 *dst = reinterpret_cast<float4 *>(slot + kBN * 128);
+    Pos<C::kSlots> p;
+    for_each_chunk<D>(U.n_tiles, [&](bool is_v, int, int) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.full[p.st], p.ph, abort))) return false;
+        uint8_t *slot = smem + C::kRing + p.st * kSlotBytes;
+        if (!is_v) {
+            const float4 *src = reinterpret_cast<const float4 *>(slot);
+            float4 *dst = reinterpret_cast<float4 *>(slot + kBN * 128);
 #pragma unroll
-                for (int e = 0; e < kBN * 128 / 16 / 128; ++e) {
-                    const float4 x = src[t + 128 * e];
-                    dst[t + 128 * e] =
-                        make_float4(x.x - tf32_hi(x.x), x.y - tf32_hi(x.y), x.z - tf32_hi(x.z), x.w - tf32_hi(x.w));
-                }
-            } else {
-                // Batches of kBatch warp instructions, each a set of whole
-                // rows: read, __syncwarp, rewrite.
-#pragma unroll
-                for (int i0 = 0; i0 < kUnitsPerThread; i0 += kBatch) {
-                    float4 x[kBatch];
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int u = ((i0 + i) * kSplitWarps + sw) * 32 + lane;
-                        const int r = u / kUnitsPerRow, c4 = u % kUnitsPerRow;
-                        x[i] = *reinterpret_cast<const float4 *>(slot + (c4 >> 3) * (C::kVK * 128) + r * 128 +
-                                                                 (((c4 & 7) ^ (r & 7)) << 4));
-                    }
-                    __syncwarp();  // the batch's rows read before any is rewritten
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int u = ((i0 + i) * kSplitWarps + sw) * 32 + lane;
-                        const int r = u / kUnitsPerRow, c4 = u % kUnitsPerRow;
-                        const uint32_t h0 = cvt_bf16x2(x[i].x, x[i].y), h1 = cvt_bf16x2(x[i].z, x[i].w);
-                        const uint32_t l0 = cvt_bf16x2(x[i].x - bf16_lo_f(h0), x[i].y - bf16_hi_f(h0));
-                        const uint32_t l1 = cvt_bf16x2(x[i].z - bf16_lo_f(h1), x[i].w - bf16_hi_f(h1));
-                        // bf16 column 4 c4: box c4 / 16, byte 8 (c4 % 16) of the box's 128-byte row
-                        const uint32_t off = (c4 >> 4) * (C::kVK * 128) + r * 128 +
-                                             ((((c4 & 15) >> 1) ^ (r & 7)) << 4) + ((c4 & 1) << 3);
-                        *reinterpret_cast<uint2 *>(slot + off) = make_uint2(h0, h1);
-                        *reinterpret_cast<uint2 *>(slot + 16384 + off) = make_uint2(l0, l1);
-                    }
-                    __syncwarp();
-                }
+            for (int e = 0; e < kBN * 128 / 16 / 128; ++e) {
+                const float4 x = src[t + 128 * e];
+                dst[t + 128 * e] =
+                    make_float4(x.x - tf32_hi(x.x), x.y - tf32_hi(x.y), x.z - tf32_hi(x.z), x.w - tf32_hi(x.w));
             }
-            fence_proxy_async_smem();  // the MMAs read the split parts through the async proxy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.ready[p.st]);
-            p.advance();
+        } else {
+            // Batches of kBatch warp instructions, each a set of whole
+            // rows: read, __syncwarp, rewrite.
+#pragma unroll
+            for (int i0 = 0; i0 < kUnitsPerThread; i0 += kBatch) {
+                float4 x[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    const int u = ((i0 + i) * kSplitWarps + sw) * 32 + lane;
+                    const int r = u / kUnitsPerRow, c4 = u % kUnitsPerRow;
+                    x[i] = *reinterpret_cast<const float4 *>(slot + (c4 >> 3) * (C::kVK * 128) + r * 128 +
+                                                             (((c4 & 7) ^ (r & 7)) << 4));
+                }
+                __syncwarp();  // the batch's rows read before any is rewritten
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    const int u = ((i0 + i) * kSplitWarps + sw) * 32 + lane;
+                    const int r = u / kUnitsPerRow, c4 = u % kUnitsPerRow;
+                    const uint32_t h0 = cvt_bf16x2(x[i].x, x[i].y), h1 = cvt_bf16x2(x[i].z, x[i].w);
+                    const uint32_t l0 = cvt_bf16x2(x[i].x - bf16_lo_f(h0), x[i].y - bf16_hi_f(h0));
+                    const uint32_t l1 = cvt_bf16x2(x[i].z - bf16_lo_f(h1), x[i].w - bf16_hi_f(h1));
+                    // bf16 column 4 c4: box c4 / 16, byte 8 (c4 % 16) of the box's 128-byte row
+                    const uint32_t off = (c4 >> 4) * (C::kVK * 128) + r * 128 +
+                                         ((((c4 & 15) >> 1) ^ (r & 7)) << 4) + ((c4 & 1) << 3);
+                    *reinterpret_cast<uint2 *>(slot + off) = make_uint2(h0, h1);
+                    *reinterpret_cast<uint2 *>(slot + 16384 + off) = make_uint2(l0, l1);
+                }
+                __syncwarp();
+            }
         }
-    }
+        fence_proxy_async_smem();  // the MMAs read the split parts through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.ready[p.st]);
+        p.advance();
+        return true;
+    });
 }
 
-// K-major operand descriptor, 128-byte swizzle, 8-row atoms of 1 KB.
-__device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
+// A shared-memory descriptor as its two 32-bit halves; stepping the start
+// address by b bytes adds b >> 4 to the low half (addresses stay far below
+// the field's 2^18-byte range).
+struct Desc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc desc_of(uint32_t saddr, uint32_t lbo) {
+    const uint64_t d = smem_desc_sw128(saddr, lbo, 1024);
+    return Desc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
 
-// MMA issuer: per tile, S = Q K^T chunk by chunk, then (once P is written)
-// O += P V chunk by chunk; each chunk's slot is released by a commit.
+// MMA issuer: S_0, S_1, then per tile t (once P_t is written) O += P_t V_t
+// and S_{t+2} into the buffer P_t came from (the tcgen05 MMAs of one thread
+// execute in order).  Each chunk's slot is released by a commit.  A single
+// thread issues every MMA, each only 64 cycles long, so the issue path is
+// kept to a few instructions per MMA: descriptors are stepped by adding to
+// their low halves and the accumulate flag is a compile-time constant.
 template <int D>
 __device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using C = Cfg<D>;
     constexpr uint32_t idQK = idesc_tf32_f32(kBM, kBN);
     constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, 0, 1);
+    constexpr uint32_t kLoHalf = (kBN * 128) >> 4;  // K_lo: 16 KB after the raw chunk
+    constexpr uint32_t kPlane1 = 16384 >> 4;        // V_1: 16 KB after V_0
     volatile int *abort = &bar.abort;
     const int n = U.n_tiles;
-    bool ok = true;
-    Pos p;
-    if (n > 0) {
-        ok = mbar_wait(&bar.q_ready, 0, abort);
-        for (int j = 0; j < n && ok; ++j) {
-            for (int c = 0; c < C::kKChunks; ++c) {
-                if (!(ok = mbar_wait(&bar.ready[p.st], p.ph, abort))) break;
-                tc_fence_after();
-                const uint32_t s = smem_u32(smem + p.st * kSlotBytes);
+    const uint32_t qlo = smem_u32(smem + C::kQlo);
+    Pos<C::kSlots> p;
+    auto wait_slot = [&]() -> uint32_t {
+        if (!mbar_wait(&bar.ready[p.st], p.ph, abort)) return 0u;
+        tc_fence_after();
+        return smem_u32(smem + C::kRing + p.st * kSlotBytes);
+    };
+    auto release_slot = [&]() {
+        mma_commit(&bar.empty[p.st]);
+        p.advance();
+    };
+    // S_t = Q_hi K + Q_hi K_lo + Q_lo K into buffer t % 2, 8 columns of d per step.
+    auto issue_s = [&](int t) -> bool {
+        const uint32_t d = tbase + col_s(C::kColS0, t & 1);
+        for (int c = 0; c < C::kKChunks; ++c) {
+            const uint32_t s = wait_slot();
+            if (s == 0u) return false;
+            const Desc k = desc_of(s, 16), q = desc_of(qlo + c * (kBM * 128), 16);
+            const uint32_t aq = tbase + C::kColQh + c * 32;
+            if (c == 0)
+                mma_ts_tf32_c<0>(d, aq, k.lo, k.hi, idQK);
+            else
+                mma_ts_tf32_c<1>(d, aq, k.lo, k.hi, idQK);
+            mma_ts_tf32_c<1>(d, aq, k.lo + kLoHalf, k.hi, idQK);
+            mma_ss_tf32_c<1>(d, q.lo, q.hi, k.lo, k.hi, idQK);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t dr = desc_k(s + kk * 32), dl = desc_k(s + kBN * 128 + kk * 32);
-                    const uint32_t aq = tbase + C::kColQh + c * 32 + kk * 8;
-                    const uint32_t al = tbase + C::kColQl + c * 32 + kk * 8;
-                    mma_ts_tf32(tbase + C::kColS, aq, (uint32_t)dr, (uint32_t)(dr >> 32), idQK, (c | kk) != 0);
-                    mma_ts_tf32(tbase + C::kColS, aq, (uint32_t)dl, (uint32_t)(dl >> 32), idQK, 1u);
-                    mma_ts_tf32(tbase + C::kColS, al, (uint32_t)dr, (uint32_t)(dr >> 32), idQK, 1u);
+            for (int kk = 1; kk < 4; ++kk) {
+                mma_ts_tf32_c<1>(d, aq + kk * 8, k.lo + kk * 2, k.hi, idQK);
+                mma_ts_tf32_c<1>(d, aq + kk * 8, k.lo + kLoHalf + kk * 2, k.hi, idQK);
+                mma_ss_tf32_c<1>(d, q.lo + kk * 2, q.hi, k.lo + kk * 2, k.hi, idQK);
+            }
+            release_slot();
+        }
+        mma_commit(&bar.s_full[t & 1]);
+        return true;
+    };
+    if (n > 0) {
+        bool ok = mbar_wait(&bar.q_ready, 0, abort);
+        if (ok) ok = issue_s(0);
+        if (ok && n > 1) ok = issue_s(1);
+        for (int j = 0; j < n && ok; ++j) {
+            if (!(ok = mbar_wait(&bar.p_full[j & 1], (j >> 1) & 1, abort))) break;
+            tc_fence_after();
+            const uint32_t sb = tbase + col_s(C::kColS0, j & 1);
+            for (int c = 0; c < C::kVChunks && ok; ++c) {
+                const uint32_t s = wait_slot();
+                ok = s != 0u;
+                if (!ok) break;
+                // 16 keys per step: 2 KB of each V plane, 8 columns of P.
+                const Desc v = desc_of(s, C::kVK * 128);
+                const uint32_t a0 = sb + c * (C::kVK / 2);
+                if ((j | c) == 0)
+                    mma_ts_c<0>(tbase + C::kColO, a0, v.lo, v.hi, idPV);
+                else
+                    mma_ts_c<1>(tbase + C::kColO, a0, v.lo, v.hi, idPV);
+                mma_ts_c<1>(tbase + C::kColO, a0, v.lo + kPlane1, v.hi, idPV);
+                mma_ts_c<1>(tbase + C::kColO, a0 + 64, v.lo, v.hi, idPV);
+#pragma unroll
+                for (int kk = 1; kk < C::kVK / 16; ++kk) {
+                    mma_ts_c<1>(tbase + C::kColO, a0 + kk * 8, v.lo + kk * 128, v.hi, idPV);
+                    mma_ts_c<1>(tbase + C::kColO, a0 + kk * 8, v.lo + kPlane1 + kk * 128, v.hi, idPV);
+                    mma_ts_c<1>(tbase + C::kColO, a0 + 64 + kk * 8, v.lo + kk * 128, v.hi, idPV);
                 }
-                mma_commit(&bar.empty[p.st]);
-                p.advance();
+                release_slot();
             }
             if (!ok) break;
-            mma_commit(&bar.s_full);
-            if (!(ok = mbar_wait(&bar.p_full, j & 1, abort))) break;
-            tc_fence_after();
-            for (int c = 0; c < C::kVChunks; ++c) {
-                if (!(ok = mbar_wait(&bar.ready[p.st], p.ph, abort))) break;
-                tc_fence_after();
-                const uint32_t s = smem_u32(smem + p.st * kSlotBytes);
-#pragma unroll
-                for (int kk = 0; kk < C::kVK / 16; ++kk) {
-                    const uint64_t d0 = smem_desc_sw128(s + kk * 2048, C::kVK * 128, 1024);
-                    const uint64_t d1 = smem_desc_sw128(s + 16384 + kk * 2048, C::kVK * 128, 1024);
-                    const uint32_t a0 = tbase + C::kColS + (c * (C::kVK / 16) + kk) * 8;  // P_0: 16 keys
-                    mma_ts(tbase + C::kColO, a0, d0, idPV, (j | c | kk) != 0);
-                    mma_ts(tbase + C::kColO, a0, d1, idPV, 1u);
-                    mma_ts(tbase + C::kColO, a0 + 64, d0, idPV, 1u);  // P_1
-                }
-                mma_commit(&bar.empty[p.st]);
-                p.advance();
-            }
+            mma_commit(&bar.o_done);
+            if (j + 2 < n) ok = issue_s(j + 2);
         }
-        mma_commit(&bar.o_final);
+        if (ok) mma_commit(&bar.o_final);
     }
     mma_commit(&bar.drain);
     int never = 0;
@@ -303,8 +371,8 @@ __device__ __forceinline__ void mma_role(const Unit &U, uint8_t *smem, Barriers 
 // lanes l and l + 16 share a row: keys [0, 64) / [64, 128) of a tile,
 // columns [0, D/2) / [D/2, D) of Q and O.
 template <int D>
-__device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Barriers &bar, uint32_t tbase, int warp,
-                                             int lane) {
+__device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, uint8_t *smem, Barriers &bar,
+                                             uint32_t tbase, int warp, int lane) {
     using C = Cfg<D>;
     constexpr int kHK = kBN / 2;  // keys per thread
     constexpr int kHD = D / 2;    // columns of Q / O per thread
@@ -319,28 +387,31 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
     const int n = U.n_tiles;
     bool ok = true;
 
-    // Q row i, this thread's half of the columns: hi and lo into tensor memory.
+    // Q row i, this thread's half of the columns: Q_hi into tensor memory,
+    // Q_lo into shared memory ([D/32 boxes][128 rows][128 B], 128-byte
+    // swizzle: the K-major A operand of Q_lo K_hi).
     {
         const float *qrow = static_cast<const float *>(P.q) + U.b * P.q_sb + U.h * P.q_sh + (int64_t)i * P.q_st;
 #pragma unroll
         for (int cc = 0; cc < kHD; cc += 32) {
-            uint32_t hi[32], lo[32];
+            uint32_t hi[32];
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
                 const int col = half * kHD + cc + e;
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (live && col < P.d) x = __ldg(reinterpret_cast<const float4 *>(qrow + col));
-                const float v[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float hv = tf32_hi(v[k]);
-                    hi[e + k] = __float_as_uint(hv);
-                    lo[e + k] = __float_as_uint(v[k] - hv);
-                }
+                const float4 h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
+                hi[e] = __float_as_uint(h.x);
+                hi[e + 1] = __float_as_uint(h.y);
+                hi[e + 2] = __float_as_uint(h.z);
+                hi[e + 3] = __float_as_uint(h.w);
+                *reinterpret_cast<float4 *>(smem + C::kQlo + (col >> 5) * (kBM * 128) + row * 128 +
+                                            ((((col & 31) >> 2) ^ (row & 7)) << 4)) =
+                    make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
             }
             tmem_store_pair32<kHD>(tbase + lane_off + C::kColQh + cc, hi);
-            tmem_store_pair32<kHD>(tbase + lane_off + C::kColQl + cc, lo);
         }
+        fence_proxy_async_smem();  // Q_lo is read by the MMAs through the async proxy
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.q_ready);
@@ -370,11 +441,11 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
         ti_lo = (int)((lo_key + kBN - 1) / kBN - U.t_begin);
         ti_hi = (int)(hi_key / kBN - U.t_begin);
     }
-    const uint32_t s_addr = tbase + lane_off + C::kColS;
     const uint32_t o_addr = tbase + lane_off + C::kColO;
 
     for (int j = 0; j < n; ++j) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1, abort)))) break;
+        const uint32_t s_addr = tbase + lane_off + col_s(C::kColS0, j & 1);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort)))) break;
         tc_fence_after();
         uint32_t sr[kHK];
         tmem_load_pair64<kHK>(s_addr, sr);
@@ -420,8 +491,10 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
             m = bm;
         }
         const float shift = (m == -INFINITY) ? 0.f : m;
-        // S_j was issued after P_{j-1} V_{j-1}, so O is complete here.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // O must hold P_{j-1} V_{j-1} before it is rescaled.
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_done, (uint32_t)((j - 1) & 1), abort)))) break;
+            tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < kHD; cc += 16) {
                 uint32_t orr[16];
@@ -452,7 +525,7 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, Bar
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.p_full);
+        if (lane == 0) mbar_arrive(&bar.p_full[j & 1]);
         l = fmaf(alpha, l, acc0 + acc1);
     }
     if (!ok) return;
@@ -500,14 +573,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     Barriers &bar = *reinterpret_cast<Barriers *>(smem + C::kBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < C::kSlots; ++s) {
             mbar_init(&bar.full[s], 1);
             mbar_init(&bar.ready[s], kSplitWarps);
             mbar_init(&bar.empty[s], 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar.s_full[b], 1);
+            mbar_init(&bar.p_full[b], kSoftmaxWarps);
+        }
         mbar_init(&bar.q_ready, kSoftmaxWarps);
-        mbar_init(&bar.s_full, 1);
-        mbar_init(&bar.p_full, kSoftmaxWarps);
+        mbar_init(&bar.o_done, 1);
         mbar_init(&bar.o_final, 1);
         mbar_init(&bar.drain, 1);
         bar.abort = 0;
@@ -536,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kWarpSplit) {
         split_role<D>(U, smem, bar, threadIdx.x - kWarpSplit * 32, lane);
     } else {
-        softmax_role<D>(P, U, bar, tbase, warp, lane);
+        softmax_role<D>(P, U, smem, bar, tbase, warp, lane);
     }
 
     tc_fence_before();
