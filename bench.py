@@ -286,13 +286,16 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
     """fp32 28-layer prefill, fp32 long-context prefill, fp32 masked batch,
     variable-length batches, windowed-sink chunked prompt: device time per
     configuration from CUDA graphs.  fp32 runs on both fp32 paths: "f32" (SIMT
-    FFMA) and "f32tc" (three TF32 tensor-core products per matrix product;
-    its tensor work is 3x the algorithmic FLOPs, set against the dense TF32
-    peak taken as the measured bf16 peak x 1.1 / 2.25)."""
+    FFMA) and "f32tc" (tensor cores, three products per matrix product: Q K^T
+    as three TF32 products, P V as three bf16 products).  The f32tc ceiling:
+    half the algorithmic FLOPs are Q K^T, done three times at the dense TF32
+    rate (measured bf16 peak x 1.1 / 2.25), half are P V, done three times at
+    the bf16 rate; ceiling = 1 / (1.5 / R_tf32 + 1.5 / R_bf16)."""
     import torch
     out = []
     codes = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC}
     tf32_peak = peak_bf16 * TF32_OVER_BF16
+    tc_ceiling = 1.0 / (1.5 / tf32_peak + 1.5 / peak_bf16)
 
     def entry(name, dtype, fn, flops, reps=10):
         med, _ = time_graph(fn, reps, flush)
@@ -301,8 +304,9 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
         if dtype == "f32":
             e["frac_of_fp32_simt_peak"] = round(tf / FP32_SIMT_PEAK_TFLOPS, 4)
         elif dtype == "f32tc":
-            e["tf32_tensor_tflops"] = round(3 * tf, 2)
-            e["frac_of_tf32_tensor_peak"] = round(3 * tf / tf32_peak, 4)
+            e["tensor_ceiling_tflops"] = round(tc_ceiling, 1)
+            e["frac_of_tensor_ceiling"] = round(tf / tc_ceiling, 4)
+            e["frac_of_fp32_simt_peak"] = round(tf / FP32_SIMT_PEAK_TFLOPS, 4)
         out.append(e)
 
     # 28 x 511-token layers in fp32
