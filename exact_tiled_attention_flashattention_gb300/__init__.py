@@ -16,11 +16,11 @@ import ctypes
 from pathlib import Path
 
 __all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_DTYPE_F32", "FA_DTYPE_BF16",
-           "FA_DTYPE_F32_TC",
+           "FA_DTYPE_F32_TC", "FA_DTYPE_FP8_E4M3",
            "FaError", "fa_fwd", "fa_last_error", "fa_version", "attention", "library_path", "load"]
 
 FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA = 0, 1, 2, 3, 4
-FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F32_TC = 0, 1, 2
+FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F32_TC, FA_DTYPE_FP8_E4M3 = 0, 1, 2, 3
 _STATUS = {0: "FA_OK", 1: "FA_EINVAL", 2: "FA_ESHAPE", 3: "FA_EUNSUPPORTED", 4: "FA_ECUDA"}
 
 _LIB_PATH = Path(__file__).resolve().parent / "libfa.so"
@@ -122,8 +122,9 @@ def fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q_strides, k_strides,
 
 def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=None, mask=None,
               mask_strides=(0, 0, 0, 0), with_lse=True, out=None, lse_out=None, stream=None, fp32_tc=False):
-    """o [B,Hq,Tq,d] (q's dtype) and lse [B,Hq,Tq] (fp32) for CUDA tensors
-    q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (fp32 or bf16).  The tensors may be
+    """o [B,Hq,Tq,d] (q's dtype; bf16 for e4m3 inputs) and lse [B,Hq,Tq] (fp32)
+    for CUDA tensors q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d] (fp32, bf16 or
+    float8_e4m3fn).  The tensors may be
     strided views (a [B,T,H,d] buffer seen through .transpose(1, 2), say) as
     long as d is contiguous; ``out`` may be strided the same way.  ``mask``
     is an fp32 CUDA tensor addressed with ``mask_strides`` (elements).
@@ -137,6 +138,8 @@ def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=N
         dt = FA_DTYPE_F32_TC if fp32_tc else FA_DTYPE_F32
     elif q.dtype == torch.bfloat16:
         dt = FA_DTYPE_BF16
+    elif q.dtype == torch.float8_e4m3fn:
+        dt = FA_DTYPE_FP8_E4M3
     else:
         raise TypeError(f"unsupported dtype {q.dtype}")
     for name, t in (("q", q), ("k", k), ("v", v)) + ((("out", out),) if out is not None else ()):
@@ -144,7 +147,10 @@ def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=N
             raise ValueError(f"{name} must be 4-D with its last dimension contiguous")
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k and v must share a dtype")
-    o = out if out is not None else torch.empty((B, Hq, Tq, d), dtype=q.dtype, device=q.device)
+    o_dtype = torch.bfloat16 if dt == FA_DTYPE_FP8_E4M3 else q.dtype
+    if out is not None and out.dtype != o_dtype:
+        raise TypeError(f"out must be {o_dtype}")
+    o = out if out is not None else torch.empty((B, Hq, Tq, d), dtype=o_dtype, device=q.device)
     if lse_out is not None and not lse_out.is_contiguous():
         raise ValueError("lse_out must be contiguous [B, Hq, Tq]")
     lse = lse_out if lse_out is not None else (

@@ -74,7 +74,9 @@ bool layout_ok(int64_t B, int64_t H, int64_t T, int64_t d, int64_t sb, int64_t s
     return true;
 }
 
-bool known_dtype(int dtype) { return dtype == FA_DTYPE_F32 || dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F32_TC; }
+bool known_dtype(int dtype) {
+    return dtype == FA_DTYPE_F32 || dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F32_TC || dtype == FA_DTYPE_FP8_E4M3;
+}
 
 // Every stride of a dimension with extent > 1 is a multiple of `m` elements.
 bool strides_multiple(int64_t B, int64_t H, int64_t T, int64_t sb, int64_t sh, int64_t st, int64_t m) {
@@ -124,27 +126,33 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     if (dtype == FA_DTYPE_F32_TC && (d % 4 != 0 || d > 128))
         return fail(FA_EUNSUPPORTED, "tensor-core fp32 path supports d a multiple of 4 up to 128 (got %lld)",
                     (long long)d);
+    if (dtype == FA_DTYPE_FP8_E4M3 && (d % 16 != 0 || d > 128))
+        return fail(FA_EUNSUPPORTED, "e4m3 path supports d a multiple of 16 up to 128 (got %lld)", (long long)d);
     if (Tq >= kMaxLen || Tk >= kMaxLen || q_offset >= kMaxLen)
         return fail(FA_EUNSUPPORTED, "Tq, Tk and q_offset must be below 2^30");
     if (B * Hq >= (int64_t(1) << 24)) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^24");
     if (!aligned16(q) || !aligned16(o) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
         return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
-    // bf16 and fp32 on the tensor cores: tensor-map strides are 16-byte
-    // multiples below 2^40 bytes.  fp32 on the SIMT cores: rows start on
-    // 8-byte boundaries (16-byte copies when all do).
+    // bf16, e4m3 and fp32 on the tensor cores: tensor-map strides are
+    // 16-byte multiples below 2^40 bytes (o is bf16 with e4m3 inputs).  fp32
+    // on the SIMT cores: rows start on 8-byte boundaries (16-byte copies when
+    // all do).
     const bool tma = dtype != FA_DTYPE_F32;
-    const int64_t m = dtype == FA_DTYPE_BF16 ? 8 : (dtype == FA_DTYPE_F32_TC ? 4 : 2);
+    const int64_t in_bytes = dtype == FA_DTYPE_FP8_E4M3 ? 1 : (dtype == FA_DTYPE_BF16 ? 2 : 4);
+    const int64_t out_bytes = dtype == FA_DTYPE_FP8_E4M3 ? 2 : in_bytes;
+    const int64_t m = tma ? 16 / in_bytes : 2, mo = tma ? 16 / out_bytes : 2;
     const bool kv = Tk > 0;
-    if (!strides_multiple(B, Hq, Tq, qs[0], qs[1], qs[2], m) || !strides_multiple(B, Hq, Tq, os[0], os[1], os[2], m) ||
+    if (!strides_multiple(B, Hq, Tq, qs[0], qs[1], qs[2], m) || !strides_multiple(B, Hq, Tq, os[0], os[1], os[2], mo) ||
         (kv && (!strides_multiple(B, Hkv, Tk, ks[0], ks[1], ks[2], m) ||
                 !strides_multiple(B, Hkv, Tk, vs[0], vs[1], vs[2], m))))
-        return fail(FA_EUNSUPPORTED, "strides must be multiples of %lld elements for this dtype", (long long)m);
+        return fail(FA_EUNSUPPORTED, "strides must be multiples of %lld elements (o: %lld) for this dtype",
+                    (long long)m, (long long)mo);
     if (tma) {
-        const int64_t lim = ((int64_t(1) << 40) / (dtype == FA_DTYPE_BF16 ? 2 : 4)) - 1;  // elements
         const int64_t ext[4][3] = {{B, Hq, Tq}, {B, Hkv, Tk}, {B, Hkv, Tk}, {B, Hq, Tq}};
         const int64_t *all[4] = {qs, ks, vs, os};
         for (int t = 0; t < 4; ++t)
             for (int i = 0; i < 3; ++i) {
+                const int64_t lim = ((int64_t(1) << 40) / (t == 3 ? out_bytes : in_bytes)) - 1;  // elements
                 if (all[t][i] > lim) return fail(FA_EUNSUPPORTED, "a stride reaches 2^40 bytes");
                 if (ext[t][i] > 1 && all[t][i] <= 0 && (t == 0 || t == 3 || kv))
                     return fail(FA_EUNSUPPORTED, "strides must be positive for this dtype (tensor maps)");
@@ -191,9 +199,10 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     P.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dtype == FA_DTYPE_F32 ? fa::launch_f32(P, s)
-                    : dtype == FA_DTYPE_BF16 ? fa::launch_bf16(P, s)
-                                             : fa::launch_f32_tc(P, s);
+    cudaError_t e = dtype == FA_DTYPE_F32      ? fa::launch_f32(P, s)
+                    : dtype == FA_DTYPE_BF16   ? fa::launch_bf16(P, s)
+                    : dtype == FA_DTYPE_F32_TC ? fa::launch_f32_tc(P, s)
+                                               : fa::launch_fp8(P, s);
     if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
     return FA_OK;
 }
@@ -328,7 +337,8 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
     if (B == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query row
     if (!q || !o || !cu_seqlens_q || !cu_seqlens_k) return fail(FA_EINVAL, "q, o or a cu_seqlens table is NULL");
     if (total_k > 0 && (!k || !v)) return fail(FA_EINVAL, "k or v is NULL with total_k > 0");
-    if (dtype == FA_DTYPE_F32_TC) return fail(FA_EUNSUPPORTED, "the varlen path is fp32 (SIMT) or bf16 only");
+    if (dtype == FA_DTYPE_F32_TC || dtype == FA_DTYPE_FP8_E4M3)
+        return fail(FA_EUNSUPPORTED, "the varlen path is fp32 (SIMT) or bf16 only");
     if (d == 0 || (d & 1)) return fail(FA_EUNSUPPORTED, "d=%lld: d must be even and positive", (long long)d);
     if (dtype == FA_DTYPE_F32 && d > 256)
         return fail(FA_EUNSUPPORTED, "fp32 path supports d <= 256 (got %lld)", (long long)d);

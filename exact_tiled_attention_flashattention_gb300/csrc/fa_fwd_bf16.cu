@@ -106,23 +106,33 @@ constexpr int kMaxStages = 6;
 //   kVarlen   kPrefill over a batch of sequences packed along the rows
 //             ([total, H, d] tensors, cu_seqlens offsets), each with its own
 //             row and key counts; O is written with predicated stores.
-constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3;
+//   kPrefill8 kPrefill with e4m3 Q, K and V: the MMAs are kind::f8f6f4 (32
+//             elements per K step), P is rounded to e4m3 (four per tensor-
+//             memory column), O stays bf16.
+constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3, kPrefill8 = 4;
+__host__ __device__ constexpr bool is_prefill(int mode) { return mode == kPrefill || mode == kPrefill8; }
+__host__ __device__ constexpr int elem_bytes(int mode) { return mode == kPrefill8 ? 1 : 2; }  // Q, K, V
 
 template <int D, int MODE>
 struct SmemLayout {
-    static constexpr int kBoxes = D / 64;  // 64-column TMA boxes per tile
-    static constexpr uint32_t kQBytes = kBM * D * 2;
-    static constexpr uint32_t kKVBytes = kBN * D * 2;     // one K or V tile (a ring stage)
-    static constexpr int kStages = D == 128 ? 3 : 6;      // K ring: 96 KB
+    static constexpr int kE = elem_bytes(MODE);
+    static constexpr int kBoxCols = 128 / kE;  // columns of a 128-byte TMA box
+    static constexpr int kBoxes = D / kBoxCols;  // boxes per Q, K or V tile
+    static constexpr int kOBoxes = D / 64;       // O is bf16
+    static_assert(D % kBoxCols == 0 && kOBoxes * 64 == D, "whole boxes");
+    static constexpr uint32_t kQBytes = kBM * D * kE;
+    static constexpr uint32_t kKVBytes = kBN * D * kE;                    // one K or V tile (a ring stage)
+    static constexpr uint32_t kOBytes = kBM * D * 2;                      // the bf16 O tile
+    static constexpr int kStages = (D == 128 && kE == 2) ? 3 : 6;         // K ring: 96 KB
     // V ring: one stage fewer in prefill, where the O tile is staged for its
     // TMA store; packed rows write O from registers and take the full ring.
-    static constexpr bool kStaging = MODE == kPrefill;  // O leaves through a TMA store
+    static constexpr bool kStaging = is_prefill(MODE);  // O leaves through a TMA store
     static constexpr int kVStages = kStaging ? kStages - 1 : kStages;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKRing = kQ + kQBytes;
     static constexpr uint32_t kVRing = kKRing + kStages * kKVBytes;
     static constexpr uint32_t kOStage = kVRing + kVStages * kKVBytes;  // O tile, bf16, for the TMA store
-    static constexpr uint32_t kBar = kOStage + (kStaging ? kQBytes : 0u);
+    static constexpr uint32_t kBar = kOStage + (kStaging ? kOBytes : 0u);
     // Packed-row split merge: O partials (fp32, padded rows) over the K ring,
     // (m, l) per row over the V ring.
     static constexpr int kOPartStride = D + 4;
@@ -307,33 +317,53 @@ __device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t
     return Desc{(uint32_t)d, (uint32_t)(d >> 32)};
 }
 
-// S = Q K^T over d: D/16 MMAs of 128 x 128 x 16.  Q and K are K-major with
-// the 128-byte swizzle: 16-element steps advance 32 bytes inside a 64-column
-// box, then jump to the next box.
-template <int D>
+// S = Q K^T over d in 32-byte K steps: D/16 MMAs of 128 x 128 x 16 (bf16) or
+// D/32 of 128 x 128 x 32 (e4m3).  Q and K are K-major with the 128-byte
+// swizzle: a step advances 32 bytes inside a 128-byte box row, and every
+// fourth step jumps to the next box.
+template <int D, int MODE>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, Desc q, Desc k) {
-    constexpr uint32_t kId = idesc_bf16_f32(kBM, kBN, 0, 0);
+    constexpr bool kF8 = elem_bytes(MODE) == 1;
+    constexpr uint32_t kId = kF8 ? idesc_e4m3_f32(kBM, kBN, 0, 0) : idesc_bf16_f32(kBM, kBN, 0, 0);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
+    for (int kk = 0; kk < D * elem_bytes(MODE) / 32; ++kk) {
         const uint32_t oq = ((kk >> 2) * (kBM * kSwRowBytes) + (kk & 3) * 32) >> 4;
         const uint32_t ok = ((kk >> 2) * (kBN * kSwRowBytes) + (kk & 3) * 32) >> 4;
-        if (kk == 0)
-            mma_ss_c<0>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
-        else
-            mma_ss_c<1>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
+        if constexpr (kF8) {
+            if (kk == 0)
+                mma_ss_f8_c<0>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
+            else
+                mma_ss_f8_c<1>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
+        } else {
+            if (kk == 0)
+                mma_ss_c<0>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
+            else
+                mma_ss_c<1>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
+        }
     }
 }
 
-// O += P V over the 128 keys of a tile: 8 MMAs of 128 x D x 16, P from tensor
-// memory (8 columns of bf16 pairs per step), V MN-major: 16 keys are two
-// 8-row swizzle atoms, the next 64 value columns one TMA box further on.
-template <int D>
+// O += P V over the 128 keys of a tile, 32 bytes of keys per step: 8 MMAs of
+// 128 x D x 16 (bf16) or 4 of 128 x D x 32 (e4m3), P from tensor memory (8
+// columns per step: bf16 pairs or e4m3 quads), V MN-major: a step's keys are
+// whole 8-row swizzle atoms, the next 128 bytes of value columns one TMA box
+// further on.
+template <int D, int MODE>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc v, uint32_t accumulate) {
-    constexpr uint32_t kId = idesc_bf16_f32(kBM, D, 0, 1);
-    mma_ts_r(o_tmem, p_tmem, v.lo, v.hi, kId, accumulate);
+    constexpr bool kF8 = elem_bytes(MODE) == 1;
+    constexpr int kKeys = 32 / elem_bytes(MODE);  // keys per step
+    constexpr uint32_t kId = kF8 ? idesc_e4m3_f32(kBM, D, 0, 1) : idesc_bf16_f32(kBM, D, 0, 1);
+    if constexpr (kF8) {
+        mma_ts_f8_r(o_tmem, p_tmem, v.lo, v.hi, kId, accumulate);
 #pragma unroll
-    for (int kk = 1; kk < kBN / 16; ++kk)
-        mma_ts_c<1>(o_tmem, p_tmem + kk * 8, v.lo + ((kk * 16 * kSwRowBytes) >> 4), v.hi, kId);
+        for (int kk = 1; kk < kBN / kKeys; ++kk)
+            mma_ts_f8_c<1>(o_tmem, p_tmem + kk * 8, v.lo + ((kk * kKeys * kSwRowBytes) >> 4), v.hi, kId);
+    } else {
+        mma_ts_r(o_tmem, p_tmem, v.lo, v.hi, kId, accumulate);
+#pragma unroll
+        for (int kk = 1; kk < kBN / kKeys; ++kk)
+            mma_ts_c<1>(o_tmem, p_tmem + kk * 8, v.lo + ((kk * kKeys * kSwRowBytes) >> 4), v.hi, kId);
+    }
 }
 
 // TMA producer (one thread).  Per unit: K_0 and K_1, then Q once the previous
@@ -380,17 +410,17 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
 #pragma unroll
                     for (int c = 0; c < L::kBoxes; ++c)
                         tma_load_4d(smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes) + k0 * kSwRowBytes, map,
-                                    &full[st], c * 64, key % P.page_size, U.g, page);
+                                    &full[st], c * L::kBoxCols, key % P.page_size, U.g, page);
                 }
             } else {
 #pragma unroll
             for (int c = 0; c < L::kBoxes; ++c) {
                 uint8_t *dst = smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes);
                 if (PAIR == 2)
-                    tma_load_4d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * 64,
+                    tma_load_4d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * L::kBoxCols,
                                           U.krow + key0 + rank * (kBN / 2), U.g, kvb, (uint16_t)0x3);
                 else
-                    tma_load_4d(dst, map, &full[st], c * 64, U.krow + key0, U.g, kvb);
+                    tma_load_4d(dst, map, &full[st], c * L::kBoxCols, U.krow + key0, U.g, kvb);
             }
             }
             ++issued[st];
@@ -415,12 +445,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
             for (int c = 0; c < L::kBoxes; ++c)
-                tma_load_5d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, 0, 0, U.g, U.b);
+                tma_load_5d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, 0, 0, U.g,
+                            U.b);
         } else {
             mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kBoxes; ++c)
-                tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * 64, U.qrow + U.r0, U.h,
+                tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, U.qrow + U.r0, U.h,
                             MODE == kVarlen ? 0 : U.b);
         }
         ++q_issued;
@@ -485,7 +516,7 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
             // the buffer's previous use: O += P V from it completed
             if (!first_use && !(ok = mbar_wait(&bar.o_done[b], sb.ph ^ 1u, abort))) break;
             tc_fence_after();
-            issue_qk<D>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
+            issue_qk<D, MODE>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
             mma_commit(&bar.s_full[b]);
             if (j + 1 == n) mma_commit(&bar.q_empty);  // the unit's last S is issued
             release_stage<PAIR>(&bar.k_empty[take.st]);
@@ -523,7 +554,8 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
             if (!(ok = mbar_wait(&bar.v_full[take.st], take.ph, abort))) break;
             if (!(ok = mbar_wait(&bar.p_full[b], sb.ph, abort))) break;
             tc_fence_after();
-            issue_pv<D>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + take.st * kTileUnits, v0.hi}, j > 0 ? 1u : 0u);
+            issue_pv<D, MODE>(tbase + kColO, tbase + col_s(b), Desc{v0.lo + take.st * kTileUnits, v0.hi},
+                              j > 0 ? 1u : 0u);
             mma_commit(&bar.o_done[b]);
             if (j + 1 == n) mma_commit(&bar.o_final);
             release_stage<PAIR>(&bar.v_empty[take.st]);
@@ -595,7 +627,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         const int64_t p = (int64_t)uq0 + i;
         // Per-row visible key interval [vlo, vhi) before the additive mask.
         int vlo = 0, vhi = 0;  // within [0, Tk]
-        if (MODE == kPrefill || live) {
+        if (is_prefill(MODE) || live) {
             int64_t lo64, hi64;
             visible_range_tk(P, uTk, p, lo64, hi64);
             vlo = (int)lo64;
@@ -604,7 +636,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         const bool has_sink = P.sinks != nullptr;
         // The sink joins the sum once: in the first CTA of a split key range.
         const bool sink_here =
-            has_sink && half == 0 && (MODE == kPrefill || MODE == kVarlen || (int)blockIdx.x % P.splits == 0);
+            has_sink && half == 0 && (is_prefill(MODE) || MODE == kVarlen || (int)blockIdx.x % P.splits == 0);
         float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;  // log2 units
         float l = sink_here ? 1.f : 0.f;                                // this thread's share of the sum
         const float *mrow = (!kSeq && P.mask != nullptr && live)
@@ -705,10 +737,13 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 }
             }
 
-            // p = 2^(s cs - shift), rounded to bf16 pairs; row sum in fp32.
+            // p = 2^(s cs - shift), rounded to bf16 pairs (e4m3 quads with
+            // e4m3 inputs: p <= 2^8 stays below the format's 448); row sum of
+            // the unrounded p in fp32.
             const float2 cs2 = make_float2(cs, cs), nsh2 = make_float2(-shift, -shift);
             float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-            uint32_t pk[kHK / 2];
+            constexpr int kPerWord = 4 / elem_bytes(MODE);  // P elements per 32-bit column
+            uint32_t pk[kHK / kPerWord];
 #pragma unroll
             for (int e = 0; e < kHK; e += 4) {
                 const float2 x0 = ffma2(make_float2(s[e], s[e + 1]), cs2, nsh2);
@@ -717,11 +752,19 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
                 acc0 = fadd2(acc0, p0);
                 acc1 = fadd2(acc1, p1);
-                pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
-                pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
+                if constexpr (kPerWord == 4) {
+                    pk[e / 4] = cvt_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+                } else {
+                    pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
+                    pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
+                }
             }
-            // P of keys [64 h, 64 h + 64) into columns [32 h, 32 h + 32) of the buffer.
-            tmem_store_pair32<kHK / 2>(s_addr, pk);
+            // P of keys [64 h, 64 h + 64) into columns [32 h, 32 h + 32) (bf16)
+            // or [16 h, 16 h + 16) (e4m3) of the buffer.
+            if constexpr (kPerWord == 4)
+                tmem_store_pair16<kHK / 4>(s_addr, pk);
+            else
+                tmem_store_pair32<kHK / 2>(s_addr, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.p_full[b]);  // one arrival per warp
@@ -838,7 +881,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_full, eps & 1, abort)))) break;
                 if (lane == 0) {
     #pragma unroll
-                    for (int cb = 0; cb < L::kBoxes; ++cb)
+                    for (int cb = 0; cb < L::kOBoxes; ++cb)
                         tma_store_4d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.h, U.b);
                     bulk_commit_group();
                 }
@@ -936,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // the peer's barriers exist before any multicast reaches them
     else
         __syncthreads();
-    static_assert(MODE == kPrefill || MODE == kVarlen || PAIR == 1, "packed rows run without K/V multicast");
+    static_assert(is_prefill(MODE) || MODE == kVarlen || PAIR == 1, "packed rows run without K/V multicast");
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
     // Inputs may come from the previous kernel in the stream, and outputs may
@@ -991,37 +1034,38 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// A bf16 tensor map over `rank` dimensions, dims[0] = d contiguous, the
-// others with element strides; boxes of 64 columns by box[1..] elements with
-// the 128-byte swizzle.  Coordinates outside the tensor read as zero (loads)
-// or are dropped (stores).  A dimension of extent 1 is never stepped, so it
-// gets a packed stride whatever the caller's.
-bool encode_bf16(EncodeTiledFn enc, CUtensorMap *map, const void *base, int rank, const int64_t *dims,
-                 const int64_t *strides, const uint32_t *box) {
+// A tensor map of bf16 (elem = 2) or e4m3 (elem = 1, as bytes) over `rank`
+// dimensions, dims[0] = d contiguous, the others with element strides; boxes
+// of 128 bytes of columns by box[1..] elements with the 128-byte swizzle.
+// Coordinates outside the tensor read as zero (loads) or are dropped
+// (stores).  A dimension of extent 1 is never stepped, so it gets a packed
+// stride whatever the caller's.
+bool encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int rank, const int64_t *dims,
+                const int64_t *strides, const uint32_t *box, int elem) {
     cuuint64_t gd[5], gs[4];
     cuuint32_t bx[5], es[5];
-    uint64_t packed = (uint64_t)dims[0] * 2;
+    uint64_t packed = (uint64_t)dims[0] * elem;
     for (int i = 0; i < rank; ++i) {
         gd[i] = (cuuint64_t)dims[i];
         bx[i] = box[i];
         es[i] = 1;
         if (i > 0) {
-            gs[i - 1] = dims[i] > 1 ? (cuuint64_t)strides[i] * 2 : (cuuint64_t)packed;
+            gs[i - 1] = dims[i] > 1 ? (cuuint64_t)strides[i] * elem : (cuuint64_t)packed;
             packed = (uint64_t)gs[i - 1] * (uint64_t)dims[i];
         }
     }
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bx, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+               const_cast<void *>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // [B, H, T, d] with element strides (sb, sh, st) as the 4-D map (d, T, H, B);
-// boxes of 64 columns x box_rows rows of one (batch, head).
+// boxes of 128 bytes of columns x box_rows rows of one (batch, head).
 bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int T, int H, int B, int64_t st,
-              int64_t sh, int64_t sb, int box_rows) {
+              int64_t sh, int64_t sb, int box_rows, int elem = 2) {
     const int64_t dims[4] = {d, T, H, B}, strides[4] = {1, st, sh, sb};
-    const uint32_t box[4] = {64, (uint32_t)box_rows, 1, 1};
-    return encode_bf16(enc, map, base, 4, dims, strides, box);
+    const uint32_t box[4] = {(uint32_t)(128 / elem), (uint32_t)box_rows, 1, 1};
+    return encode_map(enc, map, base, 4, dims, strides, box, elem);
 }
 
 // The query rows of one KV group as the 5-D map (d, group, Tq, Hkv, B): head
@@ -1031,17 +1075,17 @@ bool make_packed_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, cons
                      int64_t sb) {
     const int64_t dims[5] = {P.d, P.group, P.Tq, P.Hkv, P.B}, strides[5] = {1, sh, st, sh * P.group, sb};
     const uint32_t box[5] = {64, (uint32_t)P.group, (uint32_t)P.Tq, 1, 1};
-    return encode_bf16(enc, map, base, 5, dims, strides, box);
+    return encode_map(enc, map, base, 5, dims, strides, box, 2);
 }
 
 // The K and V maps; with Tk == 0 no key tile is ever loaded and the maps only
 // need to be valid (they then describe q).
-bool make_kv_maps(EncodeTiledFn enc, CUtensorMap *tk, CUtensorMap *tv, const Params &P, int box_rows) {
+bool make_kv_maps(EncodeTiledFn enc, CUtensorMap *tk, CUtensorMap *tv, const Params &P, int box_rows, int elem = 2) {
     if (P.Tk == 0)
-        return make_map(enc, tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, P.q_sb, box_rows) &&
-               make_map(enc, tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, P.q_sb, box_rows);
-    return make_map(enc, tk, P.k, P.d, P.Tk, P.Hkv, P.B, P.k_st, P.k_sh, P.k_sb, box_rows) &&
-           make_map(enc, tv, P.v, P.d, P.Tk, P.Hkv, P.B, P.v_st, P.v_sh, P.v_sb, box_rows);
+        return make_map(enc, tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, P.q_sb, box_rows, elem) &&
+               make_map(enc, tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, P.q_sb, box_rows, elem);
+    return make_map(enc, tk, P.k, P.d, P.Tk, P.Hkv, P.B, P.k_st, P.k_sh, P.k_sb, box_rows, elem) &&
+           make_map(enc, tv, P.v, P.d, P.Tk, P.Hkv, P.B, P.v_st, P.v_sh, P.v_sb, box_rows, elem);
 }
 
 // Streaming multiprocessors of the current device (cached per device).
@@ -1077,8 +1121,10 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
             ok = ok && make_map(enc, &tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR) &&
                  make_map(enc, &tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR);
     } else {
-        ok = make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM) &&
-             make_kv_maps(enc, &tk, &tv, P, kBN / PAIR) &&
+        // Q, K and V in the input type (bf16 or e4m3); O is bf16.
+        constexpr int kE = elem_bytes(MODE);
+        ok = make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM, kE) &&
+             make_kv_maps(enc, &tk, &tv, P, kBN / PAIR, kE) &&
              make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM);
     }
     if (!ok) return cudaErrorInvalidValue;
@@ -1215,6 +1261,12 @@ cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream) {
     const bool pair = (P.group % 2) == 0;
     if (P.d <= 64) return pair ? launch_d<64, 2, kVarlen>(P, stream) : launch_d<64, 1, kVarlen>(P, stream);
     return pair ? launch_d<128, 2, kVarlen>(P, stream) : launch_d<128, 1, kVarlen>(P, stream);
+}
+
+cudaError_t launch_fp8(const Params &P, cudaStream_t stream) {
+    // e4m3 rows of d <= 128 bytes: one 128-byte box per row, padded with zeros.
+    const bool pair = (P.group % 2) == 0;
+    return pair ? launch_d<128, 2, kPrefill8>(P, stream) : launch_d<128, 1, kPrefill8>(P, stream);
 }
 
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {

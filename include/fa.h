@@ -42,7 +42,12 @@
  * mantissa bits cleared (the part TF32 keeps) and x_lo = x - x_hi (a logit's
  * error ~2^-20 of sum |q_i k_i|); O = P V in bf16 as P_0 V_0 + P_0 V_1 +
  * P_1 V_0 with x_0 = bf16(x), x_1 = bf16(x - x_0) (~2^-17 of sum |p_j v_j|).
- * lse is fp32 in all three.
+ * FA_DTYPE_FP8_E4M3 reads e4m3 q/k/v (OCP FP8 E4M3, one byte each: the
+ * layout rows above in bytes), forms S = Q K^T and O = P V on the tensor cores
+ * (kind::f8f6f4, fp32 accumulators), keeps the softmax statistics in fp32,
+ * rounds P to e4m3 for the P.V product, and writes bf16 o.  Scaling of the
+ * inputs into e4m3's range is the caller's: a per-tensor descale of q and k
+ * folds into `scale`, and o is linear in v.  lse is fp32 in all four.
  *
  * Execution: asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  * stream); results are valid once the stream has synchronised.
@@ -58,7 +63,8 @@
  *                    even), d > 256 for fp32, bf16 d not a multiple of 8
  *                    or above 128 (rows must be 16-byte multiples for TMA),
  *                    FA_DTYPE_F32_TC d not a multiple of 4 or above 128, or
- *                    B*Hq*ceil(Tq/128) >= 2^31, Tq or Tk >= 2^30, pointers
+ *                    B*Hq*ceil(Tq/128) >= 2^31, FA_DTYPE_FP8_E4M3 d not a
+ *                    multiple of 16 or above 128, Tq or Tk >= 2^30, pointers
  *                    not 16-byte aligned.
  *   FA_ECUDA         a CUDA error while configuring or launching.
  * B*Hq*Tq == 0 is a no-op returning FA_OK.  Tk == 0 writes o = 0 and
@@ -85,7 +91,8 @@ typedef enum {
 typedef enum {
     FA_DTYPE_F32 = 0,
     FA_DTYPE_BF16 = 1,
-    FA_DTYPE_F32_TC = 2
+    FA_DTYPE_F32_TC = 2,
+    FA_DTYPE_FP8_E4M3 = 3
 } fa_dtype;
 
 /* The attention forward described above.  `dtype` is an fa_dtype value;
@@ -113,7 +120,8 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  *   FA_EUNSUPPORTED  bf16: a stride (of a dimension of extent > 1) that is
  *                    not a multiple of 8 elements (16 bytes, a TMA rule) or
  *                    reaches 2^40 bytes; FA_DTYPE_F32_TC: likewise with 4
- *                    elements; fp32: a stride that is odd.
+ *                    elements; FA_DTYPE_FP8_E4M3: 16 elements for q, k, v
+ *                    and 8 for the bf16 o; fp32: a stride that is odd.
  * Reading k or v through overlapping rows (a stride of 0 over the batch, say)
  * is allowed for FA_DTYPE_F32; the tensor-core paths need positive strides. */
 fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -95,7 +95,9 @@ CASES = [
     ("bf16 d = 136 (> 128)", dict(d=136, dtype=fa.FA_DTYPE_BF16), fa.FA_EUNSUPPORTED),
     ("fp32 tc d = 30 (not a multiple of 4)", dict(d=30, dtype=fa.FA_DTYPE_F32_TC), fa.FA_EUNSUPPORTED),
     ("fp32 tc d = 132 (> 128)", dict(d=132, dtype=fa.FA_DTYPE_F32_TC), fa.FA_EUNSUPPORTED),
-    ("unknown dtype 3", dict(dtype=3), fa.FA_EINVAL),
+    ("unknown dtype 4", dict(dtype=4), fa.FA_EINVAL),
+    ("e4m3 d = 24 (not a multiple of 16)", dict(d=24, dtype=fa.FA_DTYPE_FP8_E4M3), fa.FA_EUNSUPPORTED),
+    ("e4m3 d = 144 (> 128)", dict(d=144, dtype=fa.FA_DTYPE_FP8_E4M3), fa.FA_EUNSUPPORTED),
     ("Tk >= 2^30", dict(Tk=1 << 30), fa.FA_EUNSUPPORTED),
     ("Tq >= 2^30", dict(Tq=1 << 30, B=1, Hq=1, Hkv=1, d=2), fa.FA_EUNSUPPORTED),
 ]
@@ -161,6 +163,8 @@ def _strided(fa_mod, **kw):
     ("fp32 tc stride not a multiple of 4", dict(dtype=2, qs=(2048, 514, 64), os=(4096, 1024, 128)),
      "FA_EUNSUPPORTED"),
     ("fp32 tc zero batch stride on k", dict(dtype=2, ks=(0, 512, 64)), "FA_EUNSUPPORTED"),
+    ("e4m3 stride not a multiple of 16", dict(dtype=3, qs=(2048, 520, 64), os=(4096, 1024, 128)),
+     "FA_EUNSUPPORTED"),
 ])
 def test_strided_rejections(lib, case, kw, want):
     import exact_tiled_attention_flashattention_gb300 as fa_mod
@@ -182,6 +186,7 @@ def test_strided_bshd_layout_is_valid_up_to_launch(lib):
 @pytest.mark.parametrize("case,kw,want", [
     ("fp32 is not paged", dict(dtype=0), "FA_EUNSUPPORTED"),
     ("fp32 tc is not paged", dict(dtype=2), "FA_EUNSUPPORTED"),
+    ("e4m3 is not paged", dict(dtype=3), "FA_EUNSUPPORTED"),
     ("group * Tq > 128", dict(Tq=65), "FA_EUNSUPPORTED"),
     ("page size 48", dict(page_size=48), "FA_EUNSUPPORTED"),
     ("page size 4", dict(page_size=4), "FA_EUNSUPPORTED"),
@@ -211,6 +216,7 @@ def test_paged_rejections(lib, case, kw, want):
     ("Hq % Hkv", dict(Hq=6, Hkv=4), "FA_ESHAPE"),
     ("bf16 d = 100", dict(d=100), "FA_EUNSUPPORTED"),
     ("fp32 tc is not varlen", dict(dtype=2), "FA_EUNSUPPORTED"),
+    ("e4m3 is not varlen", dict(dtype=3), "FA_EUNSUPPORTED"),
 ])
 def test_varlen_rejections(lib, case, kw, want):
     import exact_tiled_attention_flashattention_gb300 as fa_mod
