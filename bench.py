@@ -278,8 +278,10 @@ def measure_decode(fa, dev, flush, local_rank):
 
 # FP32 SIMT peak of the GB300: 152 SMs x 128 FFMA lanes x 2 FLOP x 2.07 GHz.
 FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-# Dense TF32 against dense bf16 on the tensor cores (nominal 1.1 / 2.25 PF/s).
+# Dense TF32 and dense fp8 against dense bf16 on the tensor cores (nominal
+# 1.1 / 2.25 and 4.5 / 2.25 PF/s).
 TF32_OVER_BF16 = 1.1 / 2.25
+FP8_OVER_BF16 = 4.5 / 2.25
 
 
 def measure_other_paths(fa, dev, flush, peak_bf16):
@@ -290,10 +292,12 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
     as three TF32 products, P V as three bf16 products).  The f32tc ceiling:
     half the algorithmic FLOPs are Q K^T, done three times at the dense TF32
     rate (measured bf16 peak x 1.1 / 2.25), half are P V, done three times at
-    the bf16 rate; ceiling = 1 / (1.5 / R_tf32 + 1.5 / R_bf16)."""
+    the bf16 rate; ceiling = 1 / (1.5 / R_tf32 + 1.5 / R_bf16).  "e4m3" runs
+    e4m3 inputs (bf16 O) against the dense fp8 peak (measured bf16 x 2)."""
     import torch
     out = []
-    codes = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC}
+    codes = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC,
+             "e4m3": fa.FA_DTYPE_FP8_E4M3}
     tf32_peak = peak_bf16 * TF32_OVER_BF16
     tc_ceiling = 1.0 / (1.5 / tf32_peak + 1.5 / peak_bf16)
 
@@ -303,6 +307,8 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
         e = {"workload": name, "dtype": dtype, "ms": round(med, 4), "tflops": round(tf, 2)}
         if dtype == "f32":
             e["frac_of_fp32_simt_peak"] = round(tf / FP32_SIMT_PEAK_TFLOPS, 4)
+        elif dtype == "e4m3":
+            e["frac_of_fp8_peak"] = round(tf / (peak_bf16 * FP8_OVER_BF16), 4)
         elif dtype == "f32tc":
             e["tensor_ceiling_tflops"] = round(tc_ceiling, 1)
             e["frac_of_tensor_ceiling"] = round(tf / tc_ceiling, 4)
@@ -338,6 +344,37 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
                           0, 0, codes[dt], None)
 
             entry(name, dt, longctx, p.flops(), reps=5)
+        del q, k, v, o, lse
+
+    # e4m3 inputs: the 28-layer prefill and the long-context prefills, one call each
+    p = workloads.CONFIGS["prefill511_gqa16x8_d128_x28"].problem
+    layers = []
+    for layer in range(28):
+        q, k, v = workloads.qkv(layer, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float8_e4m3fn)
+        layers.append((q.to(dev), k.to(dev), v.to(dev),
+                       torch.empty((p.B, p.Hq, p.Tq, p.d), dtype=torch.bfloat16, device=dev),
+                       torch.empty((p.B, p.Hq, p.Tq), device=dev)))
+
+    def prefill_f8():
+        for q, k, v, o, lse in layers:
+            fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0, 0,
+                      0, codes["e4m3"], None)
+
+    entry("prefill511_gqa16x8_d128_x28", "e4m3", prefill_f8, 28 * p.flops(), reps=5)
+    del layers
+    for name in LONG_CONTEXT:
+        w = workloads.CONFIGS[name]
+        p = w.problem
+        q, k, v = [t.to(dev) for t in
+                   workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.float8_e4m3fn)]
+        o = torch.empty((p.B, p.Hq, p.Tq, p.d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((p.B, p.Hq, p.Tq), device=dev)
+
+        def longctx_f8():
+            fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, 0, 1, 0, None, None, 0, 0, 0,
+                      0, codes["e4m3"], None)
+
+        entry(name, "e4m3", longctx_f8, p.flops(), reps=5)
         del q, k, v, o, lse
 
     # additive-mask batch, fp32
@@ -656,11 +693,12 @@ def run_only(args, local_rank):
     torch.cuda.set_device(dev)
     w = {**workloads.CONFIGS, **workloads.DECODE}[args.only]
     p = w.problem
-    dt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
-    code = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC}[args.dtype]
+    dt = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}.get(args.dtype, torch.float32)
+    code = {"bf16": fa.FA_DTYPE_BF16, "f32": fa.FA_DTYPE_F32, "f32tc": fa.FA_DTYPE_F32_TC,
+            "e4m3": fa.FA_DTYPE_FP8_E4M3}[args.dtype]
     q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, dt)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if args.dtype == "e4m3" else dt, device=dev)
     lse = torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)
     def one_call():
         fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, int(p.causal), p.window,
@@ -695,8 +733,9 @@ def main():
     ap.add_argument("--only", choices=sorted({**workloads.CONFIGS, **workloads.DECODE}),
                     help="profiling driver: one workload only")
     ap.add_argument("--calls", type=int, default=3)
-    ap.add_argument("--dtype", choices=["bf16", "f32", "f32tc"], default="bf16",
-                    help="--only: bf16, fp32 on the SIMT cores, or fp32 as three TF32 tensor-core products")
+    ap.add_argument("--dtype", choices=["bf16", "f32", "f32tc", "e4m3"], default="bf16",
+                    help="--only: bf16, fp32 on the SIMT cores, fp32 on the tensor cores (three products per "
+                         "matrix product), or e4m3")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
