@@ -15,13 +15,13 @@ from __future__ import annotations
 import ctypes
 from pathlib import Path
 
-__all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_DTYPE_F32", "FA_DTYPE_BF16",
-           "FA_DTYPE_F32_TC", "FA_DTYPE_FP8_E4M3",
-           "FaError", "fa_fwd", "fa_last_error", "fa_version", "attention", "library_path", "load"]
+__all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_ETIMEOUT", "FA_DTYPE_F32",
+           "FA_DTYPE_BF16", "FA_DTYPE_F32_TC", "FA_DTYPE_FP8_E4M3", "FaError", "fa_fwd", "fa_last_error",
+           "fa_version", "fa_device_status", "fa_test_drop_arrive", "attention", "library_path", "load"]
 
-FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA = 0, 1, 2, 3, 4
+FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA, FA_ETIMEOUT = 0, 1, 2, 3, 4, 5
 FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F32_TC, FA_DTYPE_FP8_E4M3 = 0, 1, 2, 3
-_STATUS = {0: "FA_OK", 1: "FA_EINVAL", 2: "FA_ESHAPE", 3: "FA_EUNSUPPORTED", 4: "FA_ECUDA"}
+_STATUS = {0: "FA_OK", 1: "FA_EINVAL", 2: "FA_ESHAPE", 3: "FA_EUNSUPPORTED", 4: "FA_ECUDA", 5: "FA_ETIMEOUT"}
 
 _LIB_PATH = Path(__file__).resolve().parent / "libfa.so"
 _lib = None
@@ -64,6 +64,10 @@ def load():
     lib.fa_last_error.argtypes = []
     lib.fa_version.restype = ctypes.c_int
     lib.fa_version.argtypes = []
+    lib.fa_device_status.restype = ctypes.c_int
+    lib.fa_device_status.argtypes = [vp]
+    lib.fa_test_drop_arrive.restype = ctypes.c_int
+    lib.fa_test_drop_arrive.argtypes = [ctypes.c_int]
     _lib = lib
     return lib
 
@@ -91,6 +95,25 @@ def fa_last_error() -> str:
 
 def fa_version() -> int:
     return load().fa_version()
+
+
+def fa_device_status(stream=None, *, check=True) -> int:
+    """fa_device_status: FA_ETIMEOUT if a bounded wait in a tensor-core kernel
+    ran out since the previous check (raised as FaError when ``check``)."""
+    lib = load()
+    st = lib.fa_device_status(_stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+def fa_test_drop_arrive(enable: bool) -> int:
+    """Test hook: while enabled, CTA 0 of each tensor-core kernel skips one load."""
+    lib = load()
+    st = lib.fa_test_drop_arrive(1 if enable else 0)
+    if st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
 
 
 def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, scale, q_offset, causal, window, sinks, mask, mask_sb,

@@ -43,7 +43,30 @@ constexpr int64_t kMaxLen = int64_t(1) << 30;
 
 extern "C" const char *fa_last_error(void) { return g_last_error; }
 
-extern "C" int fa_version(void) { return 100; }
+extern "C" int fa_version(void) { return 101; }
+
+extern "C" fa_status fa_device_status(void *stream) {
+    g_last_error[0] = '\0';
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int tc5 = 0, tf32 = 0;
+    cudaError_t e = fa::bf16_watchdog(s, &tc5);
+    if (e == cudaSuccess) e = fa::f32tc_watchdog(s, &tf32);
+    if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
+    if (tc5 != 0 || tf32 != 0)
+        return fail(FA_ETIMEOUT, "a bounded wait ran out in the %s kernel since the last check; outputs of the calls "
+                                 "in between are not valid",
+                    tc5 != 0 && tf32 != 0 ? "bf16/e4m3 and fp32 tensor-core" : tc5 != 0 ? "bf16/e4m3" : "fp32 tensor-core");
+    return FA_OK;
+}
+
+extern "C" fa_status fa_test_drop_arrive(int enable) {
+    g_last_error[0] = '\0';
+    const int on = enable ? 1 : 0;
+    cudaError_t e = fa::bf16_set_drop_arrive(on);
+    if (e == cudaSuccess) e = fa::f32tc_set_drop_arrive(on);
+    if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
+    return FA_OK;
+}
 
 namespace {
 

@@ -73,6 +73,9 @@
 namespace fa {
 
 __device__ unsigned int g_watchdog = 0;
+// Test hook, zero unless a test sets it: CTA 0 then skips its first Q load,
+// so that the QK issuer's bounded wait runs out and the abort path runs.
+__device__ int g_drop_arrive = 0;
 
 namespace {
 
@@ -377,7 +380,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     volatile int *abort = &bar.abort;
     const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
     const Schedule sched = make_schedule<MODE, PAIR>(P);
-    int k_issued[kMaxStages] = {}, v_issued[kMaxStages] = {};
+    // Loads issued into each ring so far: a stage has a previous use once
+    // the ring has wrapped (kept as counters, not per-stage arrays, so that
+    // nothing here lives in local memory).
+    int k_loads = 0, v_loads = 0;
     int q_issued = 0;
     RingPos kput, vput;
     bool ok = true;
@@ -390,10 +396,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
 
         // Tile t of the unit into the next stage of a ring; the stage is
         // refilled once every CTA reading it released its previous use.
-        auto load_tile = [&](uint32_t ring, int stages, uint64_t *full, uint64_t *empty, int *issued, RingPos &pos,
+        auto load_tile = [&](uint32_t ring, int stages, uint64_t *full, uint64_t *empty, int &loads, RingPos &pos,
                              const CUtensorMap *map, int t) -> bool {
             const int st = pos.st;
-            if (issued[st] > 0 && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
+            if (loads >= stages && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
             mbar_arrive_expect_tx(&full[st], L::kKVBytes);  // halves from both CTAs
             const int key0 = (U.t_begin + t) * kBN;
             const int kvb = MODE == kVarlen ? 0 : U.b;  // varlen tensors have one batch
@@ -423,7 +429,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
                     tma_load_4d(dst, map, &full[st], c * L::kBoxCols, U.krow + key0, U.g, kvb);
             }
             }
-            ++issued[st];
+            ++loads;
             if (++pos.st == stages) {
                 pos.st = 0;
                 pos.ph ^= 1u;
@@ -431,16 +437,18 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             return true;
         };
         auto load_k = [&](int t) {
-            return load_tile(L::kKRing, L::kStages, bar.k_full, bar.k_empty, k_issued, kput, &tmK, t);
+            return load_tile(L::kKRing, L::kStages, bar.k_full, bar.k_empty, k_loads, kput, &tmK, t);
         };
         auto load_v = [&](int t) {
-            return load_tile(L::kVRing, L::kVStages, bar.v_full, bar.v_empty, v_issued, vput, &tmV, t);
+            return load_tile(L::kVRing, L::kVStages, bar.v_full, bar.v_empty, v_loads, vput, &tmV, t);
         };
         if (!(ok = load_k(0))) break;
         if (n > 1 && !(ok = load_k(1))) break;
         // Q of this unit, once the previous unit's S MMAs are done with the buffer.
         if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
-        if constexpr (MODE == kDecode || MODE == kPaged) {
+        if (q_issued == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0) {
+            // test hook: no Q load, no arrival on q_full
+        } else if constexpr (MODE == kDecode || MODE == kPaged) {
             // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
             mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
@@ -464,9 +472,14 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         // Drain: every copy issued above lands before shared memory goes away.
         int never = 0;
         if (q_issued > 0) mbar_wait(&bar.q_full, (q_issued - 1) & 1, &never, 200000000ull);
+        // Stage s of a ring of S stages after n loads was used (n + S - 1 - s) / S times.
         for (int s = 0; s < L::kStages; ++s) {
-            if (k_issued[s] > 0) mbar_wait(&bar.k_full[s], (k_issued[s] - 1) & 1, &never, 200000000ull);
-            if (v_issued[s] > 0) mbar_wait(&bar.v_full[s], (v_issued[s] - 1) & 1, &never, 200000000ull);
+            const int ku = (k_loads + L::kStages - 1 - s) / L::kStages;
+            if (ku > 0) mbar_wait(&bar.k_full[s], (ku - 1) & 1, &never, 200000000ull);
+        }
+        for (int s = 0; s < L::kVStages; ++s) {
+            const int vu = (v_loads + L::kVStages - 1 - s) / L::kVStages;
+            if (vu > 0) mbar_wait(&bar.v_full[s], (vu - 1) & 1, &never, 200000000ull);
         }
     }
 }
@@ -1252,6 +1265,20 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t bf16_watchdog(cudaStream_t stream, unsigned int *flag) {
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_watchdog, sizeof v, 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && v != 0)
+        e = cudaMemcpyToSymbolAsync(g_watchdog, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    *flag = v;
+    return e;
+}
+
+cudaError_t bf16_set_drop_arrive(int on) { return cudaMemcpyToSymbol(g_drop_arrive, &on, sizeof on); }
 
 cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream) {
     return P.d <= 64 ? launch_packed<64, kPaged>(P, stream) : launch_packed<128, kPaged>(P, stream);

@@ -56,6 +56,9 @@ namespace fa {
 
 // Set when a bounded wait of this kernel ran out.
 __device__ unsigned int g_watchdog_tc = 0;
+// Test hook, zero unless a test sets it: CTA 0 then skips its first chunk
+// load, so that the splitters' bounded wait runs out and the abort path runs.
+__device__ int g_drop_arrive_tc = 0;
 
 namespace {
 
@@ -169,13 +172,15 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUte
                                               uint8_t *smem, Barriers &bar) {
     using C = Cfg<D>;
     volatile int *abort = &bar.abort;
-    int uses[C::kSlots] = {};
+    int loads = 0;  // chunks issued: a slot has a previous use once the ring has wrapped
     Pos<C::kSlots> p;
     for_each_chunk<D>(U.n_tiles, [&](bool is_v, int t, int c) {
-        if (uses[p.st] > 0 && !mbar_wait(&bar.empty[p.st], p.ph ^ 1u, abort)) return false;
+        if (loads >= C::kSlots && !mbar_wait(&bar.empty[p.st], p.ph ^ 1u, abort)) return false;
         uint8_t *slot = smem + C::kRing + p.st * kSlotBytes;
         const int key0 = (U.t_begin + t) * kBN;
-        if (!is_v) {
+        if (loads == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive_tc) != 0) {
+            // test hook: no load, no arrival on full
+        } else if (!is_v) {
             mbar_arrive_expect_tx(&bar.full[p.st], kBN * 128);
             tma_load_4d(slot, &tmK, &bar.full[p.st], c * 32, key0, U.g, U.b);
         } else {
@@ -184,14 +189,17 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUte
             for (int bx = 0; bx < D / 32; ++bx)
                 tma_load_4d(slot + bx * (C::kVK * 128), &tmV, &bar.full[p.st], bx * 32, key0 + c * C::kVK, U.g, U.b);
         }
-        ++uses[p.st];
+        ++loads;
         p.advance();
         return true;
     });
-    // Every copy issued lands before shared memory goes away.
+    // Every copy issued lands before shared memory goes away: slot s was used
+    // (loads + kSlots - 1 - s) / kSlots times.
     int never = 0;
-    for (int s = 0; s < C::kSlots; ++s)
-        if (uses[s] > 0) mbar_wait(&bar.full[s], (uses[s] - 1) & 1, &never, 200000000ull);
+    for (int s = 0; s < C::kSlots; ++s) {
+        const int uses = (loads + C::kSlots - 1 - s) / C::kSlots;
+        if (uses > 0) mbar_wait(&bar.full[s], (uses - 1) & 1, &never, 200000000ull);
+    }
 }
 
 // Splitters (128 threads, t = 0..127).  Raw tiles use the 128-byte swizzle:
@@ -701,6 +709,20 @@ cudaError_t launch_tc(const Params &P, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t f32tc_watchdog(cudaStream_t stream, unsigned int *flag) {
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_watchdog_tc, sizeof v, 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && v != 0)
+        e = cudaMemcpyToSymbolAsync(g_watchdog_tc, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    *flag = v;
+    return e;
+}
+
+cudaError_t f32tc_set_drop_arrive(int on) { return cudaMemcpyToSymbol(g_drop_arrive_tc, &on, sizeof on); }
 
 cudaError_t launch_f32_tc(const Params &P, cudaStream_t stream) {
     return P.d <= 64 ? launch_tc<64>(P, stream) : launch_tc<128>(P, stream);

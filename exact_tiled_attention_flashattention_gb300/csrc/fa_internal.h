@@ -63,4 +63,12 @@ cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream);
 cudaError_t launch_f32_varlen(const Params &P, cudaStream_t stream);
 
+// Device watchdog words: nonzero once a bounded wait of the kernel ran out.
+// Read (after the stream's work) and cleared.
+cudaError_t bf16_watchdog(cudaStream_t stream, unsigned int *flag);
+cudaError_t f32tc_watchdog(cudaStream_t stream, unsigned int *flag);
+// Test hooks: make CTA 0 of the next launches skip one load (see the kernels).
+cudaError_t bf16_set_drop_arrive(int on);
+cudaError_t f32tc_set_drop_arrive(int on);
+
 }  // namespace fa

@@ -85,7 +85,8 @@ typedef enum {
     FA_EINVAL = 1,
     FA_ESHAPE = 2,
     FA_EUNSUPPORTED = 3,
-    FA_ECUDA = 4
+    FA_ECUDA = 4,
+    FA_ETIMEOUT = 5
 } fa_status;
 
 typedef enum {
@@ -192,6 +193,22 @@ const char *fa_last_error(void);
 
 /* ABI version of this library (major * 100 + minor). */
 int fa_version(void);
+
+/* Failure detection.  Every wait inside the tensor-core kernels (bf16, e4m3,
+ * fp32 on the tensor cores) is bounded (two seconds); a wait that runs out
+ * makes the kernel abandon its work, drain its copies and MMAs, free its
+ * tensor memory and return, and sets a device status word, so that the
+ * context stays usable.  fa_device_status synchronises `stream` (a
+ * cudaStream_t, NULL = legacy default stream), reads and clears those words,
+ * and returns FA_ETIMEOUT if a wait ran out since the previous check (the
+ * outputs of the calls in between are then not valid), FA_OK otherwise, or
+ * FA_ECUDA if the reads fail. */
+fa_status fa_device_status(void *stream);
+
+/* Test hook for the path above, off by default: while enabled, CTA 0 of each
+ * tensor-core kernel launch skips one of its loads, so that a bounded wait
+ * runs out.  Not for production use. */
+fa_status fa_test_drop_arrive(int enable);
 
 #ifdef __cplusplus
 }
