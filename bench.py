@@ -301,10 +301,16 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
     tf32_peak = peak_bf16 * TF32_OVER_BF16
     tc_ceiling = 1.0 / (1.5 / tf32_peak + 1.5 / peak_bf16)
 
-    def entry(name, dtype, fn, flops, reps=10):
+    def entry(name, dtype, fn, flops, reps=10, nbytes=None):
         med, _ = time_graph(fn, reps, flush)
         tf = flops / (med / 1e3) / 1e12
         e = {"workload": name, "dtype": dtype, "ms": round(med, 4), "tflops": round(tf, 2)}
+        if nbytes is not None:
+            # HBM-bound workloads: algorithmic bytes against the measured copy rate
+            gbs = nbytes / (med / 1e3) / 1e9
+            hbm, kind = _hbm_peak()
+            e.update({"algorithmic_bytes": int(nbytes), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm, 4),
+                      "hbm_peak_kind": kind})
         if dtype == "f32":
             e["frac_of_fp32_simt_peak"] = round(tf / FP32_SIMT_PEAK_TFLOPS, 4)
         elif dtype == "e4m3":
@@ -423,11 +429,15 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
         code = codes[dt]
         tdt = torch.bfloat16 if dt == "bf16" else torch.float32
         q, k, v = workloads.qkv(w.seeds[0], p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, tdt)
-        chunks, flops = [], 0
+        chunks, flops, nbytes = [], 0, 0
+        esz = 2 if dt == "bf16" else 4
         for start, n in workloads.chunk_ranges(p.Tq, w.extra["chunk"]):
             cp = workloads.Problem(p.B, p.Hq, p.Hkv, n, start + n, p.d, causal=True, window=p.window,
                                    q_offset=start)
             flops += cp.flops()
+            # Q and O of the chunk, lse, and the keys its rows can see (the window)
+            keys = start + n - max(0, start - p.window + 1)
+            nbytes += 2 * p.B * p.Hq * n * p.d * esz + p.B * p.Hq * n * 4 + 2 * p.B * p.Hkv * keys * p.d * esz
             chunks.append((start, n, q[:, :, start:start + n].contiguous().to(dev),
                            k[:, :, :start + n].contiguous().to(dev), v[:, :, :start + n].contiguous().to(dev),
                            torch.empty((p.B, p.Hq, n, p.d), dtype=tdt, device=dev),
@@ -438,7 +448,7 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
                 fa.fa_fwd(qc, kc, vc, oc, lc, p.B, p.Hq, p.Hkv, n, start + n, p.d, p.sm_scale, start, 1, p.window,
                           z, None, 0, 0, 0, 0, code, None)
 
-        entry("window128_sinks_gqa32x4_d64_chunked", dt, chunked, flops)
+        entry("window128_sinks_gqa32x4_d64_chunked", dt, chunked, flops, nbytes=nbytes)
     return out
 
 
