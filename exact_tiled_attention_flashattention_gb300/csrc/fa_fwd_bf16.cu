@@ -442,27 +442,40 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         auto load_v = [&](int t) {
             return load_tile(L::kVRing, L::kVStages, bar.v_full, bar.v_empty, v_loads, vput, &tmV, t);
         };
-        if (!(ok = load_k(0))) break;
-        if (n > 1 && !(ok = load_k(1))) break;
-        // Q of this unit, once the previous unit's S MMAs are done with the buffer.
-        if (q_issued > 0 && !(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
-        if (q_issued == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0) {
-            // test hook: no Q load, no arrival on q_full
-        } else if constexpr (MODE == kDecode || MODE == kPaged) {
-            // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
-            mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
+        // Q of this unit into the Q buffer (the caller has made sure that the
+        // previous unit's S MMAs are done with it).
+        auto load_q = [&]() {
+            if (q_issued == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0) {
+                // test hook: no Q load, no arrival on q_full
+            } else if constexpr (MODE == kDecode || MODE == kPaged) {
+                // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
+                mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
-            for (int c = 0; c < L::kBoxes; ++c)
-                tma_load_5d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, 0, 0, U.g,
-                            U.b);
+                for (int c = 0; c < L::kBoxes; ++c)
+                    tma_load_5d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, 0, 0, U.g,
+                                U.b);
+            } else {
+                mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
+#pragma unroll
+                for (int c = 0; c < L::kBoxes; ++c)
+                    tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, U.qrow + U.r0, U.h,
+                                MODE == kVarlen ? 0 : U.b);
+            }
+            ++q_issued;
+        };
+        if (q_issued == 0) {
+            // The CTA's first unit: Q first, as its first S needs Q and K_0
+            // and all three come from DRAM.
+            load_q();
+            if (!(ok = load_k(0))) break;
+            if (n > 1 && !(ok = load_k(1))) break;
         } else {
-            mbar_arrive_expect_tx(&bar.q_full, L::kQBytes);
-#pragma unroll
-            for (int c = 0; c < L::kBoxes; ++c)
-                tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, U.qrow + U.r0, U.h,
-                            MODE == kVarlen ? 0 : U.b);
+            // K_0 and K_1 first: Q waits for the previous unit's last S.
+            if (!(ok = load_k(0))) break;
+            if (n > 1 && !(ok = load_k(1))) break;
+            if (!(ok = mbar_wait(&bar.q_empty, (q_issued - 1) & 1, abort))) break;
+            load_q();
         }
-        ++q_issued;
         for (int j = 0; j < n && ok; ++j) {
             ok = load_v(j);
             if (ok && j + 2 < n) ok = load_k(j + 2);
@@ -865,19 +878,19 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             {
                 const int col0 = half * kHD;  // this thread's first O column
                 uint8_t *box = smem + L::kOStage + (col0 / 64) * (kBM * kSwRowBytes) + row * kSwRowBytes;
-    #pragma unroll
+#pragma unroll
                 for (int cc = 0; cc < kHD; cc += 32) {
                     uint32_t ov[32];
                     if (n > 0) {
                         tmem_load_pair32<kHD>(o_addr + cc, ov);
                     } else {
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = 0u;
                     }
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint32_t w[4];
-    #pragma unroll
+#pragma unroll
                         for (int k = 0; k < 4; ++k)
                             w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
                                               __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
@@ -893,7 +906,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (warp == 0) {
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.ep_full, eps & 1, abort)))) break;
                 if (lane == 0) {
-    #pragma unroll
+#pragma unroll
                     for (int cb = 0; cb < L::kOBoxes; ++cb)
                         tma_store_4d(&tmO, smem + L::kOStage + cb * (kBM * kSwRowBytes), cb * 64, U.r0, U.h, U.b);
                     bulk_commit_group();
