@@ -397,20 +397,21 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
 
         entry("mask_b4h8_t1024_d96", dt, masked, p.flops())
 
-    # variable-length causal prefill batches, bf16 and fp32
+    # variable-length causal prefill batches, bf16, e4m3 and fp32
     for name, w in workloads.VARLEN.items():
         B, Hq, Hkv, d = w["B"], w["Hq"], w["Hkv"], w["d"]
         lens = workloads.paged_lengths(w["seed"], B, w["lo"], w["hi"])
         total = sum(lens)
         cu = torch.tensor([0] + list(__import__("itertools").accumulate(lens)), dtype=torch.int32, device=dev)
         flops = sum(workloads.Problem(1, Hq, Hkv, L, L, d).flops() for L in lens)
-        for dt, code in (("bf16", fa.FA_DTYPE_BF16), ("f32", fa.FA_DTYPE_F32)):
-            tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+        for dt in ("bf16", "e4m3", "f32"):
+            code = codes[dt]
+            tdt = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}.get(dt, torch.float32)
             g = torch.Generator().manual_seed(w["seed"])
             qv = torch.randn((total, Hq, d), generator=g).to(tdt).to(dev)
             kv = torch.randn((total, Hkv, d), generator=g).to(tdt).to(dev)
             vv = torch.randn((total, Hkv, d), generator=g).to(tdt).to(dev)
-            ov = torch.empty_like(qv)
+            ov = torch.empty(qv.shape, dtype=torch.bfloat16 if dt == "e4m3" else tdt, device=dev)
             lv = torch.empty((Hq, total), dtype=torch.float32, device=dev)
 
             def varlen():

@@ -237,19 +237,22 @@ def fa_fwd_varlen(q, k, v, o, lse, B, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, to
 
 def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, scale=None, causal=True,
                      window=0, sinks=None, stream=None):
-    """Packed sequences: q [total_q, Hq, d], k/v [total_k, Hkv, d] (fp32 or
-    bf16, d contiguous), cu_seqlens_* int32 [B+1] CUDA tensors.  Returns o
-    [total_q, Hq, d] and lse [Hq, total_q]."""
+    """Packed sequences: q [total_q, Hq, d], k/v [total_k, Hkv, d] (fp32,
+    bf16 or float8_e4m3fn, d contiguous), cu_seqlens_* int32 [B+1] CUDA
+    tensors.  Returns o [total_q, Hq, d] (q's dtype; bf16 for e4m3) and lse
+    [Hq, total_q]."""
     import torch
     total_q, Hq, d = q.shape
     total_k, Hkv = k.shape[0], k.shape[1]
     B = cu_seqlens_q.numel() - 1
-    dt = FA_DTYPE_F32 if q.dtype == torch.float32 else FA_DTYPE_BF16
-    if q.dtype not in (torch.float32, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k and v must share a dtype, fp32 or bf16")
+    codes = {torch.float32: FA_DTYPE_F32, torch.bfloat16: FA_DTYPE_BF16, torch.float8_e4m3fn: FA_DTYPE_FP8_E4M3}
+    if q.dtype not in codes or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share a dtype: fp32, bf16 or float8_e4m3fn")
+    dt = codes[q.dtype]
     if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
-    o = torch.empty((total_q, Hq, d), dtype=q.dtype, device=q.device)
+    o = torch.empty((total_q, Hq, d), dtype=torch.bfloat16 if dt == FA_DTYPE_FP8_E4M3 else q.dtype,
+                    device=q.device)
     lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     sc = (1.0 / d ** 0.5) if scale is None else scale
     fa_fwd_varlen(q, k, v, o, lse, B, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q,

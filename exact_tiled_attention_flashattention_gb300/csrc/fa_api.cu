@@ -360,11 +360,13 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
     if (B == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;  // no query row
     if (!q || !o || !cu_seqlens_q || !cu_seqlens_k) return fail(FA_EINVAL, "q, o or a cu_seqlens table is NULL");
     if (total_k > 0 && (!k || !v)) return fail(FA_EINVAL, "k or v is NULL with total_k > 0");
-    if (dtype == FA_DTYPE_F32_TC || dtype == FA_DTYPE_FP8_E4M3)
-        return fail(FA_EUNSUPPORTED, "the varlen path is fp32 (SIMT) or bf16 only");
+    if (dtype == FA_DTYPE_F32_TC)
+        return fail(FA_EUNSUPPORTED, "the varlen path is fp32 (SIMT), bf16 or e4m3 only");
     if (d == 0 || (d & 1)) return fail(FA_EUNSUPPORTED, "d=%lld: d must be even and positive", (long long)d);
     if (dtype == FA_DTYPE_F32 && d > 256)
         return fail(FA_EUNSUPPORTED, "fp32 path supports d <= 256 (got %lld)", (long long)d);
+    if (dtype == FA_DTYPE_FP8_E4M3 && (d % 16 != 0 || d > 128))
+        return fail(FA_EUNSUPPORTED, "e4m3 path supports d a multiple of 16 up to 128 (got %lld)", (long long)d);
     if (dtype == FA_DTYPE_BF16 && (d % 8 != 0 || d > 128))
         return fail(FA_EUNSUPPORTED, "bf16 path supports d a multiple of 8 up to 128 (got %lld)", (long long)d);
     if (total_q >= kMaxLen || total_k >= kMaxLen || max_seqlen_q > total_q)
@@ -372,18 +374,23 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
     if (B >= (int64_t(1) << 24) || B * Hq >= (int64_t(1) << 31)) return fail(FA_EUNSUPPORTED, "too many sequences");
     if (!aligned16(q) || !aligned16(o) || (total_k > 0 && (!aligned16(k) || !aligned16(v))))
         return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
-    const int64_t m = dtype == FA_DTYPE_BF16 ? 8 : 2;
+    // Tensor maps: 16-byte stride multiples (o is bf16 with e4m3 inputs).
+    const bool tma = dtype != FA_DTYPE_F32;
+    const int64_t in_bytes = dtype == FA_DTYPE_FP8_E4M3 ? 1 : (dtype == FA_DTYPE_BF16 ? 2 : 4);
+    const int64_t m = tma ? 16 / in_bytes : 2, mo = tma ? 8 : 2;
     const bool kv = total_k > 0;
-    if (!strides_multiple(1, Hq, total_q, 0, q_sh, q_st, m) || !strides_multiple(1, Hq, total_q, 0, o_sh, o_st, m) ||
+    if (!strides_multiple(1, Hq, total_q, 0, q_sh, q_st, m) || !strides_multiple(1, Hq, total_q, 0, o_sh, o_st, mo) ||
         (kv && (!strides_multiple(1, Hkv, total_k, 0, k_sh, k_st, m) ||
                 !strides_multiple(1, Hkv, total_k, 0, v_sh, v_st, m))))
         return fail(FA_EUNSUPPORTED, "strides must be multiples of %lld elements for this dtype", (long long)m);
-    if (dtype == FA_DTYPE_BF16) {
+    if (tma) {
         const int64_t st[8] = {q_sh, q_st, k_sh, k_st, v_sh, v_st, o_sh, o_st};
         const int64_t ext[8] = {Hq, total_q, Hkv, total_k, Hkv, total_k, Hq, total_q};
         for (int i = 0; i < 8; ++i) {
-            if (st[i] > (int64_t(1) << 39) - 1) return fail(FA_EUNSUPPORTED, "a stride reaches 2^40 bytes");
-            if (ext[i] > 1 && st[i] <= 0) return fail(FA_EUNSUPPORTED, "bf16 strides must be positive (tensor maps)");
+            const int64_t lim = ((int64_t(1) << 40) / (i >= 6 ? 2 : in_bytes)) - 1;  // elements; o is bf16
+            if (st[i] > lim) return fail(FA_EUNSUPPORTED, "a stride reaches 2^40 bytes");
+            if (ext[i] > 1 && st[i] <= 0)
+                return fail(FA_EUNSUPPORTED, "strides must be positive for this dtype (tensor maps)");
         }
     }
 
@@ -417,7 +424,9 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
     P.total_q = (int)total_q;
     P.total_k = (int)total_k;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dtype == FA_DTYPE_F32 ? fa::launch_f32_varlen(P, s) : fa::launch_bf16_varlen(P, s);
+    cudaError_t e = dtype == FA_DTYPE_F32    ? fa::launch_f32_varlen(P, s)
+                    : dtype == FA_DTYPE_BF16 ? fa::launch_bf16_varlen(P, s)
+                                             : fa::launch_fp8_varlen(P, s);
     if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
     return FA_OK;
 }

@@ -112,9 +112,13 @@ constexpr int kMaxStages = 6;
 //   kPrefill8 kPrefill with e4m3 Q, K and V: the MMAs are kind::f8f6f4 (32
 //             elements per K step), P is rounded to e4m3 (four per tensor-
 //             memory column), O stays bf16.
-constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3, kPrefill8 = 4;
+//   kVarlen8  kVarlen with e4m3 Q, K and V, as kPrefill8.
+constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3, kPrefill8 = 4, kVarlen8 = 5;
 __host__ __device__ constexpr bool is_prefill(int mode) { return mode == kPrefill || mode == kPrefill8; }
-__host__ __device__ constexpr int elem_bytes(int mode) { return mode == kPrefill8 ? 1 : 2; }  // Q, K, V
+__host__ __device__ constexpr bool is_varlen(int mode) { return mode == kVarlen || mode == kVarlen8; }
+__host__ __device__ constexpr int elem_bytes(int mode) {  // Q, K, V
+    return (mode == kPrefill8 || mode == kVarlen8) ? 1 : 2;
+}
 
 template <int D, int MODE>
 struct SmemLayout {
@@ -190,7 +194,7 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     U.bh = U.b * P.Hq + U.h;
     U.g = U.h / P.group;
     U.r0 = qt * kBM;
-    if constexpr (MODE == kVarlen) {
+    if constexpr (is_varlen(MODE)) {
         // offsets clamped into the tensors: a malformed table cannot reach outside them
         const int q0 = min(max(__ldg(P.cu_q + U.b), 0), P.total_q);
         const int q1 = min(max(__ldg(P.cu_q + U.b + 1), q0), P.total_q);
@@ -402,7 +406,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             if (loads >= stages && !mbar_wait(&empty[st], pos.ph ^ 1u, abort)) return false;
             mbar_arrive_expect_tx(&full[st], L::kKVBytes);  // halves from both CTAs
             const int key0 = (U.t_begin + t) * kBN;
-            const int kvb = MODE == kVarlen ? 0 : U.b;  // varlen tensors have one batch
+            const int kvb = is_varlen(MODE) ? 0 : U.b;  // varlen tensors have one batch
             if constexpr (MODE == kPaged) {
                 // Runs of min(page_size, 128) keys, each from its page; keys
                 // past the sequence (or past the table) read page -1: zeros.
@@ -459,7 +463,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
 #pragma unroll
                 for (int c = 0; c < L::kBoxes; ++c)
                     tma_load_4d(smem + L::kQ + c * (kBM * kSwRowBytes), &tmQ, &bar.q_full, c * L::kBoxCols, U.qrow + U.r0, U.h,
-                                MODE == kVarlen ? 0 : U.b);
+                                is_varlen(MODE) ? 0 : U.b);
             }
             ++q_issued;
         };
@@ -634,11 +638,11 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         // Keys and query position of the unit's sequence: the call's, or the
         // sequence's own with paged K/V (kernel parameters stay in the
         // constant bank otherwise).
-        constexpr bool kSeq = MODE == kPaged || MODE == kVarlen;  // per-sequence lengths
+        constexpr bool kSeq = MODE == kPaged || is_varlen(MODE);  // per-sequence lengths
         const int uTk = kSeq ? U.Tk : P.Tk;
         const int uq0 = kSeq ? U.q_offset : P.q_offset;
-        const int uTq = MODE == kVarlen ? U.Tq : P.Tq;
-        if (MODE == kVarlen && U.r0 >= uTq) continue;  // a tile past the sequence's rows
+        const int uTq = is_varlen(MODE) ? U.Tq : P.Tq;
+        if (is_varlen(MODE) && U.r0 >= uTq) continue;  // a tile past the sequence's rows
         int64_t p_first = (int64_t)uq0 + U.r0, p_last = (int64_t)uq0 + min(U.r0 + kBM, uTq) - 1;
         if constexpr (MODE == kDecode || MODE == kPaged) {
             live = row < P.group * P.Tq;
@@ -662,7 +666,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         const bool has_sink = P.sinks != nullptr;
         // The sink joins the sum once: in the first CTA of a split key range.
         const bool sink_here =
-            has_sink && half == 0 && (is_prefill(MODE) || MODE == kVarlen || (int)blockIdx.x % P.splits == 0);
+            has_sink && half == 0 && (is_prefill(MODE) || is_varlen(MODE) || (int)blockIdx.x % P.splits == 0);
         float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;  // log2 units
         float l = sink_here ? 1.f : 0.f;                                // this thread's share of the sum
         const float *mrow = (!kSeq && P.mask != nullptr && live)
@@ -839,7 +843,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             }
             if (n > 0) tc_fence_before();
             if (live && half == 0) stats[row] = make_float2(m, lt);
-        } else if constexpr (MODE == kVarlen) {
+        } else if constexpr (is_varlen(MODE)) {
             // The sequence's rows only (a 128-row store would reach into the
             // next sequence): this thread's half of the row, 16-byte stores.
 #pragma unroll
@@ -1005,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // the peer's barriers exist before any multicast reaches them
     else
         __syncthreads();
-    static_assert(is_prefill(MODE) || MODE == kVarlen || PAIR == 1, "packed rows run without K/V multicast");
+    static_assert(is_prefill(MODE) || is_varlen(MODE) || PAIR == 1, "packed rows run without K/V multicast");
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
     // Inputs may come from the previous kernel in the stream, and outputs may
@@ -1137,18 +1141,17 @@ cudaError_t launch_d(const Params &P, cudaStream_t stream) {
     // O store drops them.  A variable-length batch is one [total, H, d]
     // tensor (a batch of one) with the sequences along the rows.
     bool ok;
-    if (MODE == kVarlen) {
-        ok = make_map(enc, &tq, P.q, P.d, P.total_q, P.Hq, 1, P.q_st, P.q_sh, 0, kBM) &&
+    constexpr int kE = elem_bytes(MODE);  // Q, K and V in bf16 or e4m3; O is bf16
+    if (is_varlen(MODE)) {
+        ok = make_map(enc, &tq, P.q, P.d, P.total_q, P.Hq, 1, P.q_st, P.q_sh, 0, kBM, kE) &&
              make_map(enc, &to, P.o, P.d, P.total_q, P.Hq, 1, P.o_st, P.o_sh, 0, kBM);
         if (P.total_k > 0)
-            ok = ok && make_map(enc, &tk, P.k, P.d, P.total_k, P.Hkv, 1, P.k_st, P.k_sh, 0, kBN / PAIR) &&
-                 make_map(enc, &tv, P.v, P.d, P.total_k, P.Hkv, 1, P.v_st, P.v_sh, 0, kBN / PAIR);
+            ok = ok && make_map(enc, &tk, P.k, P.d, P.total_k, P.Hkv, 1, P.k_st, P.k_sh, 0, kBN / PAIR, kE) &&
+                 make_map(enc, &tv, P.v, P.d, P.total_k, P.Hkv, 1, P.v_st, P.v_sh, 0, kBN / PAIR, kE);
         else
-            ok = ok && make_map(enc, &tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR) &&
-                 make_map(enc, &tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR);
+            ok = ok && make_map(enc, &tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR, kE) &&
+                 make_map(enc, &tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR, kE);
     } else {
-        // Q, K and V in the input type (bf16 or e4m3); O is bf16.
-        constexpr int kE = elem_bytes(MODE);
         ok = make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM, kE) &&
              make_kv_maps(enc, &tk, &tv, P, kBN / PAIR, kE) &&
              make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM);
@@ -1307,6 +1310,11 @@ cudaError_t launch_fp8(const Params &P, cudaStream_t stream) {
     // e4m3 rows of d <= 128 bytes: one 128-byte box per row, padded with zeros.
     const bool pair = (P.group % 2) == 0;
     return pair ? launch_d<128, 2, kPrefill8>(P, stream) : launch_d<128, 1, kPrefill8>(P, stream);
+}
+
+cudaError_t launch_fp8_varlen(const Params &P, cudaStream_t stream) {
+    const bool pair = (P.group % 2) == 0;
+    return pair ? launch_d<128, 2, kVarlen8>(P, stream) : launch_d<128, 1, kVarlen8>(P, stream);
 }
 
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {

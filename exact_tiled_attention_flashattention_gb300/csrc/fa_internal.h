@@ -59,6 +59,7 @@ cudaError_t launch_f32_tc(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream);
 // e4m3 Q, K, V (kind::f8f6f4 MMAs, P rounded to e4m3), bf16 O.
 cudaError_t launch_fp8(const Params &P, cudaStream_t stream);
+cudaError_t launch_fp8_varlen(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream);
 cudaError_t launch_f32_varlen(const Params &P, cudaStream_t stream);

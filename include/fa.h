@@ -177,7 +177,9 @@ fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, 
  * [0, total], so a malformed table cannot make the kernels reach outside the
  * tensors.  No additive mask.  Errors as fa_fwd_strided, plus FA_EINVAL for a
  * NULL cu_seqlens table and FA_EUNSUPPORTED when max_seqlen_q > total_q or
- * dtype is FA_DTYPE_F32_TC (fp32 batches run on FA_DTYPE_F32 here). */
+ * dtype is FA_DTYPE_F32_TC (fp32 batches run on FA_DTYPE_F32 here).  With
+ * FA_DTYPE_FP8_E4M3, q, k and v are e4m3 (strides multiples of 16 elements)
+ * and o is bf16 (strides multiples of 8). */
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                         int64_t B, int64_t Hq, int64_t Hkv, int64_t d,
                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

@@ -216,7 +216,7 @@ def test_paged_rejections(lib, case, kw, want):
     ("Hq % Hkv", dict(Hq=6, Hkv=4), "FA_ESHAPE"),
     ("bf16 d = 100", dict(d=100), "FA_EUNSUPPORTED"),
     ("fp32 tc is not varlen", dict(dtype=2), "FA_EUNSUPPORTED"),
-    ("e4m3 is not varlen", dict(dtype=3), "FA_EUNSUPPORTED"),
+    ("e4m3 varlen d = 24", dict(dtype=3, d=24), "FA_EUNSUPPORTED"),
 ])
 def test_varlen_rejections(lib, case, kw, want):
     import exact_tiled_attention_flashattention_gb300 as fa_mod

@@ -7,11 +7,11 @@ import torch
 
 import exact_tiled_attention_flashattention_gb300 as fa
 import workloads
-from parity import compare, oracle_attention
+from parity import compare, compare_fp8, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
-DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
 DEV = torch.device("cuda", 0)
 
 
@@ -49,16 +49,19 @@ def _run(dt, lens_q, lens_k, Hq, Hkv, d, seed, **kw):
         torch.cuda.synchronize()
         assert torch.equal(oi, o1.cpu()) and torch.equal(li, l1.cpu()), f"sequence {i}"
         eo, el = oracle_attention(qs[i], ks[i], vs[i], q_offset=off, **kw)
-        compare(oi, li, eo, el, DT[dt], f"varlen {dt} seq {i} ({tq}x{tk})")
+        if dt == "e4m3":
+            compare_fp8(oi, li, eo, el, vs[i], Hq // Hkv, f"varlen {dt} seq {i} ({tq}x{tk})")
+        else:
+            compare(oi, li, eo, el, DT[dt], f"varlen {dt} seq {i} ({tq}x{tk})")
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("dt", ["bf16", "f32", "e4m3"])
 def test_varlen_causal_prefill(dt):
     lens = [1, 100, 511, 129, 1000]
     _run(dt, lens, lens, 8, 4, 64, 90, scale=0.125, causal=True)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("dt", ["bf16", "f32", "e4m3"])
 def test_varlen_chunks_and_empty(dt):
     # queries as the last positions of longer key ranges; one empty sequence
     lq = [200, 0, 37, 300]
@@ -66,10 +69,11 @@ def test_varlen_chunks_and_empty(dt):
     _run(dt, lq, lk, 12, 4, 128, 91, scale=128 ** -0.5, causal=True)
 
 
-def test_varlen_window_sinks_bf16():
+@pytest.mark.parametrize("dt", ["bf16", "e4m3"])
+def test_varlen_window_sinks(dt):
     lens = [400, 260, 1500]
     z = workloads.sinks(93, 6).to(DEV)
-    _run("bf16", lens, lens, 6, 2, 96, 92, scale=0.1, causal=True, window=150, sinks=z)
+    _run(dt, lens, lens, 6, 2, 96, 92, scale=0.1, causal=True, window=150, sinks=z)
 
 
 def test_varlen_noncausal_f32():
