@@ -1300,26 +1300,41 @@ cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream) {
     return P.d <= 64 ? launch_packed<64, kPaged>(P, stream) : launch_packed<128, kPaged>(P, stream);
 }
 
+// A CTA pair shares every K/V tile between two query heads of one KV head
+// (each CTA loads half and multicasts it), at the price of cluster barriers
+// and of the two CTAs moving in step.  That pays off once a unit walks many
+// key tiles; on shorter walks the barriers cost more than the shared loads
+// save (measured on GB300, causal, d = 128: pairs 4-5 % slower at 511 and
+// 2044 keys, 0.6 % faster at 8192).
+constexpr int64_t kPairMinKeys = 4096;
+
+bool use_pair(const Params &P, bool varlen) {
+    if (P.group % 2 != 0) return false;
+    int64_t span = P.Tk;  // keys the longest unit can see
+    if (!varlen && P.causal && (int64_t)P.q_offset + P.Tq < span) span = (int64_t)P.q_offset + P.Tq;
+    if (P.window > 0 && (int64_t)P.window + kBM < span) span = (int64_t)P.window + kBM;
+    return span >= kPairMinKeys;
+}
+
 cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream) {
-    const bool pair = (P.group % 2) == 0;
+    const bool pair = use_pair(P, true);
     if (P.d <= 64) return pair ? launch_d<64, 2, kVarlen>(P, stream) : launch_d<64, 1, kVarlen>(P, stream);
     return pair ? launch_d<128, 2, kVarlen>(P, stream) : launch_d<128, 1, kVarlen>(P, stream);
 }
 
 cudaError_t launch_fp8(const Params &P, cudaStream_t stream) {
     // e4m3 rows of d <= 128 bytes: one 128-byte box per row, padded with zeros.
-    const bool pair = (P.group % 2) == 0;
+    const bool pair = use_pair(P, false);
     return pair ? launch_d<128, 2, kPrefill8>(P, stream) : launch_d<128, 1, kPrefill8>(P, stream);
 }
 
 cudaError_t launch_fp8_varlen(const Params &P, cudaStream_t stream) {
-    const bool pair = (P.group % 2) == 0;
+    const bool pair = use_pair(P, true);
     return pair ? launch_d<128, 2, kVarlen8>(P, stream) : launch_d<128, 1, kVarlen8>(P, stream);
 }
 
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
-    // Pairs of query heads share a KV head when the group size is even.
-    const bool pair = (P.group % 2) == 0;
+    const bool pair = use_pair(P, false);
     // d is a multiple of 8 up to 128: the 64- or 128-column kernel, padded.
     // All query rows of a KV group in one tile: the packed-row kernel.
     if ((int64_t)P.group * P.Tq <= kBM)
