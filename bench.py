@@ -12,7 +12,9 @@ value     causal-adjusted TFLOP/s over the K timed steps: 4*d*(visible
           write) before every timed step, outside the events.
 e2e       the same metric through the public call with host buffers: every
           step copies the 28 layers' Q/K/V from pinned host memory, runs the
-          28 calls and copies O and lse back, all inside the events.
+          28 calls and copies O and lse back, all inside the events.  The
+          copies move chunks of 7 layers on two streams of their own, so
+          that copies in, calls and copies out overlap.
 roofline  the dominant kernel (the bf16 tcgen05 kernel) against the measured
           dense bf16 tensor peak: algorithmic FLOPs per launch / average
           launch duration (step time / 28 launches, so launch gaps count).
@@ -42,6 +44,7 @@ WORKLOAD = "prefill511_gqa16x8_d128_x28"
 METRIC = "attention fwd TFLOP/s (causal-adj) and % of GB300 dense peak; ms per prefill"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
+E2E_CHUNK = 7  # layers per host<->device copy in the end-to-end measurement
 LONG_CONTEXT = ["longctx2044_gqa16x8_d128", "longctx8192_gqa16x8_d128", "longctx32768_gqa16x8_d128"]
 
 
@@ -591,23 +594,58 @@ def run_fa(args, rank, world, local_rank):
         dist.barrier()
     sampler.stop()
 
-    # End to end through the public call with host buffers.
-    host_out = [(torch.empty(o.shape, dtype=o.dtype, pin_memory=True),
-                 torch.empty(l.shape, dtype=l.dtype, pin_memory=True)) for o, l in outs]
-    h2d = sum(t.numel() * t.element_size() for trio in layers_host for t in trio)
-    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in host_out)
+    # End to end through the public call with host buffers.  Every step copies
+    # the 28 layers' q, k, v in from pinned host memory, runs the 28 calls and
+    # reads every o and lse back.  Inputs sit in one pinned buffer (per layer
+    # [q | k | v]), outputs in two (o, lse), moved in chunks of E2E_CHUNK
+    # layers on streams of their own: chunk c + 1 comes in while chunk c
+    # computes and chunk c - 1 goes out.  A chunk's input region is refilled
+    # only after its previous calls ran, its outputs rewritten only after
+    # their previous read-back.
+    nq, nk = layers_host[0][0].numel(), layers_host[0][1].numel()
+    per_in = nq + 2 * nk
+    no, nl = outs[0][0].numel(), outs[0][1].numel()
+    hin = torch.empty(L * per_in, dtype=torch.bfloat16, pin_memory=True)
+    for i, (qh, kh, vh) in enumerate(layers_host):
+        hin[i * per_in:i * per_in + nq].copy_(qh.reshape(-1))
+        hin[i * per_in + nq:i * per_in + nq + nk].copy_(kh.reshape(-1))
+        hin[i * per_in + nq + nk:(i + 1) * per_in].copy_(vh.reshape(-1))
+    din = torch.empty(L * per_in, dtype=torch.bfloat16, device=dev)
+    hout_o = torch.empty(L * no, dtype=torch.bfloat16, pin_memory=True)
+    hout_l = torch.empty(L * nl, dtype=torch.float32, pin_memory=True)
+    dout_o = torch.empty(L * no, dtype=torch.bfloat16, device=dev)
+    dout_l = torch.empty(L * nl, dtype=torch.float32, device=dev)
+    qs, ks = layers_host[0][0].shape, layers_host[0][1].shape
+    e2e_views = [(din[i * per_in:i * per_in + nq].view(qs), din[i * per_in + nq:i * per_in + nq + nk].view(ks),
+                  din[i * per_in + nq + nk:(i + 1) * per_in].view(ks),
+                  dout_o[i * no:(i + 1) * no].view(outs[i][0].shape), dout_l[i * nl:(i + 1) * nl].view(outs[i][1].shape))
+                 for i in range(L)]
+    h2d = hin.numel() * hin.element_size()
+    d2h = hout_o.numel() * hout_o.element_size() + hout_l.numel() * hout_l.element_size()
+    chunks = [(c0, min(L, c0 + E2E_CHUNK)) for c0 in range(0, L, E2E_CHUNK)]
+    s_c = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_run = [torch.cuda.Event() for _ in chunks]
+    ev_back = [torch.cuda.Event() for _ in chunks]
 
     def e2e_step():
-        for i in range(L):
-            qh, kh, vh = layers_host[i]
-            qd, kd, vd = layers_dev[i]
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            o, lse = outs[i]
-            call(i, qd, kd, vd, o, lse)
-            host_out[i][0].copy_(o, non_blocking=True)
-            host_out[i][1].copy_(lse, non_blocking=True)
+        for c, (c0, c1) in enumerate(chunks):
+            s_in.wait_event(ev_run[c])  # the chunk's previous calls have read their inputs
+            with torch.cuda.stream(s_in):
+                din[c0 * per_in:c1 * per_in].copy_(hin[c0 * per_in:c1 * per_in], non_blocking=True)
+            ev_in[c].record(s_in)
+            s_c.wait_event(ev_in[c])
+            s_c.wait_event(ev_back[c])  # the chunk's previous outputs have been read back
+            for i in range(c0, c1):
+                q, k, v, o, lse = e2e_views[i]
+                call(i, q, k, v, o, lse)
+            ev_run[c].record(s_c)
+            s_out.wait_event(ev_run[c])
+            with torch.cuda.stream(s_out):
+                hout_o[c0 * no:c1 * no].copy_(dout_o[c0 * no:c1 * no], non_blocking=True)
+                hout_l[c0 * nl:c1 * nl].copy_(dout_l[c0 * nl:c1 * nl], non_blocking=True)
+            ev_back[c].record(s_out)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -615,11 +653,19 @@ def run_fa(args, rank, world, local_rank):
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(s_c)
+    s_in.wait_stream(s_c)
     for _ in range(args.steps):
         e2e_step()
-    e1.record()
+    s_c.wait_stream(s_out)
+    e1.record(s_c)
     torch.cuda.synchronize()
+    # The read-back is the attention output: the first and last layers' o and
+    # lse equal the graph-timed calls' bit for bit.
+    for i in (0, L - 1):
+        if not (torch.equal(hout_o[i * no:(i + 1) * no], outs[i][0].reshape(-1).cpu()) and
+                torch.equal(hout_l[i * nl:(i + 1) * nl], outs[i][1].reshape(-1).cpu())):
+            raise RuntimeError(f"end-to-end read-back of layer {i} differs from the device result")
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
 
     # Long-context causal prefill at T = 2044, 8192, 32768 (bf16).  "ms": one
@@ -679,7 +725,8 @@ def run_fa(args, rank, world, local_rank):
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(job_throughput(world, flops_step, args.steps, e2e_s), 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(1e3 * e2e_s / args.steps, 4)},
+                "ms_per_step": round(1e3 * e2e_s / args.steps, 4),
+                "overlap": f"copies in, calls and copies out on three streams, {E2E_CHUNK} layers per copy"},
         "gpu_launches": L * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_burst, 4), "traffic": traffic,
