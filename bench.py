@@ -18,7 +18,12 @@ e2e       the same metric through the public call with host buffers: every
 roofline  the dominant kernel (the bf16 tcgen05 kernel) against the measured
           dense bf16 tensor peak: algorithmic FLOPs per launch / average
           launch duration (step time / 28 launches, so launch gaps count).
-cpu_baseline  the float64 oracle on the host cores on a bounded sample.
+cpu_baseline  the float64 oracle on the host cores on a bounded sample; with
+          the long-context runs also 128 rows of each long workload, their
+          time and its extrapolation to every row (labelled as such).
+long_context  bf16 causal prefill at T = 2044, 8192, 32768: one call and a
+          sequence of calls, with the count of exponentials (one per visible
+          pair) and the ex2 results per clock per SM that the time implies.
 
 --impl reference times the oracle itself (the only reference there is) on
 the host cores, each step one layer of the same workload.
@@ -187,11 +192,18 @@ def measure_long_context(fa, dev, flush, name, peak_burst, peak_sustained, local
     per_call = seq_med / n_seq
     tf = lp.flops() / (med / 1e3) / 1e12
     tf_seq = lp.flops() / (per_call / 1e3) / 1e12
+    # One exponential per visible (row, key) pair: an SFU-load check, as
+    # results per clock per SM at the sampled clock (MUFU ex2 gives 25-32).
+    exps = lp.flops() // (4 * lp.d)
+    clk = sampler.summary()
+    mhz = clk.get("sm_mhz") or 2070.0
+    ex2_rate = exps / (per_call / 1e3) / torch.cuda.get_device_properties(dev).multi_processor_count / (mhz * 1e6)
     return {"workload": name, "T": lp.Tq, "ms": round(med, 4), "tflops": round(tf, 1),
+            "exps": exps, "ex2_per_clk_per_sm_in_sequence": round(ex2_rate, 2),
             "frac_of_measured_peak": round(tf / peak_burst, 4),
             "ms_per_call_in_sequence": round(per_call, 4), "calls_in_sequence": n_seq,
             "tflops_in_sequence": round(tf_seq, 1), "frac_in_sequence": round(tf_seq / peak_burst, 4),
-            "frac_in_sequence_of_sustained": round(tf_seq / peak_sustained, 4), "clocks": sampler.summary()}
+            "frac_in_sequence_of_sustained": round(tf_seq / peak_sustained, 4), "clocks": clk}
 
 
 def _hbm_peak():
@@ -478,6 +490,32 @@ def time_oracle_layers(max_seconds: float, max_layers: int = 28):
     return flops, secs, layers, threads
 
 
+def time_oracle_long(name: str):
+    """The oracle on a row sample of a long-context workload: 128 evenly
+    spaced query rows of every head (widening to float64 outside the timed
+    region).  Returns the sampled time and its extrapolation to all
+    rows by visible (row, key) pairs, labelled as such."""
+    import numpy as np
+    import torch
+    import oracle
+    lp = workloads.CONFIGS[name].problem
+    w = workloads.CONFIGS[name]
+    q, k, v = workloads.qkv(w.seeds[0], lp.B, lp.Hq, lp.Hkv, lp.Tq, lp.Tk, lp.d, torch.bfloat16)
+    qn, kn, vn = (np.ascontiguousarray(t.float().numpy(), dtype=np.float64) for t in (q, k, v))
+    stride = max(1, lp.Tq // 128)
+    rows = np.arange(0, lp.Tq, stride, dtype=np.int64)
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.get().attention(qn, kn, vn, lp.sm_scale, causal=True, rows=rows, threads=threads)
+    secs = time.perf_counter() - t0
+    sampled_pairs = int(np.minimum(rows + 1, lp.Tk).sum())  # causal, q_offset 0: row i sees i + 1 keys
+    all_pairs = lp.flops() // (4 * lp.d * lp.B * lp.Hq)
+    fl = 4 * lp.d * lp.B * lp.Hq * sampled_pairs
+    return {"workload": name, "sample": f"every {stride}th row ({rows.size} rows) of every head",
+            "seconds": round(secs, 3), "tflops": round(fl / secs / 1e12, 4), "cores": threads,
+            "extrapolated_full_s": round(secs * all_pairs / sampled_pairs, 1)}
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: each step is one layer of the
     workload (full rows) on all host cores."""
@@ -693,6 +731,8 @@ def run_fa(args, rank, world, local_rank):
         cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"layers 0..{nl - 1} of 28 of the same workload, all rows, float64 oracle "
                          f"({secs:.1f} s)"}
+        if not args.skip_long:
+            cpu["long_context"] = [time_oracle_long(n) for n in LONG_CONTEXT]
 
     if dist is not None:
         dist.barrier()
