@@ -182,9 +182,10 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
             }
         if (B > 0x7fffffff || Hq > 0x7fffffff) return fail(FA_EUNSUPPORTED, "B and H must fit 31 bits");
     }
-    // One CTA per 128-row query tile of each (batch, head).
-    if (dtype == FA_DTYPE_F32_TC && ((Tq + 127) / 128) * B * Hq > 0x7fffffff)
-        return fail(FA_EUNSUPPORTED, "tensor-core fp32 path: B*Hq*ceil(Tq/128) must be below 2^31");
+    // The tensor-core kernels index 128-row query tiles of each (batch, head)
+    // as 31-bit unit numbers.
+    if (tma && ((Tq + 127) / 128) * B * Hq > 0x7fffffff)
+        return fail(FA_EUNSUPPORTED, "tensor-core paths: B*Hq*ceil(Tq/128) must be below 2^31");
 
     fa::Params P;
     std::memset(&P, 0, sizeof P);

@@ -181,18 +181,15 @@ template <int PAIR, int MODE>
 __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
     Unit U;
     const int nqt = (P.Tq + kBM - 1) / kBM;
-    const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
-    const int qt = nqt - 1 - u / per_qt;
-    const int r = u % per_qt;
-    if (PAIR == 2) {
-        U.b = r / (P.Hq / 2);
-        U.h = 2 * (r % (P.Hq / 2)) + rank;
-    } else {
-        U.b = r / P.Hq;
-        U.h = r % P.Hq;
-    }
+    // Divisions by launch constants: multiply-high and shift (fast_div.h).
+    const int qpos = (int)P.fd_per_qt.div((uint32_t)u);
+    const int qt = nqt - 1 - qpos;
+    const int r = u - qpos * (int)P.fd_per_qt.d;
+    U.b = (int)P.fd_heads.div((uint32_t)r);  // fd_heads: Hq, or Hq / 2 with a CTA pair
+    const int hr = r - U.b * (int)P.fd_heads.d;
+    U.h = PAIR == 2 ? 2 * hr + rank : hr;
     U.bh = U.b * P.Hq + U.h;
-    U.g = U.h / P.group;
+    U.g = (int)P.fd_group.div((uint32_t)U.h);
     U.r0 = qt * kBM;
     if constexpr (is_varlen(MODE)) {
         // offsets clamped into the tensors: a malformed table cannot reach outside them
@@ -236,9 +233,9 @@ __device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
 template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const Params &P) {
     Unit U;
-    const int cid = (int)blockIdx.x / P.splits, rank = (int)blockIdx.x % P.splits;
-    U.b = cid / P.Hkv;
-    U.g = cid % P.Hkv;
+    const int cid = (int)P.fd_splits.div(blockIdx.x), rank = (int)blockIdx.x - cid * P.splits;
+    U.b = (int)P.fd_hkv.div((uint32_t)cid);
+    U.g = cid - U.b * P.Hkv;
     U.h = U.g * P.group;
     U.bh = U.b * P.Hq + U.h;
     U.r0 = 0;
@@ -261,7 +258,7 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
     U.n_tiles = 0;
     if (khi > klo) {
         const int tb = (int)(klo / kBN), te = (int)((khi + kBN - 1) / kBN);
-        const int chunk = (te - tb + P.splits - 1) / P.splits;
+        const int chunk = (int)P.fd_splits.div((uint32_t)(te - tb + P.splits - 1));
         const int b0 = tb + rank * chunk, b1 = min(te, b0 + chunk);
         if (b1 > b0) {
             U.t_begin = b0;
@@ -646,9 +643,10 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         int64_t p_first = (int64_t)uq0 + U.r0, p_last = (int64_t)uq0 + min(U.r0 + kBM, uTq) - 1;
         if constexpr (MODE == kDecode || MODE == kPaged) {
             live = row < P.group * P.Tq;
-            const int hl = live ? row % P.group : 0;
+            const int iq = (int)P.fd_group.div((uint32_t)row);  // row = i * group + hl
+            const int hl = live ? row - iq * P.group : 0;
             h = U.g * P.group + hl;
-            i = live ? row / P.group : 0;
+            i = live ? iq : 0;
             p_first = uq0;
             p_last = (int64_t)uq0 + P.Tq - 1;
         } else {
@@ -666,7 +664,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         const bool has_sink = P.sinks != nullptr;
         // The sink joins the sum once: in the first CTA of a split key range.
         const bool sink_here =
-            has_sink && half == 0 && (is_prefill(MODE) || is_varlen(MODE) || (int)blockIdx.x % P.splits == 0);
+            has_sink && half == 0 && (is_prefill(MODE) || is_varlen(MODE) || P.fd_splits.mod(blockIdx.x) == 0);
         float m = has_sink ? __ldg(P.sinks + h) * kLog2e : -INFINITY;  // log2 units
         float l = sink_here ? 1.f : 0.f;                                // this thread's share of the sum
         const float *mrow = (!kSeq && P.mask != nullptr && live)
@@ -872,7 +870,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             }
             if (n > 0) tc_fence_before();
             if (live && P.lse != nullptr && half == 0)
-                P.lse[(int64_t)U.h * P.total_q + U.qrow + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+                P.lse[(int64_t)U.h * P.total_q + U.qrow + i] = lt > 0.f ? (m + lg2_approx(lt)) * kLn2 : -INFINITY;
         } else {
             if (threadIdx.x == 0) {
                 bulk_wait_read_all();
@@ -882,27 +880,28 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             {
                 const int col0 = half * kHD;  // this thread's first O column
                 uint8_t *box = smem + L::kOStage + (col0 / 64) * (kBM * kSwRowBytes) + row * kSwRowBytes;
+                // All of the thread's O columns in one tensor-memory load.
+                uint32_t ov[kHD];
+                if (n > 0) {
+                    if constexpr (kHD == 64)
+                        tmem_load_pair64<kHD>(o_addr, ov);
+                    else
+                        tmem_load_pair32<kHD>(o_addr, ov);
+                    tc_fence_before();
+                } else {
 #pragma unroll
-                for (int cc = 0; cc < kHD; cc += 32) {
-                    uint32_t ov[32];
-                    if (n > 0) {
-                        tmem_load_pair32<kHD>(o_addr + cc, ov);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = 0u;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
-                                              __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
-                        const int chunk = ((col0 % 64 + cc) / 8 + e) ^ (row & 7);
-                        *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                    for (int e = 0; e < kHD; ++e) ov[e] = 0u;
                 }
-                if (n > 0) tc_fence_before();
+#pragma unroll
+                for (int e = 0; e < kHD / 8; ++e) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        w[k] = cvt_bf16x2(__uint_as_float(ov[8 * e + 2 * k]) * inv,
+                                          __uint_as_float(ov[8 * e + 2 * k + 1]) * inv);
+                    const int chunk = ((col0 % 64) / 8 + e) ^ (row & 7);
+                    *reinterpret_cast<uint4 *>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
             }
             fence_proxy_async_smem();  // the TMA store reads what this thread wrote
             __syncwarp();
@@ -918,7 +917,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             }
             ++eps;
             if (i < P.Tq && P.lse != nullptr && half == 0)
-                P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+                P.lse[(int64_t)U.bh * P.Tq + i] = lt > 0.f ? (m + lg2_approx(lt)) * kLn2 : -INFINITY;
         }
         if (n > 0) ++units;
     }
@@ -937,13 +936,13 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
 template <int D>
 __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
     using L = SmemLayout<D, kDecode>;
-    const int S = P.splits, rank = (int)blockIdx.x % S, cid = (int)blockIdx.x / S;
+    const int S = P.splits, cid = (int)P.fd_splits.div(blockIdx.x), rank = (int)blockIdx.x - cid * S;
     const int R = P.group * P.Tq;
     const uint32_t op0 = smem_u32(smem + L::kKRing), st0 = smem_u32(smem + L::kVRing);
-    const int b = cid / P.Hkv, g = cid % P.Hkv;
+    const int b = (int)P.fd_hkv.div((uint32_t)cid), g = cid - b * P.Hkv;
     for (int e = rank * kThreads + (int)threadIdx.x; e < R * P.d; e += S * kThreads) {
-        const int row = e / P.d, col = e - row * P.d;
-        const int h = g * P.group + row % P.group, i = row / P.group;  // row = i * group + (h - g group)
+        const int row = (int)P.fd_d.div((uint32_t)e), col = e - row * P.d;
+        const int i = (int)P.fd_group.div((uint32_t)row), h = g * P.group + (row - i * P.group);  // row = i * group + (h - g group)
         float M = -INFINITY;
         for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ld_cluster_f32(map_to_rank(st0 + row * 8, sp)));
         float lsum = 0.f, acc = 0.f;
@@ -957,7 +956,7 @@ __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         static_cast<__nv_bfloat16 *>(P.o)[b * P.o_sb + h * P.o_sh + i * P.o_st + col] = __float2bfloat16_rn(acc * inv);
         if (col == 0 && P.lse != nullptr)
-            P.lse[((int64_t)b * P.Hq + h) * P.Tq + i] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+            P.lse[((int64_t)b * P.Hq + h) * P.Tq + i] = lsum > 0.f ? (M + lg2_approx(lsum)) * kLn2 : -INFINITY;
     }
 }
 
@@ -1132,7 +1131,11 @@ int sm_count() {
 }
 
 template <int D, int PAIR, int MODE>
-cudaError_t launch_d(const Params &P, cudaStream_t stream) {
+cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
+    Params P = P0;
+    P.fd_per_qt = FastDiv::make((uint32_t)(PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq));
+    P.fd_heads = FastDiv::make((uint32_t)(PAIR == 2 ? P.Hq / 2 : P.Hq));
+    P.fd_group = FastDiv::make((uint32_t)P.group);
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     CUtensorMap tq, tk, tv, to;
@@ -1275,6 +1278,10 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
                 break;
             }
     P.splits = S;
+    P.fd_splits = FastDiv::make((uint32_t)S);
+    P.fd_hkv = FastDiv::make((uint32_t)P.Hkv);
+    P.fd_group = FastDiv::make((uint32_t)P.group);
+    P.fd_d = FastDiv::make((uint32_t)P.d);
     cfg.gridDim = dim3((unsigned)(units * S));
     attr[1].val.clusterDim.x = (unsigned)S;
     return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, P);

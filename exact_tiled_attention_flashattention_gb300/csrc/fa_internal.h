@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "fast_div.h"
+
 namespace fa {
 
 // One validated call of fa_fwd, in the form the kernels read it.
@@ -39,6 +41,10 @@ struct Params {
     // v; its queries are its last positions.  Tq / Tk hold the maxima.
     const int *cu_q, *cu_k;
     int total_q, total_k;
+    // Divisors of the tcgen05 kernel's index arithmetic, set by its launchers:
+    // units per query tile, heads per unit row (Hq, or Hq / 2 with CTA
+    // pairs), the GQA group, the split count, Hkv and d.
+    FastDiv fd_per_qt, fd_heads, fd_group, fd_splits, fd_hkv, fd_d;
 };
 
 // Visible key range [lo, hi) of query position p (absolute) among Tk keys,

@@ -629,6 +629,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// log2 on the MUFU unit (the lse of a row: x >= 2^-8 there, no subnormals).
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------- launch / register control
 
 // 32-byte global store of eight 32-bit words; the address must be 32-byte aligned.

@@ -62,10 +62,11 @@
  *   FA_EUNSUPPORTED  d odd or 0 ("Fused attention and softmax": d must be
  *                    even), d > 256 for fp32, bf16 d not a multiple of 8
  *                    or above 128 (rows must be 16-byte multiples for TMA),
- *                    FA_DTYPE_F32_TC d not a multiple of 4 or above 128, or
- *                    B*Hq*ceil(Tq/128) >= 2^31, FA_DTYPE_FP8_E4M3 d not a
- *                    multiple of 16 or above 128, Tq or Tk >= 2^30, pointers
- *                    not 16-byte aligned.
+ *                    FA_DTYPE_F32_TC d not a multiple of 4 or above 128,
+ *                    FA_DTYPE_FP8_E4M3 d not a multiple of 16 or above 128,
+ *                    B*Hq*ceil(Tq/128) >= 2^31 on the tensor-core dtypes
+ *                    (bf16, F32_TC, e4m3), Tq or Tk >= 2^30, pointers not
+ *                    16-byte aligned.
  *   FA_ECUDA         a CUDA error while configuring or launching.
  * B*Hq*Tq == 0 is a no-op returning FA_OK.  Tk == 0 writes o = 0 and
  * lse = -inf (or the sink).  fa_last_error() describes the last non-OK
