@@ -689,11 +689,18 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], sb.ph, abort)))) break;
             tc_fence_after();
             uint32_t sr[kHK];
-            tmem_load_pair64<kHK>(s_addr, sr);
+            // Interior tiles take the maximum of the thread's raw scores from
+            // the load itself; boundary tiles mask first and reduce below.
+            const bool interior = j >= ti_lo && j < ti_hi;  // warp-uniform
+            float raw_max = 0.f;
+            if (interior)
+                raw_max = tmem_load_pair64_max<kHK>(s_addr, sr);
+            else
+                tmem_load_pair64<kHK>(s_addr, sr);
             float *s = reinterpret_cast<float *>(sr);
 
             float cs = c;  // multiplier from s[] to log2 units for this tile
-            if (j < ti_lo || j >= ti_hi) {
+            if (!interior) {
                 const int k0 = (U.t_begin + j) * kBN + half * kHK;  // this thread's first key
                 // The row's visible keys among this thread's: [elo, ehi) (clamped).
                 const int elo = min(max(vlo - k0, 0), kHK), ehi = min(max(vhi - k0, 0), kHK);
@@ -721,7 +728,10 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 }
             }
             float bm;  // tile max of s[] * cs over the whole row, in log2 units
-            {
+            if (interior) {
+                bm = raw_max * cs;
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));  // the row's other half
+            } else {
                 static_assert(kHK == 64, "max chains assume 64 keys per thread");
                 float mx[8];  // eight independent chains of three-input max
 #pragma unroll
