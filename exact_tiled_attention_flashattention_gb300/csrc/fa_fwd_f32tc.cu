@@ -456,10 +456,16 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, uin
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort)))) break;
         tc_fence_after();
         uint32_t sr[kHK];
-        tmem_load_pair64<kHK>(s_addr, sr);
+        // Interior tiles: the row maximum comes with the load (tcgen05.ld.red).
+        const bool interior = j >= ti_lo && j < ti_hi;  // warp-uniform
+        float raw_max = 0.f;
+        if (interior)
+            raw_max = tmem_load_pair64_max<kHK>(s_addr, sr);
+        else
+            tmem_load_pair64<kHK>(s_addr, sr);
         float *s = reinterpret_cast<float *>(sr);
         float cs = c;
-        if (j < ti_lo || j >= ti_hi) {
+        if (!interior) {
             const int k0 = (U.t_begin + j) * kBN + half * kHK;
             const int elo = min(max(vlo - k0, 0), kHK), ehi = min(max(vhi - k0, 0), kHK);
             if (mrow != nullptr) {
@@ -480,7 +486,10 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, uin
             }
         }
         float bm;
-        {
+        if (interior) {
+            bm = raw_max * cs;
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        } else {
             float mx[8];
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);
