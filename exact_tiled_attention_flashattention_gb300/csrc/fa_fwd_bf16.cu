@@ -7,9 +7,10 @@
 //
 //   S_t = Q K_t^T          tcgen05.mma, Q and K_t from shared memory (TMA,
 //                          128-byte swizzle), fp32 accumulator in TMEM
-//   P_t = 2^(S_t c - m)    softmax warps: tcgen05.ld of S_t, row max, ex2,
-//                          row sum; P rounded to bf16 and tcgen05.st back into
-//                          the first 64 columns of S_t's buffer
+//   P_t = 2^(S_t c - m)    softmax warps: tcgen05.ld of S_t (with the row max
+//                          from the load on interior tiles), ex2, row sum; P
+//                          rounded to bf16 and tcgen05.st back into the first
+//                          64 columns of S_t's buffer
 //   O  += P_t V_t          tcgen05.mma, A = P_t from TMEM, B = V_t (MN-major)
 //
 // S has three buffers in tensor memory and two threads issue the MMAs: one
@@ -32,8 +33,9 @@
 // K_0, K_1 and Q load while the current unit finishes, its first S tiles run
 // while the softmax warps write the current unit's output.
 //
-// K/V sharing: when the GQA group size is even, the two query heads of a KV
-// head at the same rows run as a cluster of two CTAs.  Each CTA loads half of
+// K/V sharing: when the GQA group size is even and a unit can walk 4096 keys
+// or more, the two query heads of a KV head at the same rows run as a cluster
+// of two CTAs.  Each CTA loads half of
 // every K/V tile (64 of its 128 rows) with a multicast TMA that lands in both
 // CTAs' shared memory, and a ring slot is refilled only after both CTAs'
 // tensor cores released it (a multicast tcgen05.commit arrives on the slot's
