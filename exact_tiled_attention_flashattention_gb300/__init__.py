@@ -89,6 +89,31 @@ def _stream(s):
     return s.cuda_stream or None
 
 
+def _check_tensors(dev, **tensors):
+    """The tensor wrappers pass raw addresses to the kernels, so every tensor
+    argument must live on the CUDA device ``dev`` (a host tensor's address
+    would reach the kernels as if it were device memory).  Integers (device
+    addresses) and None pass through."""
+    if dev.type != "cuda":
+        raise ValueError(f"q must be a CUDA tensor (got one on {dev})")
+    for name, t in tensors.items():
+        if t is None or isinstance(t, int):
+            continue
+        if t.device != dev:
+            raise ValueError(f"{name} must be a CUDA tensor on {dev} (got one on {t.device})")
+
+
+def _check_f32(name, t, min_numel=0):
+    """sinks and mask are read as float32 by the kernels."""
+    import torch
+    if t is None or isinstance(t, int):
+        return
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32 (got {t.dtype})")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} must hold at least {min_numel} elements (got {t.numel()})")
+
+
 def fa_last_error() -> str:
     return load().fa_last_error().decode()
 
@@ -157,6 +182,11 @@ def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=N
     import torch
     B, Hq, Tq, d = q.shape
     Hkv, Tk = k.shape[1], k.shape[2]
+    _check_tensors(q.device, k=k, v=v, out=out, lse_out=lse_out, sinks=sinks, mask=mask)
+    _check_f32("sinks", sinks, Hq)
+    _check_f32("mask", mask)
+    if isinstance(sinks, torch.Tensor) and not sinks.is_contiguous():
+        raise ValueError("sinks must be contiguous [Hq]")
     if q.dtype == torch.float32:
         dt = FA_DTYPE_F32_TC if fp32_tc else FA_DTYPE_F32
     elif q.dtype == torch.bfloat16:
@@ -173,14 +203,16 @@ def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=N
     o_dtype = torch.bfloat16 if dt == FA_DTYPE_FP8_E4M3 else q.dtype
     if out is not None and out.dtype != o_dtype:
         raise TypeError(f"out must be {o_dtype}")
-    o = out if out is not None else torch.empty((B, Hq, Tq, d), dtype=o_dtype, device=q.device)
-    if lse_out is not None and not lse_out.is_contiguous():
-        raise ValueError("lse_out must be contiguous [B, Hq, Tq]")
-    lse = lse_out if lse_out is not None else (
-        torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if with_lse else None)
-    sc = (1.0 / d ** 0.5) if scale is None else scale
-    fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q.stride()[:3], k.stride()[:3], v.stride()[:3],
-                   o.stride()[:3], sc, q_offset, causal, window, sinks, mask, *mask_strides, dt, stream)
+    if lse_out is not None and (not lse_out.is_contiguous() or lse_out.dtype != torch.float32 or
+                                lse_out.numel() < B * Hq * Tq):
+        raise ValueError("lse_out must be a contiguous float32 [B, Hq, Tq]")
+    with torch.cuda.device(q.device):  # the C call launches on the current device
+        o = out if out is not None else torch.empty((B, Hq, Tq, d), dtype=o_dtype, device=q.device)
+        lse = lse_out if lse_out is not None else (
+            torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device) if with_lse else None)
+        sc = (1.0 / d ** 0.5) if scale is None else scale
+        fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q.stride()[:3], k.stride()[:3], v.stride()[:3],
+                       o.stride()[:3], sc, q_offset, causal, window, sinks, mask, *mask_strides, dt, stream)
     return o, lse
 
 
@@ -206,17 +238,23 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, *, 
     import torch
     B, Hq, Tq, d = q.shape
     num_pages, page_size, Hkv, _ = k_cache.shape
+    _check_tensors(q.device, k_cache=k_cache, v_cache=v_cache, block_table=block_table, seq_lens=seq_lens,
+                   sinks=sinks)
+    _check_f32("sinks", sinks, Hq)
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("block_table", block_table),
                     ("seq_lens", seq_lens)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_table and seq_lens must be int32")
-    o = torch.empty_like(q)
-    lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
-    sc = (1.0 / d ** 0.5) if scale is None else scale
-    fa_fwd_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tq, d, seq_lens, max_seq_len, block_table,
-                 block_table.shape[1], page_size, num_pages, sc, causal, window, sinks, FA_DTYPE_BF16, stream)
+    if isinstance(sinks, torch.Tensor) and not sinks.is_contiguous():
+        raise ValueError("sinks must be contiguous [Hq]")
+    with torch.cuda.device(q.device):  # the C call launches on the current device
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+        sc = (1.0 / d ** 0.5) if scale is None else scale
+        fa_fwd_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tq, d, seq_lens, max_seq_len, block_table,
+                     block_table.shape[1], page_size, num_pages, sc, causal, window, sinks, FA_DTYPE_BF16, stream)
     return o, lse
 
 
@@ -245,17 +283,24 @@ def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
     total_q, Hq, d = q.shape
     total_k, Hkv = k.shape[0], k.shape[1]
     B = cu_seqlens_q.numel() - 1
+    _check_tensors(q.device, k=k, v=v, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k, sinks=sinks)
+    _check_f32("sinks", sinks, Hq)
+    if isinstance(sinks, torch.Tensor) and not sinks.is_contiguous():
+        raise ValueError("sinks must be contiguous [Hq]")
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
     codes = {torch.float32: FA_DTYPE_F32, torch.bfloat16: FA_DTYPE_BF16, torch.float8_e4m3fn: FA_DTYPE_FP8_E4M3}
     if q.dtype not in codes or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k and v must share a dtype: fp32, bf16 or float8_e4m3fn")
     dt = codes[q.dtype]
     if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
-    o = torch.empty((total_q, Hq, d), dtype=torch.bfloat16 if dt == FA_DTYPE_FP8_E4M3 else q.dtype,
-                    device=q.device)
-    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
-    sc = (1.0 / d ** 0.5) if scale is None else scale
-    fa_fwd_varlen(q, k, v, o, lse, B, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q,
-                  max_seqlen_k, (q.stride(1), q.stride(0)), (k.stride(1), k.stride(0)), (v.stride(1), v.stride(0)),
-                  (o.stride(1), o.stride(0)), sc, causal, window, sinks, dt, stream)
+    with torch.cuda.device(q.device):  # the C call launches on the current device
+        o = torch.empty((total_q, Hq, d), dtype=torch.bfloat16 if dt == FA_DTYPE_FP8_E4M3 else q.dtype,
+                        device=q.device)
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+        sc = (1.0 / d ** 0.5) if scale is None else scale
+        fa_fwd_varlen(q, k, v, o, lse, B, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q,
+                      max_seqlen_k, (q.stride(1), q.stride(0)), (k.stride(1), k.stride(0)),
+                      (v.stride(1), v.stride(0)), (o.stride(1), o.stride(0)), sc, causal, window, sinks, dt, stream)
     return o, lse
