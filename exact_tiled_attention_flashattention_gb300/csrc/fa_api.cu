@@ -293,10 +293,11 @@ extern "C" fa_status fa_fwd_paged(const void *q, const void *k_cache, const void
     if (max_seq_len > 0) {
         if (page_size < 8 || (page_size <= 128 ? (128 % page_size != 0) : (page_size % 128 != 0)))
             return fail(FA_EUNSUPPORTED, "page_size must divide 128 (and be >= 8) or be a multiple of 128");
-        if (max_blocks == 0 || max_seq_len > max_blocks * page_size)
+        int64_t capacity = 0;  // keys the table can address (a product too large for int64 addresses them all)
+        if (max_blocks == 0 || (mul_ok(max_blocks, page_size, capacity) && max_seq_len > capacity))
             return fail(FA_EINVAL, "max_seq_len exceeds max_blocks * page_size");
-        if (num_pages == 0 || num_pages > 0x7fffffff || max_blocks > 0x7fffffff)
-            return fail(FA_EUNSUPPORTED, "num_pages and max_blocks must be in [1, 2^31)");
+        if (num_pages == 0 || num_pages > 0x7fffffff || max_blocks > 0x7fffffff || page_size > 0x7fffffff)
+            return fail(FA_EUNSUPPORTED, "num_pages and max_blocks must be in [1, 2^31), page_size below 2^31");
     }
     if (max_seq_len >= kMaxLen || Tq >= kMaxLen) return fail(FA_EUNSUPPORTED, "lengths must be below 2^30");
     if (B * Hq >= (int64_t(1) << 24)) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^24");
@@ -372,7 +373,9 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
         return fail(FA_EUNSUPPORTED, "bf16 path supports d a multiple of 8 up to 128 (got %lld)", (long long)d);
     if (total_q >= kMaxLen || total_k >= kMaxLen || max_seqlen_q > total_q)
         return fail(FA_EUNSUPPORTED, "totals must be below 2^30 and max_seqlen_q <= total_q");
-    if (B >= (int64_t(1) << 24) || B * Hq >= (int64_t(1) << 31)) return fail(FA_EUNSUPPORTED, "too many sequences");
+    int64_t bh = 0;
+    if (B >= (int64_t(1) << 24) || !mul_ok(B, Hq, bh) || bh >= (int64_t(1) << 31))
+        return fail(FA_EUNSUPPORTED, "too many sequences");
     if (!aligned16(q) || !aligned16(o) || (total_k > 0 && (!aligned16(k) || !aligned16(v))))
         return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
     // Tensor maps: 16-byte stride multiples (o is bf16 with e4m3 inputs).

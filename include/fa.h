@@ -153,7 +153,7 @@ fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, f
  *                    NULL caches / block_table with max_seq_len > 0.
  *   FA_EUNSUPPORTED  dtype other than bf16; (Hq / Hkv) * Tq > 128;
  *                    page_size neither a divisor of 128 (>= 8) nor a multiple
- *                    of 128; num_pages or max_blocks >= 2^31.
+ *                    of 128; num_pages, max_blocks or page_size >= 2^31.
  * A sequence's result equals that of fa_fwd on its keys laid out
  * contiguously, bit for bit, when both calls split the key range the same
  * way (same B, Hkv and longest length). */
