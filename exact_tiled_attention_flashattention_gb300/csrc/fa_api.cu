@@ -182,10 +182,12 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
             }
         if (B > 0x7fffffff || Hq > 0x7fffffff) return fail(FA_EUNSUPPORTED, "B and H must fit 31 bits");
     }
-    // The tensor-core kernels index 128-row query tiles of each (batch, head)
-    // as 31-bit unit numbers.
+    // The kernels index the query tiles of each (batch, head) as 31-bit
+    // block or unit numbers: 128-row tiles on the tensor cores, 64 on SIMT.
     if (tma && ((Tq + 127) / 128) * B * Hq > 0x7fffffff)
         return fail(FA_EUNSUPPORTED, "tensor-core paths: B*Hq*ceil(Tq/128) must be below 2^31");
+    if (!tma && ((Tq + 63) / 64) * B * Hq > 0x7fffffff)
+        return fail(FA_EUNSUPPORTED, "fp32 path: B*Hq*ceil(Tq/64) must be below 2^31");
 
     fa::Params P;
     std::memset(&P, 0, sizeof P);
@@ -376,6 +378,11 @@ extern "C" fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, 
     int64_t bh = 0;
     if (B >= (int64_t(1) << 24) || !mul_ok(B, Hq, bh) || bh >= (int64_t(1) << 31))
         return fail(FA_EUNSUPPORTED, "too many sequences");
+    // Query tiles of every (sequence, head) as 31-bit block or unit numbers:
+    // 128 rows on the tensor cores, 64 on SIMT.
+    const int64_t tile_rows = dtype == FA_DTYPE_F32 ? 64 : 128;
+    if (((max_seqlen_q + tile_rows - 1) / tile_rows) * bh > 0x7fffffff)
+        return fail(FA_EUNSUPPORTED, "B*Hq*ceil(max_seqlen_q/%lld) must be below 2^31", (long long)tile_rows);
     if (!aligned16(q) || !aligned16(o) || (total_k > 0 && (!aligned16(k) || !aligned16(v))))
         return fail(FA_EUNSUPPORTED, "q, k, v and o must be 16-byte aligned");
     // Tensor maps: 16-byte stride multiples (o is bf16 with e4m3 inputs).

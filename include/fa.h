@@ -65,8 +65,9 @@
  *                    FA_DTYPE_F32_TC d not a multiple of 4 or above 128,
  *                    FA_DTYPE_FP8_E4M3 d not a multiple of 16 or above 128,
  *                    B*Hq*ceil(Tq/128) >= 2^31 on the tensor-core dtypes
- *                    (bf16, F32_TC, e4m3), Tq or Tk >= 2^30, pointers not
- *                    16-byte aligned.
+ *                    (bf16, F32_TC, e4m3), B*Hq*ceil(Tq/64) >= 2^31 for
+ *                    FA_DTYPE_F32, Tq or Tk >= 2^30, pointers not 16-byte
+ *                    aligned.
  *   FA_ECUDA         a CUDA error while configuring or launching.
  * B*Hq*Tq == 0 is a no-op returning FA_OK.  Tk == 0 writes o = 0 and
  * lse = -inf (or the sink).  fa_last_error() describes the last non-OK
@@ -177,8 +178,9 @@ fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, 
  * max_seqlen_k is the analogous bound on keys.  Offsets are clamped into
  * [0, total], so a malformed table cannot make the kernels reach outside the
  * tensors.  No additive mask.  Errors as fa_fwd_strided, plus FA_EINVAL for a
- * NULL cu_seqlens table and FA_EUNSUPPORTED when max_seqlen_q > total_q or
- * dtype is FA_DTYPE_F32_TC (fp32 batches run on FA_DTYPE_F32 here).  With
+ * NULL cu_seqlens table and FA_EUNSUPPORTED when max_seqlen_q > total_q,
+ * B*Hq*ceil(max_seqlen_q/128) >= 2^31 (64 for FA_DTYPE_F32), or dtype is
+ * FA_DTYPE_F32_TC (fp32 batches run on FA_DTYPE_F32 here).  With
  * FA_DTYPE_FP8_E4M3, q, k and v are e4m3 (strides multiples of 16 elements)
  * and o is bf16 (strides multiples of 8). */
 fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -35,16 +35,23 @@ _STUBS = r"""
 namespace fa {
 Params g_last;
 int g_calls = 0;
-#define FA_STUB(name) \
-    cudaError_t name(const Params &P, cudaStream_t) { g_last = P; ++g_calls; return cudaSuccess; }
-FA_STUB(launch_f32)
-FA_STUB(launch_f32_tc)
-FA_STUB(launch_bf16)
-FA_STUB(launch_fp8)
-FA_STUB(launch_fp8_varlen)
-FA_STUB(launch_bf16_paged)
-FA_STUB(launch_bf16_varlen)
-FA_STUB(launch_f32_varlen)
+long g_bad_grids = 0;
+// Every accepted call must give a grid the kernels can index with 31-bit
+// block numbers: query tiles of `rows` rows of every (batch, head).
+static void grid_ok(const Params &P, long long rows) {
+    const long long tiles = ((long long)P.Tq + rows - 1) / rows;
+    if (P.B < 0 || P.Hq < 0 || P.Tq < 0 || tiles * P.B * P.Hq > 0x7fffffffll) ++g_bad_grids;
+}
+#define FA_STUB(name, rows) \
+    cudaError_t name(const Params &P, cudaStream_t) { g_last = P; ++g_calls; grid_ok(P, rows); return cudaSuccess; }
+FA_STUB(launch_f32, 64)
+FA_STUB(launch_f32_tc, 128)
+FA_STUB(launch_bf16, 128)
+FA_STUB(launch_fp8, 128)
+FA_STUB(launch_fp8_varlen, 128)
+FA_STUB(launch_bf16_paged, 128)
+FA_STUB(launch_bf16_varlen, 128)
+FA_STUB(launch_f32_varlen, 64)
 cudaError_t bf16_watchdog(cudaStream_t, unsigned int *f) { *f = 0; return cudaSuccess; }
 cudaError_t f32tc_watchdog(cudaStream_t, unsigned int *f) { *f = 0; return cudaSuccess; }
 cudaError_t bf16_set_drop_arrive(int) { return cudaSuccess; }
@@ -60,7 +67,7 @@ _API_DRIVER = r"""
 #include <limits>
 #include "fa.h"
 #include "fa_internal.h"
-namespace fa { extern Params g_last; extern int g_calls; }
+namespace fa { extern Params g_last; extern int g_calls; extern long g_bad_grids; }
 
 static uint64_t state = 0x243f6a8885a308d3ull;
 static uint64_t next() {  // xorshift64*
@@ -156,6 +163,21 @@ int main() {
     if (st != FA_OK || fa::g_calls != c + 1 || fa::g_last.q_sb != 16ll * 511 * 128 || fa::g_last.k_sh != 511ll * 128 ||
         fa::g_last.group != 2 || fa::g_last.Tq != 511) {
         std::printf("valid call: status %d, %s\n", (int)st, fa_last_error());
+        ++bad;
+    }
+    // fp32 on the SIMT cores: 64-row tiles, so 2^31 tiles come sooner.
+    {
+        int c = fa::g_calls;
+        // B * Hq = 2^23 heads of 2^14 rows: 2^31 tiles of 64 rows; q, k and v
+        // broadcast (stride 0), o distinct rows of d = 2
+        fa_status st = fa_fwd_strided(a, a, a, out, lse, 1 << 19, 1 << 4, 1 << 4, 1 << 14, 1, 2, 0, 0, 0, 0, 0, 0, 0, 0,
+                                      0, int64_t(1) << 19, int64_t(1) << 15, 2, 0.125f, 0, 0, 0, nullptr, nullptr, 0,
+                                      0, 0, 0, FA_DTYPE_F32, nullptr);
+        check("fa_fwd_strided (2^31 fp32 tiles)", st, c);
+        if (st == FA_OK && bad++ < 5) std::printf("fp32 call with 2^31 query tiles accepted\n");
+    }
+    if (fa::g_bad_grids != 0) {
+        std::printf("%ld accepted calls with a grid of 2^31 tiles or more\n", fa::g_bad_grids);
         ++bad;
     }
     std::printf("calls %ld, launched %d, failures %ld\n", n + 1, fa::g_calls, bad);
