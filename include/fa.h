@@ -29,7 +29,9 @@
  * All pointers are DEVICE pointers on the current CUDA device.  q, k, v and o
  * must be 16-byte aligned.  The caller owns every buffer; the library keeps
  * no state between calls beyond cached kernel attributes and allocates no
- * device memory.
+ * device memory.  The attributes are set by the first call of the process on
+ * the device then current: a process drives one GPU, and its first call is
+ * not made from several host threads at once.
  *
  * Arithmetic: FA_DTYPE_F32 computes in fp32 on the SIMT cores (FFMA) and
  * writes fp32 o.  FA_DTYPE_BF16 reads bf16 q/k/v, forms S = Q K^T and O = P V
