@@ -21,6 +21,9 @@ roofline  the dominant kernel (the bf16 tcgen05 kernel) against the measured
 cpu_baseline  the float64 oracle on the host cores on a bounded sample; with
           the long-context runs also 128 rows of each long workload, their
           time and its extrapolation to every row (labelled as such).
+parity    layer 0 of the timed graph's output against the float64 oracle
+          (the oracle's run of the cpu_baseline leg): max and mean |o - oracle|,
+          max |lse - oracle|, and whether they are within the bf16 tolerance.
 long_context  bf16 causal prefill at T = 2044, 8192, 32768: one call and a
           sequence of calls, with the count of exponentials (one per visible
           pair) and the ex2 results per clock per SM that the time implies.
@@ -472,22 +475,50 @@ def measure_other_paths(fa, dev, flush, peak_bf16):
 
 def time_oracle_layers(max_seconds: float, max_layers: int = 28):
     """Oracle over whole layers of the workload until ``max_seconds`` pass.
-    Returns (flops, seconds, layers, threads)."""
+    Returns (flops, seconds, layers, threads, (o, lse) of layer 0)."""
     import torch
     import oracle
     p = workloads.CONFIGS[WORKLOAD].problem
     threads = os.cpu_count() or 1
     orc = oracle.get()
-    flops, secs, layers = 0, 0.0, 0
+    flops, secs, layers, first = 0, 0.0, 0, None
     while layers < max_layers and (layers == 0 or secs < max_seconds):
         q, k, v = workloads.qkv(layers, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, torch.bfloat16)
         qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
         t0 = time.perf_counter()
-        orc.attention(qn, kn, vn, p.sm_scale, causal=True, threads=threads)
+        res = orc.attention(qn, kn, vn, p.sm_scale, causal=True, threads=threads)
         secs += time.perf_counter() - t0
+        if first is None:
+            first = res
         flops += p.flops()
         layers += 1
-    return flops, secs, layers, threads
+    return flops, secs, layers, threads, first
+
+
+# The bf16 bound the parity tests hold the CUDA path to (oracle on the same
+# bf16-rounded inputs).
+BF16_TOL = {"o_max": 2e-2, "o_mean": 2e-3, "lse_max": 1e-2}
+
+
+def parity_summary(o, lse, eo, el, tol=BF16_TOL) -> dict:
+    """Distance of a GPU result (o, lse as float arrays) from the oracle's
+    (eo, el): max and mean |o - oracle| and max |lse - oracle| over rows
+    with a visible key; rows the oracle calls empty (lse = -inf) must be
+    empty (lse = -inf, o = 0) on the GPU too."""
+    import numpy as np
+    o = np.asarray(o, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    eo = np.asarray(eo, dtype=np.float64)
+    el = np.asarray(el, dtype=np.float64)
+    empty = np.isneginf(el)
+    empty_ok = bool(np.array_equal(np.isneginf(lse), empty) and np.all(o[empty] == 0.0))
+    d_o = np.abs(o - eo)
+    d_l = np.abs(lse[~empty] - el[~empty]) if (~empty).any() else np.zeros(1)
+    out = {"max_abs_o": float(d_o.max()) if d_o.size else 0.0, "mean_abs_o": float(d_o.mean()) if d_o.size else 0.0,
+           "max_abs_lse": float(d_l.max()), "empty_rows_match": empty_ok, "tolerance": dict(tol)}
+    out["within_tolerance"] = bool(empty_ok and out["max_abs_o"] <= tol["o_max"] and
+                                   out["mean_abs_o"] <= tol["o_mean"] and out["max_abs_lse"] <= tol["lse_max"])
+    return out
 
 
 def time_oracle_long(name: str):
@@ -725,14 +756,20 @@ def run_fa(args, rank, world, local_rank):
         others = measure_other_paths(fa, dev, flush, peak_burst)
         decode = measure_decode(fa, dev, flush, local_rank)
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
-        fl, secs, nl, thr = time_oracle_layers(args.cpu_seconds)
+        fl, secs, nl, thr, first = time_oracle_layers(args.cpu_seconds)
         cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"layers 0..{nl - 1} of 28 of the same workload, all rows, float64 oracle "
                          f"({secs:.1f} s)"}
         if not args.skip_long:
             cpu["long_context"] = [time_oracle_long(n) for n in LONG_CONTEXT]
+        # The timed graph's output of layer 0 against the oracle's.
+        try:
+            parity = {"layer": 0, **parity_summary(outs[0][0].float().cpu().numpy(), outs[0][1].cpu().numpy(),
+                                                   *first)}
+        except Exception as e:  # the field reports the failure; the line still prints
+            parity = {"layer": 0, "error": f"{type(e).__name__}: {e}"[:200]}
 
     if dist is not None:
         dist.barrier()
@@ -776,6 +813,7 @@ def run_fa(args, rank, world, local_rank):
         "other_paths": others,
         "decode": decode,
         "cpu_baseline": cpu,
+        "parity": parity,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

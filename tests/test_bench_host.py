@@ -56,3 +56,37 @@ def test_too_few_warmup_steps_are_refused():
     r = _bench("--impl", "reference", "--steps", "1", "--warmup", "2")
     assert r.returncode != 0
     assert "warmup" in r.stderr
+
+
+# --- the parity field of the bench line -----------------------------------------
+
+def test_parity_summary_reads_distances_and_empty_rows():
+    import numpy as np
+    eo = np.zeros((1, 2, 3, 4))
+    el = np.array([[[0.5, -np.inf, 1.0], [0.2, 0.3, 0.4]]])
+    s = bench.parity_summary(eo.copy(), el.copy(), eo, el)
+    assert s["within_tolerance"] and s["empty_rows_match"] and s["max_abs_o"] == 0.0 and s["max_abs_lse"] == 0.0
+    o = eo.copy()
+    o[0, 1, 2, 3] = 0.03  # above the 2e-2 bound
+    s = bench.parity_summary(o, el.copy(), eo, el)
+    assert not s["within_tolerance"] and abs(s["max_abs_o"] - 0.03) < 1e-12
+    lse = el.copy()
+    lse[0, 0, 1] = 0.0  # a row the oracle calls empty must stay empty
+    s = bench.parity_summary(eo.copy(), lse, eo, el)
+    assert not s["empty_rows_match"] and not s["within_tolerance"]
+
+
+def test_parity_of_the_benchmark_layer_shapes():
+    """The bench's expression on stand-ins for its output buffers: the
+    oracle's own layer 0, stored as bf16 O and fp32 lse, is within the bf16
+    tolerance of itself, with the shapes the timed graph writes."""
+    import torch
+    flops, secs, layers, threads, first = bench.time_oracle_layers(0.0, max_layers=1)
+    assert layers == 1 and flops > 0 and secs > 0
+    eo, el = first
+    p = bench.workloads.CONFIGS[bench.WORKLOAD].problem
+    assert eo.shape == (p.B, p.Hq, p.Tq, p.d) and el.shape == (p.B, p.Hq, p.Tq)
+    outs = [(torch.from_numpy(eo).to(torch.bfloat16), torch.from_numpy(el).float())]
+    s = {"layer": 0, **bench.parity_summary(outs[0][0].float().cpu().numpy(), outs[0][1].cpu().numpy(), *first)}
+    assert s["within_tolerance"], s
+    assert 0 < s["max_abs_o"] <= 2 ** -8 * float(abs(eo).max())  # bf16 rounding of O only
