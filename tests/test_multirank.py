@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_gloo_world2():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of a threaded test process
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0] == pytest.approx(1.25) and out[1] == pytest.approx(1.25)
 
