@@ -131,6 +131,23 @@ def kernel_sources_digest() -> str:
     return h.hexdigest()
 
 
+def recorded_traffic(workload: str, path: str | None = None):
+    """DRAM bytes per launch of ``workload``'s kernel from an ncu capture
+    (profiles/traffic.json), or None: valid only while the kernel sources
+    are the ones the capture was taken with (same digest)."""
+    prof = path or os.path.join(_ROOT, "profiles", "traffic.json")
+    if not os.path.exists(prof):
+        return None
+    try:
+        with open(prof) as f:
+            rec = json.load(f).get(workload)
+        if rec and rec.get("kernel_sources_sha256") == kernel_sources_digest():
+            return rec.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
 def max_over_ranks(seconds: float, dist=None, device=None) -> float:
     """The slowest rank's time: the whole job finishes when it does."""
     if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
@@ -778,18 +795,7 @@ def run_fa(args, rank, world, local_rank):
             dist.destroy_process_group()
         return
 
-    traffic = None
-    prof = os.path.join(_ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        # DRAM bytes per launch from an ncu capture, valid only while the
-        # kernel sources are the ones the capture was taken with.
-        try:
-            with open(prof) as f:
-                rec = json.load(f).get(WORKLOAD)
-            if rec and rec.get("kernel_sources_sha256") == kernel_sources_digest():
-                traffic = rec.get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic(WORKLOAD)
     avg_launch_s = (total_s / args.steps) / L
     achieved = flops_call / avg_launch_s / 1e12
     value = job_throughput(world, flops_step, args.steps, total_s)

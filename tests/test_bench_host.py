@@ -90,3 +90,21 @@ def test_parity_of_the_benchmark_layer_shapes():
     s = {"layer": 0, **bench.parity_summary(outs[0][0].float().cpu().numpy(), outs[0][1].cpu().numpy(), *first)}
     assert s["within_tolerance"], s
     assert 0 < s["max_abs_o"] <= 2 ** -8 * float(abs(eo).max())  # bf16 rounding of O only
+
+
+# --- the roofline's traffic figure ------------------------------------------------
+
+def test_recorded_traffic_follows_the_kernel_sources(tmp_path):
+    """A capture is read while the kernel sources match its digest; a record
+    with another digest (the kernel changed since) reads as None."""
+    rec = {bench.WORKLOAD: {"dram_bytes_per_launch": 123, "kernel_sources_sha256": bench.kernel_sources_digest()}}
+    f = tmp_path / "t.json"
+    f.write_text(json.dumps(rec))
+    assert bench.recorded_traffic(bench.WORKLOAD, str(f)) == 123
+    rec[bench.WORKLOAD]["kernel_sources_sha256"] = "0" * 64
+    f.write_text(json.dumps(rec))
+    assert bench.recorded_traffic(bench.WORKLOAD, str(f)) is None
+    assert bench.recorded_traffic("no_such_workload", str(f)) is None
+    assert bench.recorded_traffic(bench.WORKLOAD, str(tmp_path / "missing.json")) is None
+    f.write_text("{not json")
+    assert bench.recorded_traffic(bench.WORKLOAD, str(f)) is None
