@@ -17,7 +17,7 @@ from pathlib import Path
 
 __all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_ETIMEOUT", "FA_DTYPE_F32",
            "FA_DTYPE_BF16", "FA_DTYPE_F32_TC", "FA_DTYPE_FP8_E4M3", "FaError", "fa_fwd", "fa_last_error",
-           "fa_version", "fa_device_status", "fa_test_drop_arrive", "attention", "library_path", "load"]
+           "fa_version", "fa_device_status", "fa_test_drop_arrive", "fa_test_max_ctas", "attention", "library_path", "load"]
 
 FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA, FA_ETIMEOUT = 0, 1, 2, 3, 4, 5
 FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F32_TC, FA_DTYPE_FP8_E4M3 = 0, 1, 2, 3
@@ -68,6 +68,8 @@ def load():
     lib.fa_device_status.argtypes = [vp]
     lib.fa_test_drop_arrive.restype = ctypes.c_int
     lib.fa_test_drop_arrive.argtypes = [ctypes.c_int]
+    lib.fa_test_max_ctas.restype = ctypes.c_int
+    lib.fa_test_max_ctas.argtypes = [ctypes.c_int64]
     _lib = lib
     return lib
 
@@ -136,6 +138,15 @@ def fa_test_drop_arrive(enable: bool) -> int:
     """Test hook: while enabled, CTA 0 of each tensor-core kernel skips one load."""
     lib = load()
     st = lib.fa_test_drop_arrive(1 if enable else 0)
+    if st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+def fa_test_max_ctas(n: int) -> int:
+    """Test hook: cap the persistent tensor-core launches at ``n`` CTAs (0: off)."""
+    lib = load()
+    st = lib.fa_test_max_ctas(int(n))
     if st != FA_OK:
         raise FaError(st, lib.fa_last_error().decode())
     return st

@@ -59,6 +59,17 @@ extern "C" fa_status fa_device_status(void *stream) {
     return FA_OK;
 }
 
+namespace fa {
+int g_test_max_ctas = 0;
+}
+
+extern "C" fa_status fa_test_max_ctas(int64_t n) {
+    g_last_error[0] = '\0';
+    if (n < 0) return fail(FA_EINVAL, "fa_test_max_ctas: n = %lld is negative", (long long)n);
+    fa::g_test_max_ctas = n > (int64_t)1 << 30 ? 1 << 30 : (int)n;
+    return FA_OK;
+}
+
 extern "C" fa_status fa_test_drop_arrive(int enable) {
     g_last_error[0] = '\0';
     const int on = enable ? 1 : 0;

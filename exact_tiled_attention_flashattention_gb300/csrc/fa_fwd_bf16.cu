@@ -33,14 +33,9 @@
 // K_0, K_1 and Q load while the current unit finishes, its first S tiles run
 // while the softmax warps write the current unit's output.
 //
-// K/V sharing: when the GQA group size is even and a unit can walk 4096 keys
-// or more, the two query heads of a KV head at the same rows run as a cluster
-// of two CTAs.  Each CTA loads half of
-// every K/V tile (64 of its 128 rows) with a multicast TMA that lands in both
-// CTAs' shared memory, and a ring slot is refilled only after both CTAs'
-// tensor cores released it (a multicast tcgen05.commit arrives on the slot's
-// barrier in both CTAs).  K and V tiles have rings of their own, each read by
-// one issuing thread.
+// K and V tiles have rings of their own, each read by one issuing thread.
+// Every CTA loads its own tiles (no cluster multicast): the K/V tiles a GQA
+// group shares come from L2.
 //
 // Warp roles (352 threads):
 //   warps 0-7   softmax and epilogue: two threads per query row (= TMEM
@@ -70,6 +65,7 @@
 #include <cstdint>
 
 #include "fa_internal.h"
+#include "fa_tma_host.h"
 #include "sm100_ptx.cuh"
 
 namespace fa {
@@ -176,20 +172,18 @@ struct Unit {
     int qrow, krow;    // tensor rows where the sequence's queries / keys start
 };
 
-// Units sorted heaviest first: unit u has query tile nqt-1-u/per_qt.  With
-// PAIR == 2 a unit covers query heads 2h' (cluster rank 0) and 2h'+1 (rank 1)
-// of one KV group; `rank` picks this CTA's head.
-template <int PAIR, int MODE>
-__device__ __forceinline__ Unit make_unit(const Params &P, int u, int rank) {
+// Units sorted heaviest first: unit u has query tile nqt-1-u/per_qt, then
+// (batch, head).
+template <int MODE>
+__device__ __forceinline__ Unit make_unit(const Params &P, int u) {
     Unit U;
     const int nqt = (P.Tq + kBM - 1) / kBM;
     // Divisions by launch constants: multiply-high and shift (fast_div.h).
     const int qpos = (int)P.fd_per_qt.div((uint32_t)u);
     const int qt = nqt - 1 - qpos;
     const int r = u - qpos * (int)P.fd_per_qt.d;
-    U.b = (int)P.fd_heads.div((uint32_t)r);  // fd_heads: Hq, or Hq / 2 with a CTA pair
-    const int hr = r - U.b * (int)P.fd_heads.d;
-    U.h = PAIR == 2 ? 2 * hr + rank : hr;
+    U.b = (int)P.fd_heads.div((uint32_t)r);  // fd_heads: Hq
+    U.h = r - U.b * (int)P.fd_heads.d;
     U.bh = U.b * P.Hq + U.h;
     U.g = (int)P.fd_group.div((uint32_t)U.h);
     U.r0 = qt * kBM;
@@ -270,12 +264,12 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
     return U;
 }
 
-template <int MODE, int PAIR>
-__device__ __forceinline__ Unit get_unit(const Params &P, int u, int rank) {
+template <int MODE>
+__device__ __forceinline__ Unit get_unit(const Params &P, int u) {
     if constexpr (MODE == kDecode || MODE == kPaged)
         return decode_unit<MODE>(P);
     else
-        return make_unit<PAIR, MODE>(P, u, rank);
+        return make_unit<MODE>(P, u);
 }
 
 // Snake order over groups: round r gives group g unit r*G + g (r even) or
@@ -288,12 +282,11 @@ struct Schedule {
     }
 };
 
-template <int MODE, int PAIR>
+template <int MODE>
 __device__ __forceinline__ Schedule make_schedule(const Params &P) {
     if constexpr (MODE == kDecode || MODE == kPaged) return Schedule{1, 1, 0};  // one unit per CTA
     const int nqt = (P.Tq + kBM - 1) / kBM;
-    const int per_qt = PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq;
-    return Schedule{nqt * per_qt, (int)(gridDim.x / PAIR), (int)(blockIdx.x / PAIR)};
+    return Schedule{nqt * P.B * P.Hq, (int)gridDim.x, (int)blockIdx.x};
 }
 
 // Position in the K/V ring: stage index and the parity of its current use.
@@ -374,15 +367,13 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, Desc 
 
 // TMA producer (one thread).  Per unit: K_0 and K_1, then Q once the previous
 // unit's last S has released the Q buffer, then V_j and K_{j+2} in turn, each
-// into its own ring.  With PAIR == 2 this CTA loads rows [64 r, 64 r + 64) of
-// every K/V box (r = cluster rank) into both CTAs of the cluster.
-template <int D, int PAIR, int MODE>
+// into its own ring.
+template <int D, int MODE>
 __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                               const Params &P, uint8_t *smem, Barriers &bar) {
     using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
-    const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
-    const Schedule sched = make_schedule<MODE, PAIR>(P);
+    const Schedule sched = make_schedule<MODE>(P);
     // Loads issued into each ring so far: a stage has a previous use once
     // the ring has wrapped (kept as counters, not per-stage arrays, so that
     // nothing here lives in local memory).
@@ -393,7 +384,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const Unit U = get_unit<MODE, PAIR>(P, u, rank);
+        const Unit U = get_unit<MODE>(P, u);
         const int n = U.n_tiles;
         if (n == 0) continue;
 
@@ -423,14 +414,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
                 }
             } else {
 #pragma unroll
-            for (int c = 0; c < L::kBoxes; ++c) {
-                uint8_t *dst = smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes);
-                if (PAIR == 2)
-                    tma_load_4d_multicast(dst + rank * (kBN / 2) * kSwRowBytes, map, &full[st], c * L::kBoxCols,
-                                          U.krow + key0 + rank * (kBN / 2), U.g, kvb, (uint16_t)0x3);
-                else
-                    tma_load_4d(dst, map, &full[st], c * L::kBoxCols, U.krow + key0, U.g, kvb);
-            }
+            for (int c = 0; c < L::kBoxes; ++c)
+                tma_load_4d(smem + ring + st * L::kKVBytes + c * (kBN * kSwRowBytes), map, &full[st],
+                            c * L::kBoxCols, U.krow + key0, U.g, kvb);
             }
             ++loads;
             if (++pos.st == stages) {
@@ -511,20 +497,12 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
 // next S ready.  Each ring has one reader per CTA, so stage releases cannot
 // cross phases.
 
-// A ring stage is free once every CTA that reads it has finished with it.
-template <int PAIR>
-__device__ __forceinline__ void release_stage(uint64_t *empty) {
-    if (PAIR == 2)
-        mma_commit_multicast(empty, (uint16_t)0x3);
-    else
-        mma_commit(empty);
-}
 
-template <int D, int PAIR, int MODE>
+template <int D, int MODE>
 __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
-    const Schedule sched = make_schedule<MODE, PAIR>(P);
+    const Schedule sched = make_schedule<MODE>(P);
     const Desc qd = make_desc(smem_u32(smem + L::kQ), 16, 1024);
     const Desc k0 = make_desc(smem_u32(smem + L::kKRing), 16, 1024);
     constexpr uint32_t kTileUnits = L::kKVBytes >> 4;  // one stage, in descriptor units
@@ -536,7 +514,7 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const int n = get_unit<MODE, PAIR>(P, u, 0).n_tiles;  // the same for both CTAs of a pair
+        const int n = get_unit<MODE>(P, u).n_tiles;  // the same for both CTAs of a pair
         if (n == 0) continue;
         if (!(ok = mbar_wait(&bar.q_full, units & 1, abort))) break;
         for (int j = 0; j < n; ++j) {
@@ -548,7 +526,7 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
             issue_qk<D, MODE>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
             mma_commit(&bar.s_full[b]);
             if (j + 1 == n) mma_commit(&bar.q_empty);  // the unit's last S is issued
-            release_stage<PAIR>(&bar.k_empty[take.st]);
+            mma_commit(&bar.k_empty[take.st]);
             take.template advance<L::kStages>();
             sb.template advance<kSBufs>();
             if (sb.st == 0) first_use = false;
@@ -563,11 +541,11 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
 
 // The first O += P_0 V_0 of a unit overwrites O; the softmax warps read the
 // previous unit's O before they release P_0, so O is free by then.
-template <int D, int PAIR, int MODE>
+template <int D, int MODE>
 __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers &bar, uint32_t tbase) {
     using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
-    const Schedule sched = make_schedule<MODE, PAIR>(P);
+    const Schedule sched = make_schedule<MODE>(P);
     const Desc v0 = make_desc(smem_u32(smem + L::kVRing), kBN * kSwRowBytes, 1024);
     constexpr uint32_t kTileUnits = L::kKVBytes >> 4;
     RingPos take;
@@ -576,7 +554,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const int n = get_unit<MODE, PAIR>(P, u, 0).n_tiles;
+        const int n = get_unit<MODE>(P, u).n_tiles;
         if (n == 0) continue;
         for (int j = 0; j < n; ++j) {
             const int b = sb.st;
@@ -587,7 +565,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
                               j > 0 ? 1u : 0u);
             mma_commit(&bar.o_done[b]);
             if (j + 1 == n) mma_commit(&bar.o_final);
-            release_stage<PAIR>(&bar.v_empty[take.st]);
+            mma_commit(&bar.v_empty[take.st]);
             take.template advance<L::kVStages>();
             sb.template advance<kSBufs>();
         }
@@ -602,7 +580,7 @@ __device__ __forceinline__ void pv_role(const Params &P, uint8_t *smem, Barriers
 // l + 16 hold the same row, the first and second half of each tile's keys and
 // of O's columns.  Row max and row sum combine through one shuffle, and the
 // two warps on a scheduler partition hide each other's latencies.
-template <int D, int PAIR, int MODE>
+template <int D, int MODE>
 __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Params &P, uint8_t *smem, Barriers &bar,
                                              uint32_t tbase, int warp, int lane) {
     using L = SmemLayout<D, MODE>;
@@ -610,8 +588,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
     constexpr int kHD = D / 2;    // O columns per thread
     static_assert(kHD == 32 || kHD == 64, "a thread's O columns fill half or all of a 64-column box");
     volatile int *abort = &bar.abort;
-    const int rank = PAIR == 2 ? (int)(blockIdx.x & 1) : 0;
-    const Schedule sched = make_schedule<MODE, PAIR>(P);
+    const Schedule sched = make_schedule<MODE>(P);
     const int half = lane >> 4;
     const int lane0 = 32 * (warp & 3) + 16 * (warp >> 2);  // first tensor-memory lane of the warp
     const int row = lane0 + (lane & 15);
@@ -626,7 +603,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const Unit U = get_unit<MODE, PAIR>(P, u, rank);
+        const Unit U = get_unit<MODE>(P, u);
         const int n = U.n_tiles;
         // The row's query head h and its row i in that head.  Prefill: the
         // unit's head, consecutive rows.  Packed rows: row = i * group + hl
@@ -972,7 +949,7 @@ __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
     }
 }
 
-template <int D, int PAIR, int MODE>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -989,8 +966,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(&bar.k_full[s], 1);
             mbar_init(&bar.v_full[s], 1);
-            mbar_init(&bar.k_empty[s], PAIR);  // one release per CTA reading the stage
-            mbar_init(&bar.v_empty[s], PAIR);
+            mbar_init(&bar.k_empty[s], 1);
+            mbar_init(&bar.v_empty[s], 1);
         }
         for (int s = 0; s < kSBufs; ++s) {
             mbar_init(&bar.s_full[s], 1);
@@ -1016,11 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
-    if (PAIR == 2)
-        cluster_sync();  // the peer's barriers exist before any multicast reaches them
-    else
-        __syncthreads();
-    static_assert(is_prefill(MODE) || is_varlen(MODE) || PAIR == 1, "packed rows run without K/V multicast");
+    __syncthreads();
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
     // Inputs may come from the previous kernel in the stream, and outputs may
@@ -1029,13 +1002,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_launch_dependents();
 
     if (warp == kWarpTma) {
-        if (lane == 0) producer_role<D, PAIR, MODE>(tmQ, tmK, tmV, P, smem, bar);
+        if (lane == 0) producer_role<D, MODE>(tmQ, tmK, tmV, P, smem, bar);
     } else if (warp == kWarpQk) {
-        if (lane == 0) qk_role<D, PAIR, MODE>(P, smem, bar, tbase);
+        if (lane == 0) qk_role<D, MODE>(P, smem, bar, tbase);
     } else if (warp == kWarpPv) {
-        if (lane == 0) pv_role<D, PAIR, MODE>(P, smem, bar, tbase);
+        if (lane == 0) pv_role<D, MODE>(P, smem, bar, tbase);
     } else {
-        softmax_role<D, PAIR, MODE>(tmO, P, smem, bar, tbase, warp, lane);
+        softmax_role<D, MODE>(tmO, P, smem, bar, tbase, warp, lane);
     }
 
     tc_fence_before();
@@ -1044,9 +1017,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // every CTA's partial is written
         if (!bar.abort) merge_partials<D>(P, smem);
         cluster_sync();  // no CTA leaves while a peer reads its partial
-    } else if (PAIR == 2) {
-        // No CTA of a pair leaves while the other may still multicast into it.
-        cluster_sync();
     }
     if (bar.abort && threadIdx.x == 0) atomicOr(&g_watchdog, 1u);
     if (warp == kWarpQk) {
@@ -1057,57 +1027,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (fn == nullptr) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// A tensor map of bf16 (elem = 2) or e4m3 (elem = 1, as bytes) over `rank`
-// dimensions, dims[0] = d contiguous, the others with element strides; boxes
-// of 128 bytes of columns by box[1..] elements with the 128-byte swizzle.
-// Coordinates outside the tensor read as zero (loads) or are dropped
-// (stores).  A dimension of extent 1 is never stepped, so it gets a packed
-// stride whatever the caller's.
-bool encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int rank, const int64_t *dims,
-                const int64_t *strides, const uint32_t *box, int elem) {
-    cuuint64_t gd[5], gs[4];
-    cuuint32_t bx[5], es[5];
-    uint64_t packed = (uint64_t)dims[0] * elem;
-    for (int i = 0; i < rank; ++i) {
-        gd[i] = (cuuint64_t)dims[i];
-        bx[i] = box[i];
-        es[i] = 1;
-        if (i > 0) {
-            gs[i - 1] = dims[i] > 1 ? (cuuint64_t)strides[i] * elem : (cuuint64_t)packed;
-            packed = (uint64_t)gs[i - 1] * (uint64_t)dims[i];
-        }
-    }
-    return enc(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
-               const_cast<void *>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// [B, H, T, d] with element strides (sb, sh, st) as the 4-D map (d, T, H, B);
-// boxes of 128 bytes of columns x box_rows rows of one (batch, head).
-bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int T, int H, int B, int64_t st,
-              int64_t sh, int64_t sb, int box_rows, int elem = 2) {
-    const int64_t dims[4] = {d, T, H, B}, strides[4] = {1, st, sh, sb};
-    const uint32_t box[4] = {(uint32_t)(128 / elem), (uint32_t)box_rows, 1, 1};
-    return encode_map(enc, map, base, 4, dims, strides, box, elem);
-}
 
 // The query rows of one KV group as the 5-D map (d, group, Tq, Hkv, B): head
 // g * group + hl at row i is coordinate (., hl, i, g, b), and one box of 64
@@ -1129,24 +1048,11 @@ bool make_kv_maps(EncodeTiledFn enc, CUtensorMap *tk, CUtensorMap *tv, const Par
            make_map(enc, tv, P.v, P.d, P.Tk, P.Hkv, P.B, P.v_st, P.v_sh, P.v_sb, box_rows, elem);
 }
 
-// Streaming multiprocessors of the current device (cached per device).
-int sm_count() {
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
-
-template <int D, int PAIR, int MODE>
+template <int D, int MODE>
 cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
     Params P = P0;
-    P.fd_per_qt = FastDiv::make((uint32_t)(PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq));
-    P.fd_heads = FastDiv::make((uint32_t)(PAIR == 2 ? P.Hq / 2 : P.Hq));
+    P.fd_per_qt = FastDiv::make((uint32_t)(P.B * P.Hq));
+    P.fd_heads = FastDiv::make((uint32_t)P.Hq);
     P.fd_group = FastDiv::make((uint32_t)P.group);
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
@@ -1161,14 +1067,14 @@ cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
         ok = make_map(enc, &tq, P.q, P.d, P.total_q, P.Hq, 1, P.q_st, P.q_sh, 0, kBM, kE) &&
              make_map(enc, &to, P.o, P.d, P.total_q, P.Hq, 1, P.o_st, P.o_sh, 0, kBM);
         if (P.total_k > 0)
-            ok = ok && make_map(enc, &tk, P.k, P.d, P.total_k, P.Hkv, 1, P.k_st, P.k_sh, 0, kBN / PAIR, kE) &&
-                 make_map(enc, &tv, P.v, P.d, P.total_k, P.Hkv, 1, P.v_st, P.v_sh, 0, kBN / PAIR, kE);
+            ok = ok && make_map(enc, &tk, P.k, P.d, P.total_k, P.Hkv, 1, P.k_st, P.k_sh, 0, kBN, kE) &&
+                 make_map(enc, &tv, P.v, P.d, P.total_k, P.Hkv, 1, P.v_st, P.v_sh, 0, kBN, kE);
         else
-            ok = ok && make_map(enc, &tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR, kE) &&
-                 make_map(enc, &tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN / PAIR, kE);
+            ok = ok && make_map(enc, &tk, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN, kE) &&
+                 make_map(enc, &tv, P.q, P.d, 1, 1, 1, P.q_st, P.q_sh, 0, kBN, kE);
     } else {
         ok = make_map(enc, &tq, P.q, P.d, P.Tq, P.Hq, P.B, P.q_st, P.q_sh, P.q_sb, kBM, kE) &&
-             make_kv_maps(enc, &tk, &tv, P, kBN / PAIR, kE) &&
+             make_kv_maps(enc, &tk, &tv, P, kBN, kE) &&
              make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM);
     }
     if (!ok) return cudaErrorInvalidValue;
@@ -1178,32 +1084,29 @@ cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
     static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "shared memory budget");
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, PAIR, MODE>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    // One CTA (pair) per SM, no more than there are units.
+    // One CTA per SM, no more than there are units (a test may cap the grid).
     const int nqt = (P.Tq + kBM - 1) / kBM;
-    const long long units = (long long)nqt * (PAIR == 2 ? P.B * (P.Hq / 2) : P.B * P.Hq);
+    const long long units = (long long)nqt * P.B * P.Hq;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const long long groups = units < sms / PAIR ? units : sms / PAIR;
+    long long grid = units < sms ? units : sms;
+    if (g_test_max_ctas > 0 && grid > g_test_max_ctas) grid = g_test_max_ctas;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(groups * PAIR));
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = PAIR;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, PAIR, MODE>, tq, tk, tv, to, P);
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_fwd_bf16_kernel<D, MODE>, tq, tk, tv, to, P);
 }
 
 // Key tiles seen by the rows at positions q_offset .. q_offset + Tq - 1 among
@@ -1248,7 +1151,7 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     if (!ok) return cudaErrorInvalidValue;
     constexpr size_t kSmem = SmemLayout<D, MODE>::kTotal + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    auto kernel = fa_fwd_bf16_kernel<D, 1, MODE>;
+    auto kernel = fa_fwd_bf16_kernel<D, MODE>;
     constexpr int kMaxSplits = 16;
     static bool configured = false;
     static int capacity[kMaxSplits + 1] = {};  // clusters of s CTAs resident at once
@@ -1319,47 +1222,23 @@ cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream) {
     return P.d <= 64 ? launch_packed<64, kPaged>(P, stream) : launch_packed<128, kPaged>(P, stream);
 }
 
-// A CTA pair shares every K/V tile between two query heads of one KV head
-// (each CTA loads half and multicasts it), at the price of cluster barriers
-// and of the two CTAs moving in step.  That pays off once a unit walks many
-// key tiles; on shorter walks the barriers cost more than the shared loads
-// save (measured on GB300, causal, d = 128: pairs 4-5 % slower at 511 and
-// 2044 keys, 0.6 % faster at 8192).
-constexpr int64_t kPairMinKeys = 4096;
-
-bool use_pair(const Params &P, bool varlen) {
-    if (P.group % 2 != 0) return false;
-    int64_t span = P.Tk;  // keys the longest unit can see
-    if (!varlen && P.causal && (int64_t)P.q_offset + P.Tq < span) span = (int64_t)P.q_offset + P.Tq;
-    if (P.window > 0 && (int64_t)P.window + kBM < span) span = (int64_t)P.window + kBM;
-    return span >= kPairMinKeys;
-}
-
 cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream) {
-    const bool pair = use_pair(P, true);
-    if (P.d <= 64) return pair ? launch_d<64, 2, kVarlen>(P, stream) : launch_d<64, 1, kVarlen>(P, stream);
-    return pair ? launch_d<128, 2, kVarlen>(P, stream) : launch_d<128, 1, kVarlen>(P, stream);
+    return P.d <= 64 ? launch_d<64, kVarlen>(P, stream) : launch_d<128, kVarlen>(P, stream);
 }
 
 cudaError_t launch_fp8(const Params &P, cudaStream_t stream) {
     // e4m3 rows of d <= 128 bytes: one 128-byte box per row, padded with zeros.
-    const bool pair = use_pair(P, false);
-    return pair ? launch_d<128, 2, kPrefill8>(P, stream) : launch_d<128, 1, kPrefill8>(P, stream);
+    return launch_d<128, kPrefill8>(P, stream);
 }
 
-cudaError_t launch_fp8_varlen(const Params &P, cudaStream_t stream) {
-    const bool pair = use_pair(P, true);
-    return pair ? launch_d<128, 2, kVarlen8>(P, stream) : launch_d<128, 1, kVarlen8>(P, stream);
-}
+cudaError_t launch_fp8_varlen(const Params &P, cudaStream_t stream) { return launch_d<128, kVarlen8>(P, stream); }
 
 cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
-    const bool pair = use_pair(P, false);
     // d is a multiple of 8 up to 128: the 64- or 128-column kernel, padded.
     // All query rows of a KV group in one tile: the packed-row kernel.
     if ((int64_t)P.group * P.Tq <= kBM)
         return P.d <= 64 ? launch_packed<64, kDecode>(P, stream) : launch_packed<128, kDecode>(P, stream);
-    if (P.d <= 64) return pair ? launch_d<64, 2, kPrefill>(P, stream) : launch_d<64, 1, kPrefill>(P, stream);
-    return pair ? launch_d<128, 2, kPrefill>(P, stream) : launch_d<128, 1, kPrefill>(P, stream);
+    return P.d <= 64 ? launch_d<64, kPrefill>(P, stream) : launch_d<128, kPrefill>(P, stream);
 }
 
 }  // namespace fa

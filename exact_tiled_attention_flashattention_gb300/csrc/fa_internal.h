@@ -76,6 +76,10 @@ cudaError_t bf16_watchdog(cudaStream_t stream, unsigned int *flag);
 cudaError_t f32tc_watchdog(cudaStream_t stream, unsigned int *flag);
 // Test hooks: make CTA 0 of the next launches skip one load (see the kernels).
 cudaError_t bf16_set_drop_arrive(int on);
+
+// Test hook: when positive, the persistent launchers use at most this many
+// CTAs (0: one per SM).  Set through fa_test_max_ctas.
+extern int g_test_max_ctas;
 cudaError_t f32tc_set_drop_arrive(int on);
 
 }  // namespace fa

@@ -131,18 +131,6 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// tma_load_4d delivered to every CTA of the cluster in `cta_mask`, at the
-// same shared-memory offset; complete_tx is signalled on the mbarrier at the
-// same offset in each destination CTA.
-__device__ __forceinline__ void tma_load_4d_multicast(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int c0,
-                                                      int c1, int c2, int c3, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(cta_mask)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -365,16 +353,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// Arrive once on the mbarrier at the same offset in every CTA of `cta_mask`
-// when every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane, load and wait in

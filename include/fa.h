@@ -217,6 +217,15 @@ fa_status fa_device_status(void *stream);
  * runs out.  Not for production use. */
 fa_status fa_test_drop_arrive(int enable);
 
+/* Test hook, off by default (n = 0): while n > 0, the persistent launches of
+ * the tensor-core kernels (bf16 / e4m3 prefill and variable-length batches)
+ * use at most n CTAs, so that each CTA walks more units.  Results must not
+ * depend on it: a row's arithmetic is the same whichever CTA or slot runs it
+ * ("FlashAttention forward in C", section 4: the thread-pool result equals
+ * the serial one bit for bit).  FA_EINVAL for n < 0.  Host-side state of the
+ * process, not thread-safe.  Not for production use. */
+fa_status fa_test_max_ctas(int64_t n);
+
 #ifdef __cplusplus
 }
 #endif

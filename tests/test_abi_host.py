@@ -231,3 +231,12 @@ def test_varlen_rejections(lib, case, kw, want):
                               a["total_k"], a["max_q"], a["max_k"], qs, ks, ks, os_, 0.125, 1, 0, None, a["dtype"], 0,
                               check=False)
     assert st == getattr(fa_mod, want), case
+
+
+def test_grid_cap_hook_checks_its_argument(lib):
+    """fa_test_max_ctas rejects a negative cap before changing anything and
+    accepts 0 (off) and positive caps; no GPU is touched."""
+    assert lib.fa_test_max_ctas(-1) == fa.FA_EINVAL
+    assert b"negative" in lib.fa_last_error()
+    assert lib.fa_test_max_ctas(7) == fa.FA_OK
+    assert lib.fa_test_max_ctas(0) == fa.FA_OK

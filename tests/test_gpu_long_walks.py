@@ -1,14 +1,13 @@
-"""GPU parity on both launch shapes of the tcgen05 kernel.
+"""GPU parity on long key walks of the tcgen05 kernel.
 
-With an even GQA group and units that can walk 4096 keys or more, two CTAs
-of a cluster take two query heads of one KV head and share every K/V tile
-(each loads half and multicasts it); below that each CTA loads its own
-tiles.  The cases here sit on the paired side with the features that change
-a unit's key range (q_offset chunks, no causal rule, a long window with
-sinks, ragged query and key tails), checked against the float64 oracle, and
-one check crosses the two shapes: rows computed by a paired call and by an
-unpaired chunk call must agree bit for bit, since the arithmetic per row is
-the same.
+Units that walk 4096 keys or more take their K and V tiles through many
+laps of the rings, so stage and barrier phases wrap many times within one
+unit.  The cases combine that with the features that change a unit's key
+range (q_offset chunks, no causal rule, a long window with sinks, ragged
+query and key tails), checked against the float64 oracle; one check holds
+rows of a long causal call bit for bit to the same rows computed by a chunk
+call ("FlashAttention forward in C", section 2.4: absolute key tiles make a
+row's arithmetic independent of the call it is in).
 """
 import numpy as np
 import pytest
@@ -46,7 +45,7 @@ CASES = [
 
 @pytest.mark.parametrize("dt", ["bf16", "e4m3"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_paired_path(case, dt):
+def test_long_walk(case, dt):
     name, B, Hq, Hkv, Tq, Tk, d, q_offset, causal, window, use_sinks = case
     if dt == "e4m3" and d % 16 != 0:
         pytest.skip("e4m3 rows are whole 16-byte units")
@@ -58,9 +57,9 @@ def test_paired_path(case, dt):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "e4m3"])
-def test_paired_and_unpaired_rows_agree(dt):
-    # One causal call over 4200 positions (paired) and the chunk of rows
-    # 3000..3299 with the keys so far (3300: unpaired) give the same bits.
+def test_long_call_and_chunk_rows_agree(dt):
+    # One causal call over 4200 positions and the chunk of rows 3000..3299
+    # with the keys so far (3300) give the same bits.
     dtype = torch.bfloat16 if dt == "bf16" else F8
     B, Hq, Hkv, T, d = 1, 4, 2, 4200, 128
     q, k, v = _inputs(13, B, Hq, Hkv, T, T, d, dtype)
@@ -68,8 +67,8 @@ def test_paired_and_unpaired_rows_agree(dt):
     s, n = 3000, 300
     o2, l2 = gpu_attention(q[:, :, s:s + n].contiguous(), k[:, :, :s + n].contiguous(),
                            v[:, :, :s + n].contiguous(), scale=d ** -0.5, q_offset=s, causal=True)
-    assert torch.equal(o1[:, :, s:s + n], o2), "o differs between the paired and unpaired launches"
-    assert torch.equal(l1[:, :, s:s + n], l2), "lse differs between the paired and unpaired launches"
+    assert torch.equal(o1[:, :, s:s + n], o2), "o differs between the long call and the chunk call"
+    assert torch.equal(l1[:, :, s:s + n], l2), "lse differs between the long call and the chunk call"
     rows = np.arange(s, s + n, 3, dtype=np.int64)
     eo, el = oracle_attention(q, k, v, rows=rows, scale=d ** -0.5, causal=True)
     if dtype == F8:

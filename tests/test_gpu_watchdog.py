@@ -11,13 +11,16 @@ import torch
 
 import exact_tiled_attention_flashattention_gb300 as fa
 import workloads
-from parity import compare, oracle_attention
+from parity import compare, compare_fp8, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
 CASES = [
     # (name, dtype, Hq, Hkv, Tq, Tk, q_offset, fp32_tc)
-    ("bf16 prefill, 2-CTA clusters", torch.bfloat16, 2, 1, 300, 300, 0, False),
+    ("bf16 prefill", torch.bfloat16, 2, 1, 300, 300, 0, False),
+    # walks of up to 35 key tiles: the K and V rings wrap many times per unit
+    ("bf16 prefill, long walk", torch.bfloat16, 2, 1, 300, 4396, 4096, False),
+    ("e4m3 prefill", torch.float8_e4m3fn, 2, 1, 300, 300, 0, False),
     ("bf16 decode, split key range", torch.bfloat16, 8, 2, 1, 4096, 4095, False),
     ("fp32 on the tensor cores", torch.float32, 2, 1, 300, 300, 0, True),
 ]
@@ -51,4 +54,7 @@ def test_wait_runs_out_and_context_survives(case):
     torch.cuda.synchronize()
     assert fa.fa_device_status() == fa.FA_OK
     eo, el = oracle_attention(q, k, v, scale=0.125, causal=True, q_offset=q_offset)
-    compare(o.cpu(), lse.cpu(), eo, el, dt, f"{name}: after the timeout")
+    if dt == torch.float8_e4m3fn:
+        compare_fp8(o.cpu(), lse.cpu(), eo, el, v, Hq // Hkv, f"{name}: after the timeout")
+    else:
+        compare(o.cpu(), lse.cpu(), eo, el, dt, f"{name}: after the timeout")
