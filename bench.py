@@ -604,6 +604,48 @@ def run_reference(args, rank, world):
 
 # -------------------------------------------------------------------- GPU
 
+# Short names of the workloads in the compact summary at the end of the line.
+_SHORT = {"tile_crossing_d64": "c1", "prefill511_gqa16x8_d128_x28": "p511x28", "longctx2044_gqa16x8_d128": "t2044",
+          "longctx8192_gqa16x8_d128": "t8192", "longctx32768_gqa16x8_d128": "t32768",
+          "window128_sinks_gqa32x4_d64_chunked": "win128", "mask_b4h8_t1024_d96": "mask",
+          "varlen_b8_gqa16x8_d128_256-4096": "varlen"}
+
+
+def compact_summary(long_ctx, others, decode, parity, clocks):
+    """The figures of every configuration in a few hundred bytes, placed last
+    on the line (records of a run that keep only the line's tail keep these):
+    long context per T (one call and per call in a sequence: us, TF/s, fraction
+    of the measured bf16 burst peak), the other paths (ms, TF/s and one
+    fraction: of HBM for the windowed workload, of the tensor ceiling for fp32
+    on the tensor cores, of the fp8 peak for e4m3, else of the fp32 SIMT
+    peak), decode (us per call, fraction of measured HBM), the parity of the
+    timed output, and one clocks record for the whole run."""
+    out = {"legend": "long_context: [us, TF/s, frac] one call, then per call in a sequence; other_paths: "
+                     "[ms, TF/s, frac of the path's own peak]; decode: [us per call, frac of HBM]"}
+    out["long_context"] = {_SHORT.get(e["workload"], e["workload"]): [
+        round(1e3 * e["ms"], 1), round(e["tflops"]), round(e["frac_of_measured_peak"], 3),
+        round(1e3 * e["ms_per_call_in_sequence"], 1), round(e["tflops_in_sequence"]), round(e["frac_in_sequence"], 3)]
+        for e in long_ctx}
+    op = {}
+    for e in others:
+        key = f"{_SHORT.get(e['workload'], e['workload'])}_{e['dtype']}"
+        frac = next((round(e[k], 3) for k in ("frac_of_hbm_peak", "frac_of_tensor_ceiling", "frac_of_fp8_peak",
+                                                "frac_of_fp32_simt_peak") if k in e), None)
+        op[key] = [round(e["ms"], 4), round(e["tflops"], 1), frac]
+    out["other_paths"] = op
+    out["decode"] = {e["workload"].replace("decode_", "").replace("_gqa16x8_d128", "")[:22]:
+                     [round(e["us_per_call"], 1), round(e["frac_of_hbm_peak"], 3)] for e in decode}
+    if parity:
+        out["parity"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in parity.items()
+                         if k in ("max_abs_o", "mean_abs_o", "max_abs_lse", "within_tolerance", "error")}
+    reasons = sorted({r for e in list(long_ctx) + list(decode) for r in (e.get("clocks") or {}).get("reasons", [])}
+                     | set((clocks or {}).get("reasons", [])))
+    mhz = [e["clocks"]["sm_mhz"] for e in list(long_ctx) + list(decode) if e.get("clocks") and e["clocks"].get("sm_mhz")]
+    out["clocks_all"] = {"sm_mhz_min": min(mhz) if mhz else None, "reasons": reasons}
+    return out
+
+
+
 def run_fa(args, rank, world, local_rank):
     import torch
     import exact_tiled_attention_flashattention_gb300 as fa
@@ -800,6 +842,9 @@ def run_fa(args, rank, world, local_rank):
     achieved = flops_call / avg_launch_s / 1e12
     value = job_throughput(world, flops_step, args.steps, total_s)
     line = {
+        # The full per-entry records first; the compact summary of the same
+        # figures comes last on the line.
+        "detail": {"long_context": long_ctx, "other_paths": others, "decode": decode},
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -815,11 +860,9 @@ def run_fa(args, rank, world, local_rank):
                      "frac": round(achieved / peak_burst, 4), "traffic": traffic,
                      "kernel": "fa_fwd_bf16_kernel<128, 1, 0>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
         "clocks": sampler.summary(),
-        "long_context": long_ctx,
-        "other_paths": others,
-        "decode": decode,
         "cpu_baseline": cpu,
         "parity": parity,
+        "summary": compact_summary(long_ctx, others, decode, parity, sampler.summary()),
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -108,3 +108,52 @@ def test_recorded_traffic_follows_the_kernel_sources(tmp_path):
     assert bench.recorded_traffic(bench.WORKLOAD, str(tmp_path / "missing.json")) is None
     f.write_text("{not json")
     assert bench.recorded_traffic(bench.WORKLOAD, str(f)) is None
+
+
+def _lc(name, ms, tf, frac, ms_seq, tf_seq, frac_seq):
+    return {"workload": name, "ms": ms, "tflops": tf, "frac_of_measured_peak": frac, "ms_per_call_in_sequence": ms_seq,
+            "tflops_in_sequence": tf_seq, "frac_in_sequence": frac_seq,
+            "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"] if "32768" in name else []}}
+
+
+def test_compact_summary_fits_the_stored_tail():
+    """The compact summary carries every configuration's figures in a few
+    hundred bytes, so a record that keeps only the last 1,500 characters of
+    the line still holds them all."""
+    lc = [_lc(n, 0.02, 700.0, 0.36, 0.02, 850.0, 0.437) for n in bench.LONG_CONTEXT]
+    others = []
+    for name in bench._SHORT:
+        for dt in ("f32", "f32tc", "bf16", "e4m3"):
+            e = {"workload": name, "dtype": dt, "ms": 0.123456, "tflops": 123.456}
+            if dt == "f32":
+                e["frac_of_fp32_simt_peak"] = 0.17
+            if dt == "f32tc":
+                e.update(frac_of_tensor_ceiling=0.15, frac_of_fp32_simt_peak=0.8)
+            if dt == "e4m3":
+                e["frac_of_fp8_peak"] = 0.2
+            if name.startswith("window"):
+                e["frac_of_hbm_peak"] = 0.11
+            others.append(e)
+    others = others[:17]  # the bench times 17 such entries
+    decode = [{"workload": f"decode_gqa16x8_d128_k{k}", "us_per_call": 12.34, "frac_of_hbm_peak": 0.4,
+               "clocks": {"sm_mhz": 2070.0, "reasons": []}} for k in (2044, 8192, 32768, 1, 2, 3, 4)]
+    parity = {"layer": 0, "max_abs_o": 0.0077, "mean_abs_o": 0.00021, "max_abs_lse": 1e-6, "within_tolerance": True,
+              "tolerance": {"o_max": 0.02}}
+    summ = bench.compact_summary(lc, others, decode, parity, {"reasons": []})
+    text = json.dumps({"summary": summ})
+    assert len(text) < 1400, len(text)
+    assert set(summ["long_context"]) == {"t2044", "t8192", "t32768"}
+    assert summ["long_context"]["t2044"][5] == 0.437
+    assert len(summ["other_paths"]) == 17 and len(summ["decode"]) == 7
+    assert summ["clocks_all"] == {"sm_mhz_min": 2070.0, "reasons": ["sw_power_cap"]}
+
+
+def test_summary_is_the_last_key_of_the_line():
+    """run_fa builds the line with the verbose records first and the summary
+    last (json.dumps keeps insertion order)."""
+    import inspect
+    src = inspect.getsource(bench.run_fa)
+    body = src[src.index("line = {"):src.index("print(json.dumps(line)")]
+    keys = [k for k in ("\"detail\"", "\"metric\"", "\"cpu_baseline\"", "\"parity\"", "\"summary\"") if k in body]
+    assert keys == ["\"detail\"", "\"metric\"", "\"cpu_baseline\"", "\"parity\"", "\"summary\""]
+    assert body.index("\"summary\"") > body.index("\"parity\"") > body.index("\"cpu_baseline\"")
