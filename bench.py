@@ -885,9 +885,15 @@ def run_only(args, local_rank):
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty(q.shape, dtype=torch.bfloat16 if args.dtype == "e4m3" else dt, device=dev)
     lse = torch.empty((p.B, p.Hq, p.Tq), dtype=torch.float32, device=dev)
+    # The workload's own side inputs: the broadcast additive mask, the sinks.
+    mask = (workloads.strided_mask(w.extra["mask_seed"], p.Tq, p.Tk).to(dev)
+            if "mask_seed" in (w.extra or {}) else None)
+    mstr = (0, 0, p.Tk, 1) if mask is not None else (0, 0, 0, 0)
+    z = workloads.sinks(w.extra["sink_seed"], p.Hq).to(dev) if "sink_seed" in (w.extra or {}) else None
+
     def one_call():
         fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, int(p.causal), p.window,
-                  None, None, 0, 0, 0, 0, code, None)
+                  z, mask, *mstr, code, None)
 
     if args.calls <= 3:
         # few launches (profiling): plain calls, no graph

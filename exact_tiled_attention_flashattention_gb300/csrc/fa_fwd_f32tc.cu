@@ -469,11 +469,28 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, uin
             const int k0 = (U.t_begin + j) * kBN + half * kHK;
             const int elo = min(max(vlo - k0, 0), kHK), ehi = min(max(vhi - k0, 0), kHK);
             if (mrow != nullptr) {
+                if (P.msk == 1 && k0 + kHK <= P.Tk && (reinterpret_cast<uintptr_t>(mrow + k0) & 15) == 0) {
+                    // Contiguous keys, all inside the mask row, 16-byte aligned:
+                    // 16 vector loads instead of 64 scalar ones (same values).
+                    const float4 *m4 = reinterpret_cast<const float4 *>(mrow + k0);
 #pragma unroll
-                for (int e = 0; e < kHK; ++e) {
-                    const int jj = min(k0 + e, P.Tk - 1);
-                    const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
-                    s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                    for (int q4 = 0; q4 < kHK / 4; ++q4) {
+                        const float4 mv = __ldg(m4 + q4);
+                        const float mvals[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int e = 4 * q4 + t;
+                            const float x = fmaf(mvals[t], kLog2e, s[e] * c);
+                            s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kHK; ++e) {
+                        const int jj = min(k0 + e, P.Tk - 1);
+                        const float x = fmaf(__ldg(mrow + (int64_t)jj * P.msk), kLog2e, s[e] * c);
+                        s[e] = (e >= elo && e < ehi) ? x : -INFINITY;
+                    }
                 }
                 cs = 1.f;
             } else if (c <= 0.f) {
