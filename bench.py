@@ -858,7 +858,7 @@ def run_fa(args, rank, world, local_rank):
         "gpu_launches": L * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_burst, 4), "traffic": traffic,
-                     "kernel": "fa_fwd_bf16_kernel<128, 1, 0>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
+                     "kernel": "fa_fwd_bf16_kernel<128, 0>", "peak_kind": f"{peak_kind} bf16 dense (burst)"},
         "clocks": sampler.summary(),
         "cpu_baseline": cpu,
         "parity": parity,
