@@ -238,7 +238,12 @@ def measure_decode(fa, dev, flush, local_rank):
     """Decode steps (Tq = 1 at q_offset = Tk - 1) on the packed-row split-KV
     path: per call in a sequence of calls on distinct inputs, each read cold
     (L2 flushed before the sequence, no input read twice), against the HBM
-    roofline: algorithmic bytes = Q + K + V + O (bf16) + lse (fp32)."""
+    roofline: algorithmic bytes = Q + K + V + O (bf16) + lse (fp32).  Each
+    workload is timed twice: through fa_fwd (the split over one thread-block
+    cluster, partials merged in distributed shared memory) and through
+    fa_fwd_splitkv (the split over every SM, partials merged through a
+    workspace allocated once, outside the timed region, and shared by the
+    calls of the sequence in stream order)."""
     import torch
     peak_gbs, peak_kind = _hbm_peak()
     out = []
@@ -258,16 +263,28 @@ def measure_decode(fa, dev, flush, local_rank):
                 fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, 1, 0, None,
                           None, 0, 0, 0, 0, fa.FA_DTYPE_BF16, None)
 
+        ws_bytes = fa.fa_splitkv_workspace_bytes(p.B, p.Hq, p.Hkv, p.Tq, p.d, fa.FA_DTYPE_BF16)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+        def seq_ws():
+            for q, k, v, o, lse in sets:
+                fa.fa_fwd_splitkv(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, 1, 0,
+                                  None, None, 0, 0, 0, 0, ws, ws_bytes, fa.FA_DTYPE_BF16, None)
+
         sampler = ClockSampler(local_rank)
         med, _ = time_graph(seq, 10, flush)
+        med_ws, _ = time_graph(seq_ws, 10, flush)
         sampler.stop()
-        per_call = med / n_seq
-        gbs = alg / (per_call / 1e3) / 1e9
+        per_call, per_call_ws = med / n_seq, med_ws / n_seq
+        gbs, gbs_ws = alg / (per_call / 1e3) / 1e9, alg / (per_call_ws / 1e3) / 1e9
         out.append({"workload": name, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Tk": p.Tk, "d": p.d,
                     "us_per_call": round(per_call * 1e3, 2), "calls_in_sequence": n_seq,
                     "algorithmic_bytes": alg, "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak_gbs, 4),
+                    "splitkv_workspace": {"us_per_call": round(per_call_ws * 1e3, 2), "gbs": round(gbs_ws, 1),
+                                          "frac_of_hbm_peak": round(gbs_ws / peak_gbs, 4),
+                                          "workspace_bytes": ws_bytes},
                     "hbm_peak_kind": peak_kind, "clocks": sampler.summary()})
-        del sets
+        del sets, ws
     # Paged caches: the keys of each sequence scattered over shuffled pages.
     for name, w in workloads.PAGED.items():
         B, Hq, Hkv, d, ps = w["B"], w["Hq"], w["Hkv"], w["d"], w["page_size"]
@@ -620,8 +637,8 @@ def compact_summary(long_ctx, others, decode, parity, clocks):
     on the tensor cores, of the fp8 peak for e4m3, else of the fp32 SIMT
     peak), decode (us per call, fraction of measured HBM), the parity of the
     timed output, and one clocks record for the whole run."""
-    out = {"legend": "long_context: [us, TF/s, frac] one call, then per call in a sequence; other_paths: "
-                     "[ms, TF/s, frac of the path's own peak]; decode: [us per call, frac of HBM]"}
+    out = {"legend": "long_context: [us,TF/s,frac] 1 call, then per call in a sequence; other_paths: "
+                     "[ms,TF/s,frac of own peak]; decode: [us/call,frac of HBM] fa_fwd, then fa_fwd_splitkv"}
     out["long_context"] = {_SHORT.get(e["workload"], e["workload"]): [
         round(1e3 * e["ms"], 1), round(e["tflops"]), round(e["frac_of_measured_peak"], 3),
         round(1e3 * e["ms_per_call_in_sequence"], 1), round(e["tflops_in_sequence"]), round(e["frac_in_sequence"], 3)]
@@ -633,8 +650,11 @@ def compact_summary(long_ctx, others, decode, parity, clocks):
                                                 "frac_of_fp32_simt_peak") if k in e), None)
         op[key] = [round(e["ms"], 4), round(e["tflops"], 1), frac]
     out["other_paths"] = op
-    out["decode"] = {e["workload"].replace("decode_", "").replace("_gqa16x8_d128", "")[:22]:
-                     [round(e["us_per_call"], 1), round(e["frac_of_hbm_peak"], 3)] for e in decode}
+    out["decode"] = {e["workload"].replace("decode_", "").replace("gqa16x8_d128_", "")[:22]:
+                     [round(e["us_per_call"], 1), round(e["frac_of_hbm_peak"], 3)] +
+                     ([round(e["splitkv_workspace"]["us_per_call"], 1),
+                       round(e["splitkv_workspace"]["frac_of_hbm_peak"], 3)] if "splitkv_workspace" in e else [])
+                     for e in decode}
     if parity:
         out["parity"] = {k: (round(v, 5) if isinstance(v, float) else v) for k, v in parity.items()
                          if k in ("max_abs_o", "mean_abs_o", "max_abs_lse", "within_tolerance", "error")}
@@ -891,9 +911,16 @@ def run_only(args, local_rank):
     mstr = (0, 0, p.Tk, 1) if mask is not None else (0, 0, 0, 0)
     z = workloads.sinks(w.extra["sink_seed"], p.Hq).to(dev) if "sink_seed" in (w.extra or {}) else None
 
+    ws_bytes = fa.fa_splitkv_workspace_bytes(p.B, p.Hq, p.Hkv, p.Tq, p.d, code) if args.splitkv else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if args.splitkv else None
+
     def one_call():
-        fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, int(p.causal), p.window,
-                  z, mask, *mstr, code, None)
+        if args.splitkv:
+            fa.fa_fwd_splitkv(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset,
+                              int(p.causal), p.window, z, mask, *mstr, ws, ws_bytes, code, None)
+        else:
+            fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Tq, p.Tk, p.d, p.sm_scale, p.q_offset, int(p.causal),
+                      p.window, z, mask, *mstr, code, None)
 
     if args.calls <= 3:
         # few launches (profiling): plain calls, no graph
@@ -924,6 +951,7 @@ def main():
     ap.add_argument("--only", choices=sorted({**workloads.CONFIGS, **workloads.DECODE}),
                     help="profiling driver: one workload only")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--splitkv", action="store_true", help="--only: call fa_fwd_splitkv (workspace split-KV)")
     ap.add_argument("--dtype", choices=["bf16", "f32", "f32tc", "e4m3"], default="bf16",
                     help="--only: bf16, fp32 on the SIMT cores, fp32 on the tensor cores (three products per "
                          "matrix product), or e4m3")

@@ -17,7 +17,8 @@ from pathlib import Path
 
 __all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_ETIMEOUT", "FA_DTYPE_F32",
            "FA_DTYPE_BF16", "FA_DTYPE_F32_TC", "FA_DTYPE_FP8_E4M3", "FaError", "fa_fwd", "fa_last_error",
-           "fa_version", "fa_device_status", "fa_test_drop_arrive", "fa_test_max_ctas", "attention", "library_path", "load"]
+           "fa_version", "fa_device_status", "fa_test_drop_arrive", "fa_test_max_ctas", "attention", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes",
+           "splitkv_attention", "library_path", "load"]
 
 FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA, FA_ETIMEOUT = 0, 1, 2, 3, 4, 5
 FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F32_TC, FA_DTYPE_FP8_E4M3 = 0, 1, 2, 3
@@ -60,6 +61,12 @@ def load():
     lib.fa_fwd_varlen.restype = ctypes.c_int
     lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, i64, i64, i64, i64] + [i64] * 8 + [
         ctypes.c_float, ctypes.c_int, i64, vp, ctypes.c_int, vp]
+    lib.fa_fwd_splitkv.restype = ctypes.c_int
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_float, i64,
+                                   ctypes.c_int, i64, vp, vp, i64, i64, i64, i64, vp, ctypes.c_size_t, ctypes.c_int,
+                                   vp]
+    lib.fa_splitkv_workspace_bytes.restype = ctypes.c_int
+    lib.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, vp]
     lib.fa_last_error.restype = ctypes.c_char_p
     lib.fa_last_error.argtypes = []
     lib.fa_version.restype = ctypes.c_int
@@ -177,6 +184,61 @@ def fa_fwd_strided(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, q_strides, k_strides,
     if check and st != FA_OK:
         raise FaError(st, lib.fa_last_error().decode())
     return st
+
+
+def fa_splitkv_workspace_bytes(B, Hq, Hkv, Tq, d, dtype) -> int:
+    """Bytes of device workspace that fa_fwd_splitkv needs for these sizes on
+    the current device (0 when the call takes the plain fa_fwd path)."""
+    lib = load()
+    n = ctypes.c_size_t(0)
+    st = lib.fa_splitkv_workspace_bytes(int(B), int(Hq), int(Hkv), int(Tq), int(d), int(dtype), ctypes.addressof(n))
+    if st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return int(n.value)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, scale, q_offset, causal, window, sinks, mask, mask_sb,
+                   mask_sh, mask_sq, mask_sk, workspace, workspace_bytes, dtype, stream=None, *, check=True) -> int:
+    """Call the split-KV C entry point (contiguous tensors, a caller-owned
+    device workspace); raises FaError on a non-OK status when ``check``."""
+    lib = load()
+    st = lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv), int(Tq),
+                            int(Tk), int(d), float(scale), int(q_offset), int(bool(causal)), int(window), _ptr(sinks),
+                            _ptr(mask), int(mask_sb), int(mask_sh), int(mask_sq), int(mask_sk), _ptr(workspace),
+                            int(workspace_bytes), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+def splitkv_attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=None, mask=None,
+                      mask_strides=(0, 0, 0, 0), workspace=None, out=None, lse_out=None, stream=None):
+    """Decode attention through fa_fwd_splitkv for contiguous bf16 CUDA
+    tensors q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d]; returns (o, lse).  ``workspace``
+    is a uint8 CUDA tensor of at least fa_splitkv_workspace_bytes bytes (one
+    is allocated with torch when None)."""
+    import torch
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    _check_tensors(q.device, k=k, v=v, out=out, lse_out=lse_out, sinks=sinks, mask=mask, workspace=workspace)
+    _check_f32("sinks", sinks, Hq)
+    _check_f32("mask", mask)
+    if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must be bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v)) + ((("out", out),) if out is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    with torch.cuda.device(q.device):
+        need = fa_splitkv_workspace_bytes(B, Hq, Hkv, Tq, d, FA_DTYPE_BF16)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        nbytes = workspace.numel() * workspace.element_size()
+        o = out if out is not None else torch.empty((B, Hq, Tq, d), dtype=torch.bfloat16, device=q.device)
+        lse = lse_out if lse_out is not None else torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+        sc = (1.0 / d ** 0.5) if scale is None else scale
+        fa_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, sc, q_offset, causal, window, sinks, mask,
+                       *mask_strides, workspace, nbytes, FA_DTYPE_BF16, stream)
+    return o, lse
 
 
 def attention(q, k, v, *, scale=None, q_offset=0, causal=True, window=0, sinks=None, mask=None,

@@ -121,7 +121,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
                    int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, const int64_t *qs, const int64_t *ks,
                    const int64_t *vs, const int64_t *os, float scale, int64_t q_offset, int causal, int64_t window,
                    const float *sinks, const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq,
-                   int64_t mask_sk, int dtype, void *stream) {
+                   int64_t mask_sk, int dtype, void *stream, bool splitkv = false, void *workspace = nullptr,
+                   size_t workspace_bytes = 0) {
     g_last_error[0] = '\0';
     if (!known_dtype(dtype)) return fail(FA_EINVAL, "unknown dtype %d", dtype);
     if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || Tk < 0 || d < 0)
@@ -236,6 +237,18 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     P.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (splitkv && dtype == FA_DTYPE_BF16) {
+        const size_t need = fa::splitkv_workspace_bytes(P.B, P.Hkv, P.group, P.Tq, P.d);
+        if (need > 0) {
+            if (workspace == nullptr || workspace_bytes < need)
+                return fail(FA_EINVAL, "fa_fwd_splitkv: the workspace needs %zu bytes (got %zu%s)", need,
+                            workspace_bytes, workspace == nullptr ? ", NULL" : "");
+            if (!aligned16(workspace)) return fail(FA_EINVAL, "fa_fwd_splitkv: the workspace must be 16-byte aligned");
+            const cudaError_t e = fa::launch_bf16_splitkv(P, workspace, s);
+            if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
+            return FA_OK;
+        }
+    }
     cudaError_t e = dtype == FA_DTYPE_F32      ? fa::launch_f32(P, s)
                     : dtype == FA_DTYPE_BF16   ? fa::launch_bf16(P, s)
                     : dtype == FA_DTYPE_F32_TC ? fa::launch_f32_tc(P, s)
@@ -245,6 +258,38 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
 }
 
 }  // namespace
+
+extern "C" fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t d,
+                                                int dtype, size_t *bytes) {
+    g_last_error[0] = '\0';
+    if (bytes == nullptr) return fail(FA_EINVAL, "fa_splitkv_workspace_bytes: bytes is NULL");
+    *bytes = 0;
+    if (!known_dtype(dtype)) return fail(FA_EINVAL, "unknown dtype %d", dtype);
+    if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || d < 0) return fail(FA_EINVAL, "negative size");
+    if (Hkv == 0 ? Hq > 0 : (Hkv > Hq || Hq % Hkv != 0))
+        return fail(FA_ESHAPE, "Hq=%lld is not a multiple of Hkv=%lld (or Hkv > Hq)", (long long)Hq,
+                    (long long)Hkv);
+    if (dtype != FA_DTYPE_BF16 || B == 0 || Hq == 0 || Tq == 0 || d == 0) return FA_OK;  // no workspace
+    if (Tq >= kMaxLen || d > 128) return FA_OK;  // not a call fa_fwd_splitkv accepts
+    if (B > 0x7fffffff / Hq) return fail(FA_EUNSUPPORTED, "B*Hq must be below 2^31");
+    *bytes = fa::splitkv_workspace_bytes((int)B, (int)Hkv, (int)(Hq / Hkv), (int)Tq, (int)d);
+    return FA_OK;
+}
+
+extern "C" fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                                    int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, float scale,
+                                    int64_t q_offset, int causal, int64_t window, const float *sinks,
+                                    const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq,
+                                    int64_t mask_sk, void *workspace, size_t workspace_bytes, int dtype,
+                                    void *stream) {
+    // Contiguous [B, H, T, d], as in fa_fwd.
+    const uint64_t uq = (uint64_t)(Tq < 0 ? 0 : Tq) * (uint64_t)(d < 0 ? 0 : d);
+    const uint64_t uk = (uint64_t)(Tk < 0 ? 0 : Tk) * (uint64_t)(d < 0 ? 0 : d);
+    const int64_t qs[3] = {(int64_t)(uq * (uint64_t)(Hq < 0 ? 0 : Hq)), (int64_t)uq, d},
+                  ks[3] = {(int64_t)(uk * (uint64_t)(Hkv < 0 ? 0 : Hkv)), (int64_t)uk, d};
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, qs, ks, ks, qs, scale, q_offset, causal, window, sinks,
+                    mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream, true, workspace, workspace_bytes);
+}
 
 extern "C" fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                                     int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d, int64_t q_sb,

@@ -111,7 +111,16 @@ constexpr int kMaxStages = 6;
 //             elements per K step), P is rounded to e4m3 (four per tensor-
 //             memory column), O stays bf16.
 //   kVarlen8  kVarlen with e4m3 Q, K and V, as kPrefill8.
-constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3, kPrefill8 = 4, kVarlen8 = 5;
+//   kSplitKv  kDecode without a cluster: the key range of a KV head is split
+//             over as many CTAs as fill the SMs, each CTA writes its partial
+//             (m, l, O) to a workspace in global memory, and the last CTA of
+//             the KV head to finish (a counter per KV head) merges them.
+constexpr int kPrefill = 0, kDecode = 1, kPaged = 2, kVarlen = 3, kPrefill8 = 4, kVarlen8 = 5, kSplitKv = 6;
+__host__ __device__ constexpr bool is_packed(int mode) { return mode == kDecode || mode == kPaged || mode == kSplitKv; }
+// One split's block of the split-KV workspace: R rows of D fp32 (unnormalised
+// O), then R (m, l) pairs, padded to a multiple of 4 floats so that every
+// block starts on a 16-byte boundary (the rows are written and read as float4).
+__host__ __device__ constexpr int64_t ws_block_floats(int R, int D) { return ((int64_t)R * (D + 2) + 3) & ~int64_t(3); }
 __host__ __device__ constexpr bool is_prefill(int mode) { return mode == kPrefill || mode == kPrefill8; }
 __host__ __device__ constexpr bool is_varlen(int mode) { return mode == kVarlen || mode == kVarlen8; }
 __host__ __device__ constexpr int elem_bytes(int mode) {  // Q, K, V
@@ -160,6 +169,7 @@ struct Barriers {
     uint64_t drain[2];                                 // issuers' last MMAs completed
     uint32_t tmem_base;
     int abort;
+    int last;  // split-KV through the workspace: this CTA merges its KV head
 };
 
 
@@ -266,7 +276,7 @@ __device__ __forceinline__ Unit decode_unit(const Params &P) {
 
 template <int MODE>
 __device__ __forceinline__ Unit get_unit(const Params &P, int u) {
-    if constexpr (MODE == kDecode || MODE == kPaged)
+    if constexpr (is_packed(MODE))
         return decode_unit<MODE>(P);
     else
         return make_unit<MODE>(P, u);
@@ -284,7 +294,7 @@ struct Schedule {
 
 template <int MODE>
 __device__ __forceinline__ Schedule make_schedule(const Params &P) {
-    if constexpr (MODE == kDecode || MODE == kPaged) return Schedule{1, 1, 0};  // one unit per CTA
+    if constexpr (is_packed(MODE)) return Schedule{1, 1, 0};  // one unit per CTA
     const int nqt = (P.Tq + kBM - 1) / kBM;
     return Schedule{nqt * P.B * P.Hq, (int)gridDim.x, (int)blockIdx.x};
 }
@@ -436,7 +446,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         auto load_q = [&]() {
             if (q_issued == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0) {
                 // test hook: no Q load, no arrival on q_full
-            } else if constexpr (MODE == kDecode || MODE == kPaged) {
+            } else if constexpr (is_packed(MODE)) {
                 // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
                 mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(L::kBoxes * P.group * P.Tq) * kSwRowBytes);
 #pragma unroll
@@ -620,7 +630,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
         const int uTq = is_varlen(MODE) ? U.Tq : P.Tq;
         if (is_varlen(MODE) && U.r0 >= uTq) continue;  // a tile past the sequence's rows
         int64_t p_first = (int64_t)uq0 + U.r0, p_last = (int64_t)uq0 + min(U.r0 + kBM, uTq) - 1;
-        if constexpr (MODE == kDecode || MODE == kPaged) {
+        if constexpr (is_packed(MODE)) {
             live = row < P.group * P.Tq;
             const int iq = (int)P.fd_group.div((uint32_t)row);  // row = i * group + hl
             const int hl = live ? row - iq * P.group : 0;
@@ -821,7 +831,33 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_final, units & 1, abort)))) break;
             tc_fence_after();
         }
-        if constexpr (MODE == kDecode || MODE == kPaged) {
+        if constexpr (MODE == kSplitKv) {
+            // This CTA's partial result over its share of the keys into its
+            // block of the workspace: unnormalised O, [R rows][D] fp32, then
+            // (m, l) per row (R = group * Tq).
+            const int S = P.splits, cid = (int)P.fd_splits.div(blockIdx.x), rank = (int)blockIdx.x - cid * S;
+            const int R = P.group * P.Tq;
+            float *blk = P.ws + ((int64_t)cid * S + rank) * ws_block_floats(R, D);
+#pragma unroll
+            for (int cc = 0; cc < kHD; cc += 32) {
+                uint32_t ov[32];
+                if (n > 0) {
+                    tmem_load_pair32<kHD>(o_addr + cc, ov);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                }
+                if (live) {
+                    float4 *dst = reinterpret_cast<float4 *>(blk + row * D + half * kHD + cc);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        __stcg(dst + e, make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                                    __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3])));
+                }
+            }
+            if (n > 0) tc_fence_before();
+            if (live && half == 0) __stcg(reinterpret_cast<float2 *>(blk + R * D) + row, make_float2(m, lt));
+        } else if constexpr (MODE == kDecode || MODE == kPaged) {
             // This CTA's partial result over its share of the keys:
             // unnormalised O (fp32, rows of kOPartStride floats) and (m, l) per
             // row, in the K/V ring space (no copy or MMA is in flight any
@@ -966,6 +1002,70 @@ __device__ __forceinline__ void merge_partials(const Params &P, uint8_t *smem) {
     }
 }
 
+// The split-KV merge through global memory, run by the last CTA of a KV head
+// to finish: the same rescale as merge_partials over the S partials of the
+// workspace (M = max m_s, w_s = 2^(m_s - M), o = sum w_s O_s / sum w_s l_s,
+// lse = (M + log2 sum w_s l_s) ln 2), the partials taken in split order.
+// The per-row weights are formed once (the (row, split) pairs spread over
+// the threads, the reductions in split order in shared memory, over the K
+// ring), then every thread merges 4 columns of a row at a time.  The
+// workspace was written by other CTAs of this grid: it is read through L2
+// (ld.global.cg), never through L1.
+template <int D>
+__device__ __forceinline__ void merge_partials_ws(const Params &P, uint8_t *smem) {
+    using L = SmemLayout<D, kSplitKv>;
+    const int S = P.splits, cid = (int)P.fd_splits.div(blockIdx.x);
+    const int R = P.group * P.Tq;
+    const int b = (int)P.fd_hkv.div((uint32_t)cid), g = cid - b * P.Hkv;
+    const int64_t bstride = ws_block_floats(R, D);
+    const float *blk0 = P.ws + (int64_t)cid * S * bstride;
+    float *mls = reinterpret_cast<float *>(smem + L::kKRing);  // [S][R] (m, l) pairs, then weights [S][R]
+    float *wts = mls + 2 * S * R;
+    float *rowM = wts + S * R, *rowL = rowM + R;
+    for (int t = (int)threadIdx.x; t < S * R; t += kThreads) {
+        const int sp = t / R, row = t - sp * R;
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(blk0 + sp * bstride + R * D) + row);
+        mls[2 * t] = ml.x;
+        mls[2 * t + 1] = ml.y;
+    }
+    __syncthreads();
+    for (int row = (int)threadIdx.x; row < R; row += kThreads) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, mls[2 * (sp * R + row)]);
+        float lsum = 0.f;
+        for (int sp = 0; sp < S; ++sp) {
+            const float m = mls[2 * (sp * R + row)], l = mls[2 * (sp * R + row) + 1];
+            const float w = m == M ? 1.f : ex2_approx(m - M);  // 0 for an empty partial
+            wts[sp * R + row] = w;
+            lsum = sp == 0 ? w * l : fmaf(w, l, lsum);
+        }
+        rowM[row] = M;
+        rowL[row] = lsum;
+    }
+    __syncthreads();
+    const int q4 = P.d / 4;  // 4-column groups of a row (d is a multiple of 8)
+    for (int e = (int)threadIdx.x; e < R * q4; e += kThreads) {
+        const int row = e / q4, col = 4 * (e - row * q4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int sp = 0; sp < S; ++sp) {
+            const float w = wts[sp * R + row];
+            const float4 ov = __ldcg(reinterpret_cast<const float4 *>(blk0 + sp * bstride + row * D + col));
+            acc = sp == 0 ? make_float4(w * ov.x, w * ov.y, w * ov.z, w * ov.w)
+                          : make_float4(fmaf(w, ov.x, acc.x), fmaf(w, ov.y, acc.y), fmaf(w, ov.z, acc.z),
+                                        fmaf(w, ov.w, acc.w));
+        }
+        const float lsum = rowL[row];
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const int i = (int)P.fd_group.div((uint32_t)row), h = g * P.group + (row - i * P.group);
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(P.o) + b * P.o_sb + h * P.o_sh + (int64_t)i * P.o_st + col;
+        const uint2 w2 = make_uint2(cvt_bf16x2(acc.x * inv, acc.y * inv), cvt_bf16x2(acc.z * inv, acc.w * inv));
+        *reinterpret_cast<uint2 *>(dst) = w2;
+        if (col == 0 && P.lse != nullptr)
+            P.lse[((int64_t)b * P.Hq + h) * P.Tq + i] = lsum > 0.f ? (rowM[row] + lg2_approx(lsum)) * kLn2 : -INFINITY;
+    }
+}
+
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -1034,6 +1134,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();  // every CTA's partial is written
         if (!bar.abort) merge_partials<D>(P, smem);
         cluster_sync();  // no CTA leaves while a peer reads its partial
+    } else if constexpr (MODE == kSplitKv) {
+        // Every thread's workspace writes are visible device-wide before the
+        // CTA is counted; the CTA that completes its KV head's count merges.
+        __threadfence();
+        __syncthreads();
+        const int cid = (int)P.fd_splits.div(blockIdx.x);
+        if (threadIdx.x == 0) bar.last = atomicAdd(P.ws_cnt + cid, 1u) == (unsigned)(P.splits - 1) ? 1 : 0;
+        __syncthreads();
+        if (bar.last) {
+            __threadfence();
+            if (!bar.abort) merge_partials_ws<D>(P, smem);
+        }
     }
     if (bar.abort && threadIdx.x == 0) atomicOr(&g_watchdog, 1u);
     if (warp == kWarpQk) {
@@ -1235,6 +1347,69 @@ cudaError_t bf16_watchdog(cudaStream_t stream, unsigned int *flag) {
 
 cudaError_t bf16_set_drop_arrive(int on) { return cudaMemcpyToSymbol(g_drop_arrive, &on, sizeof on); }
 
+// Split-KV through the workspace: splits per (batch, KV head) so that the
+// grid fills the SMs once (at most kMaxSplitsWs, at least two key tiles per
+// CTA, at least 1).
+constexpr int kMaxSplitsWs = 64;
+
+int splitkv_splits(int units, int sms) {
+    int S = units > 0 ? sms / units : 1;
+    return S < 1 ? 1 : (S > kMaxSplitsWs ? kMaxSplitsWs : S);
+}
+
+size_t counters_bytes(int units) { return ((size_t)units * sizeof(unsigned int) + 255) / 256 * 256; }
+
+template <int D>
+cudaError_t launch_splitkv_d(const Params &P0, void *workspace, cudaStream_t stream) {
+    constexpr int MODE = kSplitKv;
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    Params P = P0;
+    const int n = packed_tiles(P, P.Tk, P.q_offset);
+    CUtensorMap tq, tk, tv, to;
+    bool ok = make_packed_map(enc, &tq, P.q, P, P.q_st, P.q_sh, P.q_sb) &&
+              // to is not used by the packed path (O leaves through the merge).
+              make_map(enc, &to, P.o, P.d, P.Tq, P.Hq, P.B, P.o_st, P.o_sh, P.o_sb, kBM) &&
+              make_kv_maps(enc, &tk, &tv, P, kBN);
+    if (!ok) return cudaErrorInvalidValue;
+    constexpr size_t kSmem = SmemLayout<D, MODE>::kTotal + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert((3 * kMaxSplitsWs + 2) * kBM * 4 <= 2 * SmemLayout<D, MODE>::kStages * SmemLayout<D, MODE>::kKVBytes,
+                  "the merge's per-row weights fit the K/V rings");
+    auto kernel = fa_fwd_bf16_kernel<D, MODE>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int units = P.B * P.Hkv;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    int S = splitkv_splits(units, sms);
+    if (S > n / 2) S = n / 2 > 1 ? n / 2 : 1;  // at least two key tiles per CTA
+    P.splits = S;
+    P.fd_splits = FastDiv::make((uint32_t)S);
+    P.fd_hkv = FastDiv::make((uint32_t)P.Hkv);
+    P.fd_group = FastDiv::make((uint32_t)P.group);
+    P.fd_d = FastDiv::make((uint32_t)P.d);
+    P.ws_cnt = static_cast<unsigned int *>(workspace);
+    P.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters_bytes(units));
+    cudaError_t e = cudaMemsetAsync(P.ws_cnt, 0, (size_t)units * sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, P);
+}
+
 cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream) {
     return P.d <= 64 ? launch_packed<64, kPaged>(P, stream) : launch_packed<128, kPaged>(P, stream);
 }
@@ -1256,6 +1431,18 @@ cudaError_t launch_bf16(const Params &P, cudaStream_t stream) {
     if ((int64_t)P.group * P.Tq <= kBM)
         return P.d <= 64 ? launch_packed<64, kDecode>(P, stream) : launch_packed<128, kDecode>(P, stream);
     return P.d <= 64 ? launch_d<64, kPrefill>(P, stream) : launch_d<128, kPrefill>(P, stream);
+}
+
+size_t splitkv_workspace_bytes(int B, int Hkv, int group, int Tq, int d) {
+    if ((int64_t)group * Tq > kBM || B <= 0 || Hkv <= 0 || Tq <= 0 || d <= 0) return 0;
+    const int units = B * Hkv, D = d <= 64 ? 64 : 128;
+    const int S = splitkv_splits(units, sm_count());
+    return counters_bytes(units) + (size_t)units * S * (size_t)ws_block_floats(group * Tq, D) * sizeof(float);
+}
+
+cudaError_t launch_bf16_splitkv(const Params &P, void *workspace, cudaStream_t stream) {
+    if ((int64_t)P.group * P.Tq > kBM) return launch_bf16(P, stream);  // not a packed-row call: no workspace
+    return P.d <= 64 ? launch_splitkv_d<64>(P, workspace, stream) : launch_splitkv_d<128>(P, workspace, stream);
 }
 
 }  // namespace fa

@@ -41,6 +41,11 @@ struct Params {
     // v; its queries are its last positions.  Tq / Tk hold the maxima.
     const int *cu_q, *cu_k;
     int total_q, total_k;
+    // Split-KV through a workspace (bf16 packed rows, fa_fwd_splitkv): the
+    // partials [B * Hkv][splits][R rows][D + 2] fp32 (R = group * Tq, D = 64
+    // or 128: O, then (m, l) per row) and one counter per (batch, KV head).
+    float *ws;
+    unsigned int *ws_cnt;
     // Divisors of the tcgen05 kernel's index arithmetic, set by its launchers:
     // units per query tile, heads per unit row (Hq, or Hq / 2 with CTA
     // pairs), the GQA group, the split count, Hkv and d.
@@ -68,6 +73,14 @@ cudaError_t launch_fp8(const Params &P, cudaStream_t stream);
 cudaError_t launch_fp8_varlen(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_paged(const Params &P, cudaStream_t stream);
 cudaError_t launch_bf16_varlen(const Params &P, cudaStream_t stream);
+// Packed-row calls (group * Tq <= 128) with their key ranges split over as
+// many CTAs as fill the SMs, merged through a workspace of
+// splitkv_workspace_bytes(P) bytes (see fa_fwd_splitkv).  The launcher
+// clears the counters on `stream` before the kernel.
+cudaError_t launch_bf16_splitkv(const Params &P, void *workspace, cudaStream_t stream);
+// Bytes of that workspace for calls of this shape on the current device (0
+// if the call does not take the packed-row mapping).
+size_t splitkv_workspace_bytes(int B, int Hkv, int group, int Tq, int d);
 cudaError_t launch_f32_varlen(const Params &P, cudaStream_t stream);
 
 // Device watchdog words: nonzero once a bounded wait of the kernel ran out.

@@ -79,6 +79,7 @@
 #define FA_GB300_FA_H
 
 #include <stdint.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -167,6 +168,45 @@ fa_status fa_fwd_paged(const void *q, const void *k_cache, const void *v_cache, 
                        int64_t page_size, int64_t num_pages,
                        float scale, int causal, int64_t window, const float *sinks,
                        int dtype, void *stream);
+
+/* Split-KV decode through a caller-owned workspace (Flash-Decoding, named on
+ * "FlashAttention forward in C", section 5, beside the fixed tile order: long
+ * contexts are split across thread blocks and the partial (m, l, a) merged
+ * with the same rescale, which trades invariance for parallelism).  Same
+ * arguments, layout and result as fa_fwd.  When every query row of a KV group
+ * fits one 128-row tile ((Hq / Hkv) * Tq <= 128) and dtype is bf16, each
+ * (batch, KV head) is split over S CTAs (S = SM count / (B * Hkv), 1..64, at
+ * least two key tiles each), not over one thread-block cluster as fa_fwd
+ * does: every SM gets work however few KV heads there are.  Each CTA writes
+ * its unnormalised fp32 O and (m, l) per row into the workspace; the last CTA
+ * of a KV head to finish merges them, in split order, into o and lse.  Other
+ * calls (other dtypes, larger groups) run exactly as fa_fwd and ignore the
+ * workspace.
+ *   workspace        device memory of at least the size that
+ *                    fa_splitkv_workspace_bytes reports for these sizes,
+ *                    16-byte aligned, owned by the caller; its contents
+ *                    before and after the call are scratch.  A call clears
+ *                    the counters it uses (a memset on `stream`) before its
+ *                    kernel, so the same workspace serves any number of
+ *                    calls in stream order; calls that run at the same time
+ *                    need separate workspaces.
+ * The split count depends on B * Hkv and the SM count, so results agree with
+ * fa_fwd within rounding, not bit for bit, and are not batch-invariant.
+ * Errors as fa_fwd, plus FA_EINVAL for a NULL, short or unaligned workspace
+ * when the call needs one. */
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d,
+                         float scale, int64_t q_offset, int causal, int64_t window,
+                         const float *sinks,
+                         const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq, int64_t mask_sk,
+                         void *workspace, size_t workspace_bytes, int dtype, void *stream);
+
+/* The workspace size in bytes that fa_fwd_splitkv needs for these sizes on
+ * the current device (0 when the call takes another path).  Host-only; it
+ * reads the device's SM count once.  FA_EINVAL for NULL `bytes`, an unknown
+ * dtype or a negative size; FA_ESHAPE when Hq is not a multiple of Hkv. */
+fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t d, int dtype,
+                                     size_t *bytes);
 
 /* A variable-length batch: B sequences packed along the rows of q, o
  * ([total_q, Hq, d]) and k, v ([total_k, Hkv, d]), element (t, h, x) of q at

@@ -137,6 +137,8 @@ def test_compact_summary_fits_the_stored_tail():
     others = others[:17]  # the bench times 17 such entries
     decode = [{"workload": f"decode_gqa16x8_d128_k{k}", "us_per_call": 12.34, "frac_of_hbm_peak": 0.4,
                "clocks": {"sm_mhz": 2070.0, "reasons": []}} for k in (2044, 8192, 32768, 1, 2, 3, 4)]
+    for e in decode[:4]:  # the contiguous decode steps are also timed through fa_fwd_splitkv
+        e["splitkv_workspace"] = {"us_per_call": 10.5, "frac_of_hbm_peak": 0.612}
     parity = {"layer": 0, "max_abs_o": 0.0077, "mean_abs_o": 0.00021, "max_abs_lse": 1e-6, "within_tolerance": True,
               "tolerance": {"o_max": 0.02}}
     summ = bench.compact_summary(lc, others, decode, parity, {"reasons": []})
@@ -145,6 +147,7 @@ def test_compact_summary_fits_the_stored_tail():
     assert set(summ["long_context"]) == {"t2044", "t8192", "t32768"}
     assert summ["long_context"]["t2044"][5] == 0.437
     assert len(summ["other_paths"]) == 17 and len(summ["decode"]) == 7
+    assert summ["decode"]["k2044"] == [12.3, 0.4, 10.5, 0.612]
     assert summ["clocks_all"] == {"sm_mhz_min": 2070.0, "reasons": ["sw_power_cap"]}
 
 

@@ -92,10 +92,11 @@ def _header_signatures():
 def test_ctypes_argument_lists_match_the_header():
     import ctypes
     lib = fa.load()
-    want = {"ptr": ctypes.c_void_p, "int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float}
+    want = {"ptr": ctypes.c_void_p, "int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float,
+            "size_t": ctypes.c_size_t}
     sigs = _header_signatures()
     assert {"fa_fwd", "fa_fwd_strided", "fa_fwd_paged", "fa_fwd_varlen", "fa_last_error", "fa_version",
-            "fa_device_status", "fa_test_drop_arrive"} <= set(sigs)
+            "fa_device_status", "fa_test_drop_arrive", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes"} <= set(sigs)
     for name, types in sigs.items():
         got = getattr(lib, name).argtypes
         assert got is not None, name

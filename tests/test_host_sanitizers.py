@@ -52,6 +52,19 @@ FA_STUB(launch_fp8_varlen, 128)
 FA_STUB(launch_bf16_paged, 128)
 FA_STUB(launch_bf16_varlen, 128)
 FA_STUB(launch_f32_varlen, 64)
+cudaError_t launch_bf16_splitkv(const Params &P, void *, cudaStream_t) {
+    g_last = P; ++g_calls; grid_ok(P, 128); return cudaSuccess;
+}
+// The sizing rule of the real launcher with a fixed SM count of 152.
+size_t splitkv_workspace_bytes(int B, int Hkv, int group, int Tq, int d) {
+    if ((long long)group * Tq > 128 || B <= 0 || Hkv <= 0 || Tq <= 0 || d <= 0) return 0;
+    const long long units = (long long)B * Hkv;
+    if (units > 0x7fffffffll) { ++g_bad_grids; return 0; }
+    long long S = 152 / units;
+    S = S < 1 ? 1 : (S > 64 ? 64 : S);
+    const long long blk = ((long long)group * Tq * ((d <= 64 ? 64 : 128) + 2) + 3) / 4 * 4;  // 16-byte blocks
+    return (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * S * blk * 4;
+}
 cudaError_t bf16_watchdog(cudaStream_t, unsigned int *f) { *f = 0; return cudaSuccess; }
 cudaError_t f32tc_watchdog(cudaStream_t, unsigned int *f) { *f = 0; return cudaSuccess; }
 cudaError_t bf16_set_drop_arrive(int) { return cudaSuccess; }
@@ -134,7 +147,15 @@ int main() {
                            pick(), pick(), pick(), pick(), scale(), (int)(next() & 1), pick(), nullptr, dtype,
                            nullptr);
         check("fa_fwd_varlen", st, c);
-        n += 4;
+        c = fa::g_calls;
+        st = fa_fwd_splitkv(ptr(), ptr(), ptr(), out, lse, pick(), pick(), pick(), pick(), pick(), pick(), scale(),
+                            pick(), (int)(next() & 1), pick(), nullptr, nullptr, 0, 0, 0, 0,
+                            (next() & 1) ? (void *)ptr() : nullptr, (size_t)pick(), dtype, nullptr);
+        check("fa_fwd_splitkv", st, c);
+        size_t ws = 0;
+        st = fa_splitkv_workspace_bytes(pick(), pick(), pick(), pick(), pick(), dtype, (next() & 7) ? &ws : nullptr);
+        check("fa_splitkv_workspace_bytes", st, fa::g_calls);
+        n += 6;
     }
     // Arguments that pass the earlier checks and reach the products of the
     // later ones: a page size near 2^62 with no pages, a varlen batch whose
@@ -164,6 +185,28 @@ int main() {
         fa::g_last.group != 2 || fa::g_last.Tq != 511) {
         std::printf("valid call: status %d, %s\n", (int)st, fa_last_error());
         ++bad;
+    }
+    // Split-KV: a decode step needs the size the query reports; one byte less
+    // is refused before any launch, the exact size reaches the launcher.
+    {
+        size_t need = 0;
+        fa_status st = fa_splitkv_workspace_bytes(2, 16, 8, 1, 128, FA_DTYPE_BF16, &need);
+        void *ws = reinterpret_cast<void *>(0x400000);
+        int c = fa::g_calls;
+        fa_status st2 = fa_fwd_splitkv(a, a, a, out, lse, 2, 16, 8, 1, 4096, 128, 0.088f, 4095, 1, 0, nullptr, nullptr,
+                                       0, 0, 0, 0, ws, need - 1, FA_DTYPE_BF16, nullptr);
+        check("fa_fwd_splitkv (short workspace)", st2, c);
+        if (st != FA_OK || need == 0 || st2 != FA_EINVAL) {
+            std::printf("split-KV sizing: %d %zu %d\n", (int)st, need, (int)st2);
+            ++bad;
+        }
+        c = fa::g_calls;
+        st2 = fa_fwd_splitkv(a, a, a, out, lse, 2, 16, 8, 1, 4096, 128, 0.088f, 4095, 1, 0, nullptr, nullptr, 0, 0, 0,
+                             0, ws, need, FA_DTYPE_BF16, nullptr);
+        if (st2 != FA_OK || fa::g_calls != c + 1 || fa::g_last.Tk != 4096 || fa::g_last.group != 2) {
+            std::printf("split-KV valid call: status %d, %s\n", (int)st2, fa_last_error());
+            ++bad;
+        }
     }
     // fp32 on the SIMT cores: 64-row tiles, so 2^31 tiles come sooner.
     {
