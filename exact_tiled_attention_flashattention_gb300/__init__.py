@@ -17,7 +17,7 @@ from pathlib import Path
 
 __all__ = ["FA_OK", "FA_EINVAL", "FA_ESHAPE", "FA_EUNSUPPORTED", "FA_ECUDA", "FA_ETIMEOUT", "FA_DTYPE_F32",
            "FA_DTYPE_BF16", "FA_DTYPE_F32_TC", "FA_DTYPE_FP8_E4M3", "FaError", "fa_fwd", "fa_last_error",
-           "fa_version", "fa_device_status", "fa_test_drop_arrive", "fa_test_max_ctas", "attention", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes",
+           "fa_version", "fa_device_status", "fa_test_drop_arrive", "fa_test_max_ctas", "attention", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",
            "splitkv_attention", "library_path", "load"]
 
 FA_OK, FA_EINVAL, FA_ESHAPE, FA_EUNSUPPORTED, FA_ECUDA, FA_ETIMEOUT = 0, 1, 2, 3, 4, 5
@@ -65,6 +65,9 @@ def load():
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_float, i64,
                                    ctypes.c_int, i64, vp, vp, i64, i64, i64, i64, vp, ctypes.c_size_t, ctypes.c_int,
                                    vp]
+    lib.fa_fwd_splitkv_noalloc.restype = ctypes.c_int
+    lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ctypes.c_float, i64,
+                                           ctypes.c_int, i64, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
     lib.fa_splitkv_workspace_bytes.restype = ctypes.c_int
     lib.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, vp]
     lib.fa_last_error.restype = ctypes.c_char_p
@@ -206,6 +209,24 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, scale, q_offset, caus
                             int(Tk), int(d), float(scale), int(q_offset), int(bool(causal)), int(window), _ptr(sinks),
                             _ptr(mask), int(mask_sb), int(mask_sh), int(mask_sq), int(mask_sk), _ptr(workspace),
                             int(workspace_bytes), int(dtype), _stream(stream))
+    if check and st != FA_OK:
+        raise FaError(st, lib.fa_last_error().decode())
+    return st
+
+
+FA_SPLITKV_NOALLOC_MAX_SCRATCH = 4 << 20  # bytes of the library's static split-KV scratch per GPU
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, scale, q_offset, causal, window, sinks, mask,
+                           mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream=None, *, check=True) -> int:
+    """Call the C entry point that runs split-KV with the library's static
+    scratch array instead of a workspace (for callers that cannot allocate
+    device memory); raises FaError on a non-OK status when ``check``."""
+    lib = load()
+    st = lib.fa_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
+                                    int(Tq), int(Tk), int(d), float(scale), int(q_offset), int(bool(causal)),
+                                    int(window), _ptr(sinks), _ptr(mask), int(mask_sb), int(mask_sh), int(mask_sq),
+                                    int(mask_sk), int(dtype), _stream(stream))
     if check and st != FA_OK:
         raise FaError(st, lib.fa_last_error().decode())
     return st

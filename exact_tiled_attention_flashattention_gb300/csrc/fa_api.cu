@@ -122,7 +122,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
                    const int64_t *vs, const int64_t *os, float scale, int64_t q_offset, int causal, int64_t window,
                    const float *sinks, const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq,
                    int64_t mask_sk, int dtype, void *stream, bool splitkv = false, void *workspace = nullptr,
-                   size_t workspace_bytes = 0) {
+                   size_t workspace_bytes = 0, bool noalloc = false) {
     g_last_error[0] = '\0';
     if (!known_dtype(dtype)) return fail(FA_EINVAL, "unknown dtype %d", dtype);
     if (B < 0 || Hq < 0 || Hkv < 0 || Tq < 0 || Tk < 0 || d < 0)
@@ -237,6 +237,21 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     P.scale_log2 = (float)((double)scale * 1.4426950408889634);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (noalloc && dtype == FA_DTYPE_BF16) {
+        // The split-KV call of fa_fwd_splitkv with the library's static
+        // scratch array as its workspace; calls that need none run as fa_fwd.
+        const size_t need = fa::splitkv_workspace_bytes(P.B, P.Hkv, P.group, P.Tq, P.d);
+        if (need > 0) {
+            if (need > fa::kNoAllocScratchBytes)
+                return fail(FA_EUNSUPPORTED,
+                            "fa_fwd_splitkv_noalloc: this call needs %zu bytes of scratch, more than the %zu bytes "
+                            "the library holds per GPU; use fa_fwd_splitkv with a workspace of that size",
+                            need, fa::kNoAllocScratchBytes);
+            const cudaError_t e = fa::launch_bf16_splitkv_noalloc(P, s);
+            if (e != cudaSuccess) return fail(FA_ECUDA, "CUDA error: %s", cudaGetErrorString(e));
+            return FA_OK;
+        }
+    }
     if (splitkv && dtype == FA_DTYPE_BF16) {
         const size_t need = fa::splitkv_workspace_bytes(P.B, P.Hkv, P.group, P.Tq, P.d);
         if (need > 0) {
@@ -289,6 +304,22 @@ extern "C" fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v,
                   ks[3] = {(int64_t)(uk * (uint64_t)(Hkv < 0 ? 0 : Hkv)), (int64_t)uk, d};
     return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, qs, ks, ks, qs, scale, q_offset, causal, window, sinks,
                     mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream, true, workspace, workspace_bytes);
+}
+
+static_assert(FA_SPLITKV_NOALLOC_MAX_SCRATCH == fa::kNoAllocScratchBytes, "the header states the array's size");
+
+extern "C" fa_status fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                            int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d,
+                                            float scale, int64_t q_offset, int causal, int64_t window,
+                                            const float *sinks, const float *mask, int64_t mask_sb, int64_t mask_sh,
+                                            int64_t mask_sq, int64_t mask_sk, int dtype, void *stream) {
+    // Contiguous [B, H, T, d], as in fa_fwd.
+    const uint64_t uq = (uint64_t)(Tq < 0 ? 0 : Tq) * (uint64_t)(d < 0 ? 0 : d);
+    const uint64_t uk = (uint64_t)(Tk < 0 ? 0 : Tk) * (uint64_t)(d < 0 ? 0 : d);
+    const int64_t qs[3] = {(int64_t)(uq * (uint64_t)(Hq < 0 ? 0 : Hq)), (int64_t)uq, d},
+                  ks[3] = {(int64_t)(uk * (uint64_t)(Hkv < 0 ? 0 : Hkv)), (int64_t)uk, d};
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, qs, ks, ks, qs, scale, q_offset, causal, window, sinks,
+                    mask, mask_sb, mask_sh, mask_sq, mask_sk, dtype, stream, false, nullptr, 0, true);
 }
 
 extern "C" fa_status fa_fwd_strided(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,

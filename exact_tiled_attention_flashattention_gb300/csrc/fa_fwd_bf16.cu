@@ -63,6 +63,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "fa_internal.h"
 #include "fa_tma_host.h"
@@ -1443,6 +1444,48 @@ size_t splitkv_workspace_bytes(int B, int Hkv, int group, int Tq, int d) {
 cudaError_t launch_bf16_splitkv(const Params &P, void *workspace, cudaStream_t stream) {
     if ((int64_t)P.group * P.Tq > kBM) return launch_bf16(P, stream);  // not a packed-row call: no workspace
     return P.d <= 64 ? launch_splitkv_d<64>(P, workspace, stream) : launch_splitkv_d<128>(P, workspace, stream);
+}
+
+// Scratch for callers that cannot allocate device memory: the split-KV
+// workspace (counters, then the partial blocks) in one array that every GPU
+// loading this library holds until the process exits.  All calls on a device
+// share it and the last call's contents stay in it; the launcher clears the
+// counters before each kernel, and the partial blocks are always written
+// before they are read.  Two calls whose kernels overlap on the GPU (other
+// streams, other host threads) race on it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// g_noalloc_scratch names a host-side stand-in in host code, not device
+// memory: the kernels get the address that cudaGetSymbolAddress returns on
+// the device where they run, looked up once per device with it current.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+cudaError_t noalloc_scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (p == nullptr) return cudaErrorInvalidSymbol;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_bf16_splitkv_noalloc(const Params &P, cudaStream_t stream) {
+    void *scratch = nullptr;
+    const cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    return launch_bf16_splitkv(P, scratch, stream);
 }
 
 }  // namespace fa

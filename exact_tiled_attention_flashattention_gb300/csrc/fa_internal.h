@@ -81,6 +81,12 @@ cudaError_t launch_bf16_splitkv(const Params &P, void *workspace, cudaStream_t s
 // Bytes of that workspace for calls of this shape on the current device (0
 // if the call does not take the packed-row mapping).
 size_t splitkv_workspace_bytes(int B, int Hkv, int group, int Tq, int d);
+// The same split-KV call with its workspace in a static device array of
+// kNoAllocScratchBytes per GPU instead of caller memory (fa_fwd_splitkv_noalloc):
+// the caller checks the size first; the launcher looks up the array's device
+// address on the current device (once per device) and launches.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+cudaError_t launch_bf16_splitkv_noalloc(const Params &P, cudaStream_t stream);
 cudaError_t launch_f32_varlen(const Params &P, cudaStream_t stream);
 
 // Device watchdog words: nonzero once a bounded wait of the kernel ran out.

@@ -208,6 +208,45 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
 fa_status fa_splitkv_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t d, int dtype,
                                      size_t *bytes);
 
+/* Size in bytes of the device array that fa_fwd_splitkv_noalloc uses as its
+ * workspace: 4 MiB, held by every GPU that loads this library until the
+ * process exits. */
+#define FA_SPLITKV_NOALLOC_MAX_SCRATCH ((size_t)4 << 20)
+
+/* fa_fwd_splitkv for callers that must not allocate device memory.  This
+ * entry point is a service of the library; the paper has no counterpart.
+ * Some callers cannot call cudaMalloc or hand out a buffer of their own:
+ *   - an inference engine whose memory planner has already reserved the GPU's
+ *     memory and accounts for every byte;
+ *   - a plugin whose host forbids allocation inside its execute callback;
+ *   - a latency-critical loop where cudaMalloc, which can synchronise the
+ *     device, would stall the pipeline.
+ * They still pass q, k, v, o and lse, with the arguments and layout of fa_fwd.
+ * The split-KV workspace is a static device array of
+ * FA_SPLITKV_NOALLOC_MAX_SCRATCH bytes inside the library.  Neither this call
+ * nor anything it reaches calls cudaMalloc, cudaFree or an allocating library
+ * routine.
+ *   - Size limit: a call whose workspace (fa_splitkv_workspace_bytes) exceeds
+ *     the array fails with FA_EUNSUPPORTED and a message giving both sizes.
+ *     Nothing is launched.  Use fa_fwd_splitkv with a workspace of that size
+ *     instead.  Calls that need no workspace run exactly as fa_fwd.
+ *   - First call on a device: it looks up the array's device address on the
+ *     current device, once per device.  Make that first call before any
+ *     stream capture.
+ *   - Sharing: every call on a device shares the one array, and the array
+ *     keeps whatever the previous call left in it.  Each call clears the
+ *     counters it needs (a memset on `stream`) before its kernel.  Calls in
+ *     stream order are safe.  Calls whose work overlaps on the GPU race on the
+ *     array and give wrong results: other streams, or other host threads on
+ *     the same device.
+ * Results, invariance and other errors are those of fa_fwd_splitkv. */
+fa_status fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t d,
+                                 float scale, int64_t q_offset, int causal, int64_t window,
+                                 const float *sinks,
+                                 const float *mask, int64_t mask_sb, int64_t mask_sh, int64_t mask_sq,
+                                 int64_t mask_sk, int dtype, void *stream);
+
 /* A variable-length batch: B sequences packed along the rows of q, o
  * ([total_q, Hq, d]) and k, v ([total_k, Hkv, d]), element (t, h, x) of q at
  * q[h*q_sh + t*q_st + x] (likewise k, v, o), d contiguous.  Sequence b has the

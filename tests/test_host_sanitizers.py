@@ -55,6 +55,9 @@ FA_STUB(launch_f32_varlen, 64)
 cudaError_t launch_bf16_splitkv(const Params &P, void *, cudaStream_t) {
     g_last = P; ++g_calls; grid_ok(P, 128); return cudaSuccess;
 }
+cudaError_t launch_bf16_splitkv_noalloc(const Params &P, cudaStream_t) {
+    g_last = P; ++g_calls; grid_ok(P, 128); return cudaSuccess;
+}
 // The sizing rule of the real launcher with a fixed SM count of 152.
 size_t splitkv_workspace_bytes(int B, int Hkv, int group, int Tq, int d) {
     if ((long long)group * Tq > 128 || B <= 0 || Hkv <= 0 || Tq <= 0 || d <= 0) return 0;
@@ -152,6 +155,11 @@ int main() {
                             pick(), (int)(next() & 1), pick(), nullptr, nullptr, 0, 0, 0, 0,
                             (next() & 1) ? (void *)ptr() : nullptr, (size_t)pick(), dtype, nullptr);
         check("fa_fwd_splitkv", st, c);
+        c = fa::g_calls;
+        st = fa_fwd_splitkv_noalloc(ptr(), ptr(), ptr(), out, lse, pick(), pick(), pick(), pick(), pick(), pick(),
+                                    scale(), pick(), (int)(next() & 1), pick(), nullptr, nullptr, 0, 0, 0, 0, dtype,
+                                    nullptr);
+        check("fa_fwd_splitkv_noalloc", st, c);
         size_t ws = 0;
         st = fa_splitkv_workspace_bytes(pick(), pick(), pick(), pick(), pick(), dtype, (next() & 7) ? &ws : nullptr);
         check("fa_splitkv_workspace_bytes", st, fa::g_calls);
@@ -205,6 +213,25 @@ int main() {
                              0, ws, need, FA_DTYPE_BF16, nullptr);
         if (st2 != FA_OK || fa::g_calls != c + 1 || fa::g_last.Tk != 4096 || fa::g_last.group != 2) {
             std::printf("split-KV valid call: status %d, %s\n", (int)st2, fa_last_error());
+            ++bad;
+        }
+    }
+    // The static-scratch variant: a call whose workspace exceeds the array is
+    // refused before any launch; a decode step within it is launched.
+    {
+        int c = fa::g_calls;
+        fa_status st = fa_fwd_splitkv_noalloc(a, a, a, out, lse, 200, 128, 8, 8, 4096, 128, 0.088f, 4088, 1, 0,
+                                              nullptr, nullptr, 0, 0, 0, 0, FA_DTYPE_BF16, nullptr);
+        check("fa_fwd_splitkv_noalloc (oversize)", st, c);
+        if (st != FA_EUNSUPPORTED || std::strstr(fa_last_error(), "scratch") == nullptr) {
+            std::printf("oversize no-alloc call: status %d, %s\n", (int)st, fa_last_error());
+            ++bad;
+        }
+        c = fa::g_calls;
+        st = fa_fwd_splitkv_noalloc(a, a, a, out, lse, 1, 16, 8, 1, 32768, 128, 0.088f, 32767, 1, 0, nullptr, nullptr,
+                                    0, 0, 0, 0, FA_DTYPE_BF16, nullptr);
+        if (st != FA_OK || fa::g_calls != c + 1 || fa::g_last.Tk != 32768) {
+            std::printf("no-alloc decode step: status %d, %s\n", (int)st, fa_last_error());
             ++bad;
         }
     }
