@@ -1212,12 +1212,14 @@ cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
     // (the K/V ring fills it) keeps a second CTA off the SM.
     constexpr size_t kSmem = SmemLayout<D, MODE>::kTotal + 1024;
     static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "shared memory budget");
-    static bool configured = false;
-    if (!configured) {
+    static DeviceOnce configured;
+    int dev = -1;
+    if (!configured.done(dev)) {
+        if (dev < 0) return cudaErrorInvalidDevice;
         cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.mark(dev);
     }
     // One CTA per SM, no more than there are units (a test may cap the grid).
     const int nqt = (P.Tq + kBM - 1) / kBM;
@@ -1283,8 +1285,11 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     auto kernel = fa_fwd_bf16_kernel<D, MODE>;
     constexpr int kMaxSplits = 16;
-    static bool configured = false;
-    static int capacity[kMaxSplits + 1] = {};  // clusters of s CTAs resident at once
+    static DeviceOnce configured;
+    static int capacity[64][kMaxSplits + 1] = {};  // per device: clusters of s CTAs resident at once
+    int dev = -1;
+    const bool have = configured.done(dev);
+    if (dev < 0) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
@@ -1297,7 +1302,7 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (!configured) {
+    if (!have) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -1309,16 +1314,16 @@ cudaError_t launch_packed(const Params &P0, cudaStream_t stream) {
                 (void)cudaGetLastError();
                 clusters = 0;
             }
-            capacity[sp] = clusters;
+            capacity[dev][sp] = clusters;
         }
-        if (capacity[1] <= 0) return cudaErrorInvalidConfiguration;
-        configured = true;
+        if (capacity[dev][1] <= 0) return cudaErrorInvalidConfiguration;
+        configured.mark(dev);
     }
     const int units = P.B * P.Hkv;
     int S = 1;
     if (n >= 4)
         for (int sp = n / 2 < kMaxSplits ? n / 2 : kMaxSplits; sp > 1; --sp)
-            if (capacity[sp] >= units) {
+            if (capacity[dev][sp] >= units) {
                 S = sp;
                 break;
             }
@@ -1378,11 +1383,13 @@ cudaError_t launch_splitkv_d(const Params &P0, void *workspace, cudaStream_t str
     static_assert((3 * kMaxSplitsWs + 2) * kBM * 4 <= 2 * SmemLayout<D, MODE>::kStages * SmemLayout<D, MODE>::kKVBytes,
                   "the merge's per-row weights fit the K/V rings");
     auto kernel = fa_fwd_bf16_kernel<D, MODE>;
-    static bool configured = false;
-    if (!configured) {
+    static DeviceOnce configured;
+    int dev = -1;
+    if (!configured.done(dev)) {
+        if (dev < 0) return cudaErrorInvalidDevice;
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.mark(dev);
     }
     const int units = P.B * P.Hkv;
     const int sms = sm_count();

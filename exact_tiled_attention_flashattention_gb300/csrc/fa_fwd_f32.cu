@@ -297,12 +297,14 @@ template <int DT, bool VARLEN>
 cudaError_t launch_dt(const Params &P, cudaStream_t stream) {
     constexpr int LD = DT + 4;
     const size_t smem = (size_t)(kBr * LD + 2 * kBc * LD + kBc * kPLd) * sizeof(float);
-    static bool configured = false;  // one attribute call per instantiation
-    if (!configured) {
+    static DeviceOnce configured;  // one attribute call per instantiation and device
+    int dev = -1;
+    if (!configured.done(dev)) {
+        if (dev < 0) return cudaErrorInvalidDevice;
         cudaError_t e = cudaFuncSetAttribute(fa_fwd_f32_kernel<DT, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.mark(dev);
     }
     const int nqt = (P.Tq + kBr - 1) / kBr;
     const unsigned grid = (unsigned)nqt * (unsigned)(P.B * P.Hq);

@@ -713,12 +713,14 @@ cudaError_t launch_tc(const Params &P, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     constexpr size_t kSmem = C::kSmem + 1024;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static bool configured = false;
-    if (!configured) {
+    static DeviceOnce configured;
+    int dev = -1;
+    if (!configured.done(dev)) {
+        if (dev < 0) return cudaErrorInvalidDevice;
         cudaError_t e = cudaFuncSetAttribute(fa_fwd_f32tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.mark(dev);
     }
     const int nqt = (P.Tq + kBM - 1) / kBM;
     cudaLaunchConfig_t cfg = {};

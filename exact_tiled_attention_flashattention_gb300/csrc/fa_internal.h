@@ -2,6 +2,7 @@
 // Not part of the public ABI (include/fa.h is).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -95,6 +96,26 @@ cudaError_t bf16_watchdog(cudaStream_t stream, unsigned int *flag);
 cudaError_t f32tc_watchdog(cudaStream_t stream, unsigned int *flag);
 // Test hooks: make CTA 0 of the next launches skip one load (see the kernels).
 cudaError_t bf16_set_drop_arrive(int on);
+
+// Launchers set their kernels' function attributes (shared-memory size,
+// cluster sizes) once per device: the attributes belong to each device's
+// context, so a process that calls on several GPUs sets them on each.  Bit
+// `dev` records the device; devices 0..63.
+struct DeviceOnce {
+    std::atomic<unsigned long long> bits{0};
+    // The current device in `dev` (-1 if none or >= 64); true once mark(dev) ran.
+    bool done(int &dev) const {
+        dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+            dev = -1;
+            return false;
+        }
+        return ((bits.load(std::memory_order_acquire) >> dev) & 1ull) != 0;
+    }
+    void mark(int dev) {
+        if (dev >= 0 && dev < 64) bits.fetch_or(1ull << dev, std::memory_order_release);
+    }
+};
 
 // Test hook: when positive, the persistent launchers use at most this many
 // CTAs (0: one per SM).  Set through fa_test_max_ctas.
