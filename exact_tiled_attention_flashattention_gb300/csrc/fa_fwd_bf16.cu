@@ -53,7 +53,8 @@
 //
 // Launch: programmatic dependent launch lets the CTA prologue overlap the
 // previous kernel in the stream; griddepcontrol.wait orders every global
-// access after it.
+// access after it.  The producer looks up its first unit (kernel parameters
+// only) before that wait, so its first loads issue as soon as it returns.
 //
 // Every mbarrier wait is bounded (two seconds of wall time); a wait that runs
 // out sets a CTA-wide abort flag and the device watchdog word, every role
@@ -385,6 +386,20 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     using L = SmemLayout<D, MODE>;
     volatile int *abort = &bar.abort;
     const Schedule sched = make_schedule<MODE>(P);
+    // The first unit's lookup reads kernel parameters only (not with per-
+    // sequence lengths, which are device data), so it runs before the
+    // dependency wait: the first loads issue as soon as the previous grid's
+    // writes are visible.
+    constexpr bool kParamUnits = !is_varlen(MODE) && MODE != kPaged;
+    Unit first{};
+    if constexpr (kParamUnits) {
+        const int u0 = sched.unit_at(0);
+        if (u0 >= 0) first = get_unit<MODE>(P, u0);
+    }
+    // The test hook is set by the host before the launch, not by a kernel.
+    const bool drop_first_q = blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0;
+    grid_dependency_wait();
+    grid_launch_dependents();
     // Loads issued into each ring so far: a stage has a previous use once
     // the ring has wrapped (kept as counters, not per-stage arrays, so that
     // nothing here lives in local memory).
@@ -395,7 +410,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const Unit U = get_unit<MODE>(P, u);
+        const Unit U = (kParamUnits && r == 0) ? first : get_unit<MODE>(P, u);
         const int n = U.n_tiles;
         if (n == 0) continue;
 
@@ -445,7 +460,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         // Q of this unit into the Q buffer (the caller has made sure that the
         // previous unit's S MMAs are done with it).
         auto load_q = [&]() {
-            if (q_issued == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0) {
+            if (q_issued == 0 && drop_first_q) {
                 // test hook: no Q load, no arrival on q_full
             } else if constexpr (is_packed(MODE)) {
                 // [64 columns] x [group heads] x [Tq rows] boxes: group * Tq rows.
@@ -1115,18 +1130,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
     // Inputs may come from the previous kernel in the stream, and outputs may
-    // still be read by it.
-    grid_dependency_wait();
-    grid_launch_dependents();
-
-    if (warp == kWarpTma) {
-        if (lane == 0) producer_role<D, MODE>(tmQ, tmK, tmV, P, smem, bar);
-    } else if (warp == kWarpQk) {
-        if (lane == 0) qk_role<D, MODE>(P, smem, bar, tbase);
-    } else if (warp == kWarpPv) {
-        if (lane == 0) pv_role<D, MODE>(P, smem, bar, tbase);
+    // still be read by it: every thread passes the dependency wait before its
+    // first global access (the producer inside its role, after the first
+    // unit's lookup).
+    if (warp == kWarpTma && lane == 0) {
+        producer_role<D, MODE>(tmQ, tmK, tmV, P, smem, bar);
     } else {
-        softmax_role<D, MODE>(tmO, P, smem, bar, tbase, warp, lane);
+        grid_dependency_wait();
+        grid_launch_dependents();
+        if (warp == kWarpQk) {
+            if (lane == 0) qk_role<D, MODE>(P, smem, bar, tbase);
+        } else if (warp == kWarpPv) {
+            if (lane == 0) pv_role<D, MODE>(P, smem, bar, tbase);
+        } else if (warp != kWarpTma) {
+            softmax_role<D, MODE>(tmO, P, smem, bar, tbase, warp, lane);
+        }
     }
 
     tc_fence_before();

@@ -54,6 +54,11 @@ __device__ __forceinline__ void cp_async8(void *smem, const void *gmem, int src_
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 
+// Programmatic dependent launch: wait for the previous grid in the stream
+// (its writes visible), and let the next grid start launching.
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
@@ -115,6 +120,11 @@ __global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
     // positions, with its rows and keys starting at tensor rows qrow / krow.
     int Tq = P.Tq, Tk = P.Tk, qoff = P.q_offset;
     int64_t qrow = 0, krow = 0;
+    // Everything above reads kernel parameters only and runs while the
+    // previous grid finishes; the call's tensors (and, in a variable-length
+    // batch, its offsets) are read after the dependency wait.
+    grid_wait();
+    grid_launch_next();
     if constexpr (VARLEN) {
         // offsets clamped into the tensors: a malformed table cannot reach outside them
         const int q0 = min(max(__ldg(P.cu_q + b), 0), P.total_q), k0 = min(max(__ldg(P.cu_k + b), 0), P.total_k);
@@ -308,8 +318,17 @@ cudaError_t launch_dt(const Params &P, cudaStream_t stream) {
     }
     const int nqt = (P.Tq + kBr - 1) / kBr;
     const unsigned grid = (unsigned)nqt * (unsigned)(P.B * P.Hq);
-    fa_fwd_f32_kernel<DT, VARLEN><<<grid, kThreads, smem, stream>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_fwd_f32_kernel<DT, VARLEN>, P);
 }
 
 }  // namespace

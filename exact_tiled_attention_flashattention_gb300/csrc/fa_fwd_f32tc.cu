@@ -169,7 +169,7 @@ __device__ __forceinline__ Unit make_unit(const Params &P) {
 // TMA producer: the raw chunks into the ring in consumption order.
 template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUtensorMap &tmV, const Unit &U,
-                                              uint8_t *smem, Barriers &bar) {
+                                              uint8_t *smem, Barriers &bar, bool drop_first) {
     using C = Cfg<D>;
     volatile int *abort = &bar.abort;
     int loads = 0;  // chunks issued: a slot has a previous use once the ring has wrapped
@@ -178,7 +178,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmK, const CUte
         if (loads >= C::kSlots && !mbar_wait(&bar.empty[p.st], p.ph ^ 1u, abort)) return false;
         uint8_t *slot = smem + C::kRing + p.st * kSlotBytes;
         const int key0 = (U.t_begin + t) * kBN;
-        if (loads == 0 && blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive_tc) != 0) {
+        if (loads == 0 && drop_first) {
             // test hook: no load, no arrival on full
         } else if (!is_v) {
             mbar_arrive_expect_tx(&bar.full[p.st], kBN * 128);
@@ -635,12 +635,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = bar.tmem_base;
+    // The unit's lookup reads kernel parameters only, and the test hook is
+    // set by the host before the launch: both before the dependency wait,
+    // which orders every access to the call's tensors after the previous
+    // grid's writes.
+    const Unit U = make_unit(P);
+    const bool drop_first = warp == kWarpTma && lane == 0 && blockIdx.x == 0 &&
+                            *static_cast<volatile int *>(&g_drop_arrive_tc) != 0;
     grid_dependency_wait();
     grid_launch_dependents();
-    const Unit U = make_unit(P);
 
     if (warp == kWarpTma) {
-        if (lane == 0) producer_role<D>(tmK, tmV, U, smem, bar);
+        if (lane == 0) producer_role<D>(tmK, tmV, U, smem, bar, drop_first);
     } else if (warp == kWarpMma) {
         if (lane == 0) mma_role<D>(U, smem, bar, tbase);
     } else if (warp >= kWarpSplit) {
