@@ -95,8 +95,11 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, int row
     }
 }
 
+// Registers: at d >= 128 shared memory holds one CTA per SM, so the kernel
+// declares one resident CTA and the compiler may use what it needs (no
+// spills); smaller d keeps the compiler's own choice.
 template <int DT, bool VARLEN>
-__global__ void __launch_bounds__(kThreads) fa_fwd_f32_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreads, DT >= 128 ? 1 : 0) fa_fwd_f32_kernel(const Params P) {
     constexpr int LD = DT + 4;
     constexpr int NC = DT / 32;  // float2 column pairs per thread
     extern __shared__ float4 smem_f4[];
