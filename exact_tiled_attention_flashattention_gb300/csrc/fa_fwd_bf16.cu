@@ -86,6 +86,16 @@ constexpr int kBN = 128;  // keys per tile
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 352;
 constexpr int kWarpTma = 8, kWarpQk = 9, kWarpPv = 10;
+// Prefill mappings add an idle warp 11, so that warps 8-11 form a whole
+// warpgroup: it gives registers back (setmaxnreg) and the two softmax
+// warpgroups take them, so the softmax keeps every value in registers.
+// 384 threads x 168 at launch (three warps per scheduler partition);
+// softmax 2 x 128 x 216 + issuers 128 x 64 <= 384 x 168.
+constexpr int kThreadsPrefill = 384;
+constexpr int kRegsLaunchPrefill = 168, kRegsSoftmaxPrefill = 216, kRegsIssuePrefill = 64;
+static_assert(256 * kRegsSoftmaxPrefill + 128 * kRegsIssuePrefill <= kThreadsPrefill * kRegsLaunchPrefill,
+              "the register split fits the launch allocation");
+static_assert(2 * kRegsSoftmaxPrefill + kRegsIssuePrefill <= 512, "per scheduler partition: two softmax warps and one issuer");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;                                                     // S (and P) buffers
 __host__ __device__ constexpr uint32_t col_s(int buf) { return 128u * buf; }  // S_0, S_1, S_2
@@ -128,6 +138,7 @@ __host__ __device__ constexpr bool is_varlen(int mode) { return mode == kVarlen 
 __host__ __device__ constexpr int elem_bytes(int mode) {  // Q, K, V
     return (mode == kPrefill8 || mode == kVarlen8) ? 1 : 2;
 }
+__host__ __device__ constexpr int threads_for(int mode) { return is_prefill(mode) ? kThreadsPrefill : kThreads; }
 
 template <int D, int MODE>
 struct SmemLayout {
@@ -1083,7 +1094,7 @@ __device__ __forceinline__ void merge_partials_ws(const Params &P, uint8_t *smem
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(MODE), 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                        const Params P) {
@@ -1133,18 +1144,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // still be read by it: every thread passes the dependency wait before its
     // first global access (the producer inside its role, after the first
     // unit's lookup).
-    if (warp == kWarpTma && lane == 0) {
-        producer_role<D, MODE>(tmQ, tmK, tmV, P, smem, bar);
+    if (warp >= kWarpTma) {  // warps 8-10 issue (one lane each); warp 11 (prefill) idles
+        if constexpr (is_prefill(MODE)) regs_decrease<kRegsIssuePrefill>();
+        if (warp == kWarpTma && lane == 0) {
+            producer_role<D, MODE>(tmQ, tmK, tmV, P, smem, bar);
+        } else {
+            grid_dependency_wait();
+            grid_launch_dependents();
+            if (warp == kWarpQk) {
+                if (lane == 0) qk_role<D, MODE>(P, smem, bar, tbase);
+            } else if (warp == kWarpPv) {
+                if (lane == 0) pv_role<D, MODE>(P, smem, bar, tbase);
+            }
+        }
     } else {
+        if constexpr (is_prefill(MODE)) regs_increase<kRegsSoftmaxPrefill>();
         grid_dependency_wait();
         grid_launch_dependents();
-        if (warp == kWarpQk) {
-            if (lane == 0) qk_role<D, MODE>(P, smem, bar, tbase);
-        } else if (warp == kWarpPv) {
-            if (lane == 0) pv_role<D, MODE>(P, smem, bar, tbase);
-        } else if (warp != kWarpTma) {
-            softmax_role<D, MODE>(tmO, P, smem, bar, tbase, warp, lane);
-        }
+        softmax_role<D, MODE>(tmO, P, smem, bar, tbase, warp, lane);
     }
 
     tc_fence_before();
@@ -1237,6 +1254,15 @@ cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
+        if constexpr (is_prefill(MODE)) {
+            // The warpgroups' register shares come from what the CTA was
+            // launched with; with fewer, the softmax warps' increase could
+            // never be granted.  Refuse a build that differs.
+            cudaFuncAttributes fattr{};
+            e = cudaFuncGetAttributes(&fattr, fa_fwd_bf16_kernel<D, MODE>);
+            if (e != cudaSuccess) return e;
+            if (fattr.numRegs != kRegsLaunchPrefill) return cudaErrorInvalidKernelImage;
+        }
         configured.mark(dev);
     }
     // One CTA per SM, no more than there are units (a test may cap the grid).
@@ -1248,7 +1274,7 @@ cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
     if (g_test_max_ctas > 0 && grid > g_test_max_ctas) grid = g_test_max_ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_for(MODE));
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
