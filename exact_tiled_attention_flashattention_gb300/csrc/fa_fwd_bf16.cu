@@ -37,12 +37,14 @@
 // Every CTA loads its own tiles (no cluster multicast): the K/V tiles a GQA
 // group shares come from L2.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads in prefill, 352 for the other mappings):
 //   warps 0-7   softmax and epilogue: two threads per query row (= TMEM
 //               lane), each with half of the row's keys and of O's columns
 //   warp 8      TMA producer (one lane)
 //   warp 9      S = Q K^T issuer (one lane) and tensor-memory owner
 //   warp 10     O += P V issuer (one lane)
+//   warp 11     prefill only, idle: it completes warps 8-11 as a warpgroup,
+//               which gives registers to the softmax warpgroups
 // Tensor memory (512 columns allocated): S_0 [0,128) S_1 [128,256)
 // S_2 [256,384) O [384, 384+d).
 //
