@@ -491,12 +491,19 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             }
             ++q_issued;
         };
+        int k_next = 2;  // the unit's next K tile to load
         if (q_issued == 0) {
             // The CTA's first unit: Q first, as its first S needs Q and K_0
-            // and all three come from DRAM.
+            // and all three come from DRAM.  A short unit (up to 16 key
+            // tiles) also sends K_2 out before V_0, which is needed only
+            // after the first softmax: its S chain is its critical path.
             load_q();
             if (!(ok = load_k(0))) break;
             if (n > 1 && !(ok = load_k(1))) break;
+            if (n > 2 && n <= 16 && L::kStages >= 3) {
+                if (!(ok = load_k(2))) break;
+                k_next = 3;
+            }
         } else {
             // K_0 and K_1 first: Q waits for the previous unit's last S.
             if (!(ok = load_k(0))) break;
@@ -506,7 +513,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         }
         for (int j = 0; j < n && ok; ++j) {
             ok = load_v(j);
-            if (ok && j + 2 < n) ok = load_k(j + 2);
+            if (ok && j + 2 < n && j + 2 >= k_next) ok = load_k(j + 2);
         }
     }
     if (*abort) {
