@@ -837,14 +837,19 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 } else {
                     pk[e / 2] = cvt_bf16x2(p0.x, p0.y);
                     pk[e / 2 + 1] = cvt_bf16x2(p1.x, p1.y);
+                    // bf16: the first 32 keys' P goes out while the rest
+                    // are computed; one wait below covers both stores.
+                    if (e + 4 == kHK / 2) tmem_store_pair16_nowait<kHK / 2>(s_addr, pk);
                 }
             }
             // P of keys [64 h, 64 h + 64) into columns [32 h, 32 h + 32) (bf16)
             // or [16 h, 16 h + 16) (e4m3) of the buffer.
-            if constexpr (kPerWord == 4)
+            if constexpr (kPerWord == 4) {
                 tmem_store_pair16<kHK / 4>(s_addr, pk);
-            else
-                tmem_store_pair32<kHK / 2>(s_addr, pk);
+            } else {
+                tmem_store_pair16_nowait<kHK / 2>(s_addr + 16, pk + 16);
+                tmem_wait_st();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.p_full[b]);  // one arrival per warp

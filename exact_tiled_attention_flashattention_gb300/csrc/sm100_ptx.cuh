@@ -561,6 +561,19 @@ __device__ __forceinline__ void tmem_store_pair16(uint32_t taddr, const uint32_t
         : "memory");
 }
 
+// The same store without its completion wait: the thread issues
+// tmem_wait_st() before anything that relies on the stored values.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_store_pair16_nowait(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17};\n" ::"r"(taddr),
+        "n"(SPLIT), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <int SPLIT>
 __device__ __forceinline__ void tmem_store_pair32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
