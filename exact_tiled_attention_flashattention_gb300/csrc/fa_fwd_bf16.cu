@@ -729,7 +729,8 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 const int k0 = (U.t_begin + j) * kBN + half * kHK;  // this thread's first key
                 // The row's visible keys among this thread's: [elo, ehi) (clamped).
                 const int elo = min(max(vlo - k0, 0), kHK), ehi = min(max(vhi - k0, 0), kHK);
-                auto visible = [&](int e) { return e >= elo && e < ehi; };
+                const KeyBits kb = key_bits(elo, ehi);
+                auto visible = [&](int e) { return kb.has(e); };
                 if (mrow != nullptr) {
                     // Additive mask: scores in log2 units; keys past Tk read a
                     // clamped (valid) address and are dropped by the interval.

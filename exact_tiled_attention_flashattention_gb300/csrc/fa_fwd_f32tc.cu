@@ -383,6 +383,7 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, uin
                                              uint32_t tbase, int warp, int lane) {
     using C = Cfg<D>;
     constexpr int kHK = kBN / 2;  // keys per thread
+    static_assert(kHK <= 64, "a thread's visible keys fit one KeyBits");
     constexpr int kHD = D / 2;    // columns of Q / O per thread
     volatile int *abort = &bar.abort;
     const int half = lane >> 4;
@@ -498,8 +499,10 @@ __device__ __forceinline__ void softmax_role(const Params &P, const Unit &U, uin
                 for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] * c : -INFINITY;
                 cs = 1.f;
             } else {
+                // keys outside the row's interval drop to -inf, tested as bits
+                const KeyBits kb = key_bits(elo, ehi);
 #pragma unroll
-                for (int e = 0; e < kHK; ++e) s[e] = (e >= elo && e < ehi) ? s[e] : -INFINITY;
+                for (int e = 0; e < kHK; ++e) s[e] = kb.has(e) ? s[e] : -INFINITY;
             }
         }
         float bm;

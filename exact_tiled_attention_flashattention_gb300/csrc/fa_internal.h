@@ -65,6 +65,21 @@ __host__ __device__ inline void visible_range(const Params &P, int64_t p, int64_
     visible_range_tk(P, (int64_t)P.Tk, p, lo, hi);
 }
 
+// A thread's visible keys among its (at most 64) keys of a tile, the interval
+// [elo, ehi) with 0 <= elo, ehi <= 64, as a bit mask: key e is visible iff
+// bit e is set (none when ehi <= elo).  On a boundary tile the kernels test
+// one constant bit per key instead of comparing e with both ends.
+struct KeyBits {
+    uint32_t lo, hi;  // keys 0-31, 32-63
+    __host__ __device__ bool has(int e) const { return ((e < 32 ? lo : hi) & (1u << (e & 31))) != 0u; }
+};
+__host__ __device__ inline KeyBits key_bits(int elo, int ehi) {
+    const uint64_t below_hi = ehi >= 64 ? ~0ull : (1ull << ehi) - 1ull;
+    const uint64_t below_lo = elo >= 64 ? ~0ull : (1ull << elo) - 1ull;
+    const uint64_t v = below_hi & ~below_lo;
+    return KeyBits{(uint32_t)v, (uint32_t)(v >> 32)};
+}
+
 cudaError_t launch_f32(const Params &P, cudaStream_t stream);
 // fp32 with three TF32 tensor-core products per matrix product.
 cudaError_t launch_f32_tc(const Params &P, cudaStream_t stream);

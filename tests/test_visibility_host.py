@@ -8,7 +8,9 @@ forward in C" (section 2.1) applied key by key: j is visible from position p
 iff j < Tk, (not causal or j <= p) and (w <= 0 or j > p - w).  Also checked:
 the interval moves monotonically with p, so the keys of a 128-row query tile
 are exactly the keys from its first row's lo to its last row's hi, which is
-the range the kernels walk.
+the range the kernels walk.  And the bit mask of a thread's interval
+among its 64 keys of a tile (``key_bits``), which the kernels test on
+boundary tiles, against the interval itself.
 """
 from __future__ import annotations
 
@@ -103,6 +105,18 @@ int main() {
             if (bad++ < 5) std::printf("the last row's hi is not the largest\n");
         }
     }
+    // The boundary tiles' bit form of a thread's interval [elo, ehi) of its
+    // 64 keys: every interval, every key.
+    for (int elo = 0; elo <= 64; ++elo)
+        for (int ehi = 0; ehi <= 64; ++ehi) {
+            const fa::KeyBits kb = fa::key_bits(elo, ehi);
+            for (int e = 0; e < 64; ++e) {
+                ++checked;
+                if (kb.has(e) != (e >= elo && e < ehi)) {
+                    if (bad++ < 5) std::printf("key bit %d of [%d, %d)\n", e, elo, ehi);
+                }
+            }
+        }
     std::printf("checked %ld, failures %ld\n", checked, bad);
     return bad == 0 ? 0 : 1;
 }
