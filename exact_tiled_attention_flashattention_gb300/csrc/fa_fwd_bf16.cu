@@ -633,6 +633,9 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
     constexpr int kHK = kBN / 2;  // keys per thread per tile
     constexpr int kHD = D / 2;    // O columns per thread
     static_assert(kHD == 32 || kHD == 64, "a thread's O columns fill half or all of a 64-column box");
+    // Prefill-like mappings bound a boundary tile's maximum by the load's
+    // (packed rows, whose tiles are nearly all interior, keep the registers).
+    constexpr bool kBoundByLoad = !is_packed(MODE);
     volatile int *abort = &bar.abort;
     const Schedule sched = make_schedule<MODE>(P);
     const int half = lane >> 4;
@@ -714,11 +717,12 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[b], sb.ph, abort)))) break;
             tc_fence_after();
             uint32_t sr[kHK];
-            // Interior tiles take the maximum of the thread's raw scores from
-            // the load itself; boundary tiles mask first and reduce below.
+            // The load also gives the maximum of the thread's raw scores: the
+            // row maximum of an interior tile, and a bound on a boundary
+            // tile's (masked) one.
             const bool interior = j >= ti_lo && j < ti_hi;  // warp-uniform
             float raw_max = 0.f;
-            if (interior)
+            if (kBoundByLoad || interior)
                 raw_max = tmem_load_pair64_max<kHK>(s_addr, sr);
             else
                 tmem_load_pair64<kHK>(s_addr, sr);
@@ -775,18 +779,34 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap &tmO, const Param
                 bm = raw_max * cs;
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));  // the row's other half
             } else {
-                static_assert(kHK == 64, "max chains assume 64 keys per thread");
-                float mx[8];  // eight independent chains of three-input max
+                // Without an additive mask (and with c > 0) the masked maximum
+                // is at most the raw one times c.  When that bound cannot move
+                // m past the threshold below, neither can the masked maximum,
+                // and m stays as it would have: the maximum is not needed.
+                bool exact = true;
+                if constexpr (kBoundByLoad) {
+                    // every lane shuffles (mrow differs between rows); the
+                    // two lanes of a row share mrow and so the outcome
+                    float ub = raw_max * c;
+                    ub = fmaxf(ub, __shfl_xor_sync(0xffffffffu, ub, 16));
+                    exact = mrow != nullptr || c <= 0.f || ub > m + kRescaleThreshold;
+                }
+                if (!kBoundByLoad || __any_sync(0xffffffffu, exact)) {
+                    static_assert(kHK == 64, "max chains assume 64 keys per thread");
+                    float mx[8];  // eight independent chains of three-input max
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);  // keys 0..23
+                    for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(s[c8], s[8 + c8], s[16 + c8]);  // keys 0..23
 #pragma unroll
-                for (int e = 24; e < 56; e += 16)  // keys 24..55
+                    for (int e = 24; e < 56; e += 16)  // keys 24..55
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
+                        for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmax3(mx[c8], s[e + c8], s[e + 8 + c8]);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[56 + c8]);  // keys 56..63
-                bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
-                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));  // the row's other half
+                    for (int c8 = 0; c8 < 8; ++c8) mx[c8] = fmaxf(mx[c8], s[56 + c8]);  // keys 56..63
+                    bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * cs;
+                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));  // the row's other half
+                } else {
+                    bm = -INFINITY;  // at most m + threshold: m stays
+                }
             }
 
             // Lazy max: move m only when the tile exceeds it by the threshold
