@@ -105,6 +105,7 @@ constexpr uint32_t kColO = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: weights stay below 2^8
+constexpr int kPrefetchTiles = 4;          // K and V tiles of the first unit requested into L2 early
 constexpr uint32_t kSwRowBytes = 128;      // one swizzled row: 64 bf16
 constexpr int kMaxStages = 6;
 
@@ -408,6 +409,27 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     if constexpr (kParamUnits) {
         const int u0 = sched.unit_at(0);
         if (u0 >= 0) first = get_unit<MODE>(P, u0);
+    }
+    // With half the SMs or more left free, a call's CTAs start while the
+    // previous grid still runs (programmatic dependent launch) and then wait
+    // for it; meanwhile the first unit's Q and first K and V tiles are
+    // requested into L2, so that its first loads after the wait hit there.
+    // A prefetch changes no value: data the previous grid writes later
+    // replaces what L2 holds.
+    if constexpr (is_prefill(MODE)) {
+        if (P.prefetch_l2 && first.n_tiles > 0) {
+#pragma unroll
+            for (int c = 0; c < L::kBoxes; ++c) tma_prefetch_l2_4d(&tmQ, c * L::kBoxCols, first.r0, first.h, first.b);
+            const int nt = first.n_tiles < kPrefetchTiles ? first.n_tiles : kPrefetchTiles;
+            for (int t = 0; t < nt; ++t) {
+                const int key0 = (first.t_begin + t) * kBN;
+#pragma unroll
+                for (int c = 0; c < L::kBoxes; ++c) {
+                    tma_prefetch_l2_4d(&tmK, c * L::kBoxCols, key0, first.g, first.b);
+                    tma_prefetch_l2_4d(&tmV, c * L::kBoxCols, key0, first.g, first.b);
+                }
+            }
+        }
     }
     // The test hook is set by the host before the launch, not by a kernel.
     const bool drop_first_q = blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0;
@@ -1307,6 +1329,9 @@ cudaError_t launch_d(const Params &P0, cudaStream_t stream) {
     if (sms <= 0) return cudaErrorInvalidDevice;
     long long grid = units < sms ? units : sms;
     if (g_test_max_ctas > 0 && grid > g_test_max_ctas) grid = g_test_max_ctas;
+    // A grid on at most half the SMs leaves room for the next call's CTAs
+    // to start early, so its first tiles are worth requesting into L2.
+    if constexpr (is_prefill(MODE)) P.prefetch_l2 = 2 * grid <= sms ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(threads_for(MODE));

@@ -26,6 +26,8 @@ struct Params {
     float scale;          // scale applied to q.k
     float scale_log2;     // scale * log2(e)
     int splits;           // bf16 packed-row path: CTAs that split a key range (set by its launcher)
+    int prefetch_l2;      // bf16 prefill: request the first unit's tiles into L2 before the
+                          // dependency wait (set by its launcher)
     // Element strides of q, k, v, o: batch, head, row (the d elements of a
     // row are contiguous).
     int64_t q_sb, q_sh, q_st, k_sb, k_sh, k_st, v_sb, v_sh, v_st, o_sb, o_sh, o_st;
