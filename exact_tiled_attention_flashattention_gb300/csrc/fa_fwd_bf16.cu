@@ -142,6 +142,14 @@ __host__ __device__ constexpr int elem_bytes(int mode) {  // Q, K, V
     return (mode == kPrefill8 || mode == kVarlen8) ? 1 : 2;
 }
 __host__ __device__ constexpr int threads_for(int mode) { return is_prefill(mode) ? kThreadsPrefill : kThreads; }
+// bf16 prefill with d = 128 (two 64-column boxes per tile) issues the CTA's
+// first S in two halves of d: the first four MMAs need only box 0 of Q and
+// K_0, which land on a barrier of their own, while box 1 is still in flight.
+// The MMAs and their order are unchanged.
+template <int D, int MODE>
+__host__ __device__ constexpr bool split_first_s() {
+    return is_prefill(MODE) && elem_bytes(MODE) == 2 && D == 128;
+}
 
 template <int D, int MODE>
 struct SmemLayout {
@@ -183,6 +191,7 @@ struct Barriers {
     uint64_t ep_free;                                  // the O staging tile may be written
     uint64_t ep_full;                                  // the O staging tile is written
     uint64_t drain[2];                                 // issuers' last MMAs completed
+    uint64_t first_lo;  // column box 0 of the CTA's first Q and K_0 landed (first S in halves)
     uint32_t tmem_base;
     int abort;
     int last;  // split-KV through the workspace: this CTA merges its KV head
@@ -345,13 +354,15 @@ __device__ __forceinline__ Desc make_desc(uint32_t saddr, uint32_t lbo, uint32_t
 // S = Q K^T over d in 32-byte K steps: D/16 MMAs of 128 x 128 x 16 (bf16) or
 // D/32 of 128 x 128 x 32 (e4m3).  Q and K are K-major with the 128-byte
 // swizzle: a step advances 32 bytes inside a 128-byte box row, and every
-// fourth step jumps to the next box.
-template <int D, int MODE>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, Desc q, Desc k) {
+// fourth step jumps to the next box.  issue_qk_steps issues steps [K0, K1)
+// (step 0 overwrites the accumulator), so that S can be issued in two halves
+// of d.
+template <int D, int MODE, int K0, int K1>
+__device__ __forceinline__ void issue_qk_steps(uint32_t d_tmem, Desc q, Desc k) {
     constexpr bool kF8 = elem_bytes(MODE) == 1;
     constexpr uint32_t kId = kF8 ? idesc_e4m3_f32(kBM, kBN, 0, 0) : idesc_bf16_f32(kBM, kBN, 0, 0);
 #pragma unroll
-    for (int kk = 0; kk < D * elem_bytes(MODE) / 32; ++kk) {
+    for (int kk = K0; kk < K1; ++kk) {
         const uint32_t oq = ((kk >> 2) * (kBM * kSwRowBytes) + (kk & 3) * 32) >> 4;
         const uint32_t ok = ((kk >> 2) * (kBN * kSwRowBytes) + (kk & 3) * 32) >> 4;
         if constexpr (kF8) {
@@ -366,6 +377,11 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, Desc q, Desc k) {
                 mma_ss_c<1>(d_tmem, q.lo + oq, q.hi, k.lo + ok, k.hi, kId);
         }
     }
+}
+
+template <int D, int MODE>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, Desc q, Desc k) {
+    issue_qk_steps<D, MODE, 0, D * elem_bytes(MODE) / 32>(d_tmem, q, k);
 }
 
 // O += P V over the 128 keys of a tile, 32 bytes of keys per step: 8 MMAs of
@@ -442,6 +458,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
     int q_issued = 0;
     RingPos kput, vput;
     bool ok = true;
+    bool first_split = false;  // the first S's box-0 loads went to first_lo
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
@@ -519,8 +536,31 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
             // and all three come from DRAM.  A short unit (up to 16 key
             // tiles) also sends K_2 out before V_0, which is needed only
             // after the first softmax: its S chain is its critical path.
-            load_q();
-            if (!(ok = load_k(0))) break;
+            if constexpr (split_first_s<D, MODE>()) {
+              if (!drop_first_q) {
+                // Column box 0 of Q and K_0 on first_lo, box 1 on the usual
+                // barriers (stage 0 of the K ring, never used before).
+                constexpr uint32_t kBox = kBM * kSwRowBytes;
+                static_assert(kBN == kBM && L::kBoxes == 2 && L::kQBytes == 2 * kBox && L::kKVBytes == 2 * kBox,
+                              "two boxes per Q and K tile");
+                const int key0 = U.t_begin * kBN;
+                mbar_arrive_expect_tx(&bar.first_lo, 2 * kBox);
+                mbar_arrive_expect_tx(&bar.q_full, kBox);
+                mbar_arrive_expect_tx(&bar.k_full[0], kBox);
+                tma_load_4d(smem + L::kQ, &tmQ, &bar.first_lo, 0, U.r0, U.h, U.b);
+                tma_load_4d(smem + L::kKRing, &tmK, &bar.first_lo, 0, key0, U.g, U.b);
+                tma_load_4d(smem + L::kQ + kBox, &tmQ, &bar.q_full, L::kBoxCols, U.r0, U.h, U.b);
+                tma_load_4d(smem + L::kKRing + kBox, &tmK, &bar.k_full[0], L::kBoxCols, key0, U.g, U.b);
+                ++q_issued;
+                ++k_loads;
+                kput.st = 1;  // stage 0 taken (kStages >= 2)
+                first_split = true;
+              }
+            }
+            if (!first_split) {
+                load_q();
+                if (!(ok = load_k(0))) break;
+            }
             if (n > 1 && !(ok = load_k(1))) break;
             if (n > 2 && n <= 16 && L::kStages >= 3) {
                 if (!(ok = load_k(2))) break;
@@ -542,6 +582,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap &tmQ, const CUte
         // Drain: every copy issued above lands before shared memory goes away.
         int never = 0;
         if (q_issued > 0) mbar_wait(&bar.q_full, (q_issued - 1) & 1, &never, 200000000ull);
+        if (first_split) mbar_wait(&bar.first_lo, 0, &never, 200000000ull);
         // Stage s of a ring of S stages after n loads was used (n + S - 1 - s) / S times.
         for (int s = 0; s < L::kStages; ++s) {
             const int ku = (k_loads + L::kStages - 1 - s) / L::kStages;
@@ -579,19 +620,35 @@ __device__ __forceinline__ void qk_role(const Params &P, uint8_t *smem, Barriers
     bool first_use = true;   // no buffer has been used yet on this pass
     int units = 0;           // non-empty units before this one
     bool ok = true;
+    // The producer splits the first S's loads unless the test hook drops
+    // that Q (the same host-set value it reads).
+    const bool first_split =
+        split_first_s<D, MODE>() && !(blockIdx.x == 0 && *static_cast<volatile int *>(&g_drop_arrive) != 0);
+    constexpr int kSteps = D * elem_bytes(MODE) / 32;
     for (int r = 0; ok; ++r) {
         const int u = sched.unit_at(r);
         if (u < 0) break;
-        const int n = get_unit<MODE>(P, u).n_tiles;  // the same for both CTAs of a pair
+        const int n = get_unit<MODE>(P, u).n_tiles;
         if (n == 0) continue;
-        if (!(ok = mbar_wait(&bar.q_full, units & 1, abort))) break;
+        const bool halves = first_split && units == 0;  // this unit's first S in two halves
+        if (!halves && !(ok = mbar_wait(&bar.q_full, units & 1, abort))) break;
         for (int j = 0; j < n; ++j) {
             const int b = sb.st;
+            if (halves && j == 0) {
+                if (!(ok = mbar_wait(&bar.first_lo, 0, abort))) break;
+                tc_fence_after();
+                issue_qk_steps<D, MODE, 0, kSteps / 2>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
+                if (!(ok = mbar_wait(&bar.q_full, 0, abort))) break;
+            }
             if (!(ok = mbar_wait(&bar.k_full[take.st], take.ph, abort))) break;
             // the buffer's previous use: O += P V from it completed
             if (!first_use && !(ok = mbar_wait(&bar.o_done[b], sb.ph ^ 1u, abort))) break;
             tc_fence_after();
-            issue_qk<D, MODE>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
+            if (halves && j == 0)
+                issue_qk_steps<D, MODE, kSteps / 2, kSteps>(tbase + col_s(b), qd,
+                                                             Desc{k0.lo + take.st * kTileUnits, k0.hi});
+            else
+                issue_qk<D, MODE>(tbase + col_s(b), qd, Desc{k0.lo + take.st * kTileUnits, k0.hi});
             mma_commit(&bar.s_full[b]);
             if (j + 1 == n) mma_commit(&bar.q_empty);  // the unit's last S is issued
             mma_commit(&bar.k_empty[take.st]);
@@ -1180,6 +1237,7 @@ __global__ void __launch_bounds__(threads_for(MODE), 1)
         mbar_init(&bar.ep_full, kSoftmaxWarps);
         mbar_init(&bar.drain[0], 1);
         mbar_init(&bar.drain[1], 1);
+        mbar_init(&bar.first_lo, 1);
         bar.abort = 0;
         mbar_init_fence();
     }
